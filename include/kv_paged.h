@@ -1,0 +1,216 @@
+/*
+ * kv_paged.h -- C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * The decode step of a serving engine over a paged KV cache:
+ *   - The cache is a single pool of equal-sized blocks, made once when the
+ *     engine starts; a per-sequence block table turns the sequence's logical
+ *     block numbers into physical block ids, which can sit anywhere in the
+ *     pool (xuewyang.github.io/posts/kv, section "PagedAttention: the KV cache
+ *     in blocks").
+ *   - In a decode step the new token's key and value are stored first; its
+ *     query then attends over all cached tokens of the sequence, itself
+ *     included (same page, section "Prefill and decode"; brunomaga.github.io
+ *     "inference-prefill-decode-roofline-cache", section "PagedAttention: memory
+ *     management for the KV cache", PagedKVCache.append and
+ *     paged_decode_attention).
+ *   - The attention kernel walks the table and reads the cache block by block,
+ *     combining per-block partial results with the online-softmax update
+ *     (learn.mohebi.ai lesson 12 "LLM inference serving", section
+ *     "PagedAttention (4.1-4.3)"); long contexts are spread over the SMs by
+ *     split-KV decoding (same lesson, section 6 "Where it shows up").
+ *
+ * Conventions common to every call:
+ *   - All array pointers are DEVICE pointers on the pool's device, owned by the
+ *     caller, except the pool's own K/V/scale memory (owned by the pool).
+ *     Tensor data (q, k_new, v_new, out, workspace) must be 16-byte aligned;
+ *     int32 / float arrays 4-byte aligned.
+ *   - The calling thread's current CUDA device must be the pool's device.
+ *   - `stream` is a cudaStream_t (NULL: the legacy default stream).  append and
+ *     decode only enqueue work: they never allocate, never synchronise and
+ *     never read device memory on the host, so they may be captured in a CUDA
+ *     graph.  Their results are ready when the stream reaches them.
+ *   - Errors detectable on the host (shapes, pointers, alignment, sizes) are
+ *     returned before anything is launched.  Values that live on the device
+ *     (block ids, context lengths, sequence indices) are checked by the
+ *     kernels: a bad entry is skipped or clamped, never dereferenced, and a
+ *     bit is set in the pool's device error word (kv_pool_device_errors).
+ *   - No call aborts the process and no C++ exception crosses this ABI.
+ */
+#ifndef KV_PAGED_H
+#define KV_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV_PAGED_ABI_VERSION 1
+
+typedef enum kv_status {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,     /* a host-checkable argument is wrong; nothing was launched */
+    KV_ERR_OUT_OF_MEMORY = 2,   /* the pool allocation failed */
+    KV_ERR_OUT_OF_BLOCKS = 3,   /* reserved for a host block allocator (no free block left) */
+    KV_ERR_UNSUPPORTED = 4,     /* valid but not implemented (head_dim, block_size, dtype combo) */
+    KV_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
+    KV_ERR_DEVICE_CHECK = 6     /* kv_pool_device_errors found device-side error bits */
+} kv_status;
+
+typedef enum kv_dtype {
+    KV_DTYPE_BF16 = 0,          /* cache stores bf16 values bit for bit */
+    KV_DTYPE_FP8_E4M3 = 1       /* cache stores OCP e4m3fn codes, value = code * scale[kv_head] */
+} kv_dtype;
+
+/* Bits of the pool's device error word. */
+#define KV_DEVERR_BLOCK_ID 0x1u  /* a block-table entry outside [0, num_blocks) was skipped */
+#define KV_DEVERR_CONTEXT  0x2u  /* a context length < 0 or > max_blocks * block_size was clamped */
+#define KV_DEVERR_SEQ      0x4u  /* an appended token named a sequence outside [0, batch) */
+#define KV_DEVERR_POSITION 0x8u  /* an appended token's position was < 0 or past the table */
+#define KV_DEVERR_TIMEOUT  0x10u /* a pipeline wait gave up after its time limit (about 2 s) */
+
+typedef struct kv_pool kv_pool;  /* opaque; owned by the library */
+
+/* ABI version of the loaded library (KV_PAGED_ABI_VERSION when built). */
+int kv_abi_version(void);
+
+/* Static, never-NULL description of a status code. */
+const char* kv_status_string(kv_status status);
+
+/*
+ * kv_pool_create -- one allocation holding the K pool, the V pool, the
+ * per-kv-head fp8 scales and the device error word.  A single allocation at
+ * start-up keeps every address fixed for the life of the pool, which is what
+ * CUDA-graph capture of the step relies on (xuewyang.github.io/posts/kv,
+ * section "Why vLLM sizes the cache at startup").
+ *   K and V: [num_blocks, block_size, kv_heads, head_dim] elements each (the
+ *   vLLM per-layer layout of that page's "Reading the code" section, with K and
+ *   V as the two halves).  Token slot `s` of block `b` holds every kv head of
+ *   one token.  Initial contents: all bytes zero; fp8 scales 1.0.
+ *   Supported: block_size 16 or 32; bf16 with head_dim 64 or 128; fp8 e4m3
+ *   with head_dim 128; kv_heads >= 1; num_blocks >= 1 and the pool below 2^40
+ *   bytes.  One pool serves one layer.
+ *   device: CUDA ordinal; the pool's memory lives there.  The caller's current
+ *   device is restored before returning.
+ *   Errors: KV_ERR_INVALID_ARG (NULL out, sizes <= 0), KV_ERR_UNSUPPORTED,
+ *   KV_ERR_OUT_OF_MEMORY, KV_ERR_CUDA (no such device, tensor-map encoding).
+ *   On error *out is set to NULL.
+ */
+kv_status kv_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim,
+                         kv_dtype dtype, int device, kv_pool** out);
+
+/* Frees the pool's memory (synchronises the device first).  NULL is a no-op. */
+kv_status kv_pool_destroy(kv_pool* pool);
+
+/*
+ * Device addresses of the pool's arrays (any output pointer may be NULL):
+ * K and V pools as above, k_scale / v_scale float32 [kv_heads] (meaningful for
+ * the fp8 cache; 1.0 otherwise).  The pointers stay valid until destroy.
+ */
+kv_status kv_pool_tensors(const kv_pool* pool, void** k_pool, void** v_pool,
+                          float** k_scale, float** v_scale);
+
+/* Shape of the pool (any output pointer may be NULL). */
+kv_status kv_pool_shape(const kv_pool* pool, int* num_blocks, int* block_size, int* kv_heads,
+                        int* head_dim, kv_dtype* dtype, int* device);
+
+/*
+ * Copies per-kv-head scales from HOST arrays of kv_heads floats into the pool
+ * (synchronous; a set-up call, not part of the step).  Scales must be finite
+ * and > 0.  Either pointer may be NULL to leave that scale unchanged.
+ */
+kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_host, const float* v_scale_host);
+
+/*
+ * Reads the pool's device error word (synchronises the device).  *bits gets
+ * the KV_DEVERR_* bits raised by kernels since the last clear; clear != 0
+ * resets it.  Returns KV_ERR_DEVICE_CHECK when any bit is set, else KV_OK.
+ */
+kv_status kv_pool_device_errors(kv_pool* pool, uint32_t* bits, int clear);
+
+/*
+ * paged_kv_append -- writes the key and value of num_tokens tokens into the
+ * pool: the token at position p lands in table entry p / block_size at slot
+ * p % block_size (xuewyang.github.io/posts/kv, sections "A toy vLLM" (write_kv)
+ * and "Reading the code: a warehouse of lockers"; brunomaga.github.io,
+ * PagedKVCache.append).
+ *   k_new, v_new: bf16 [num_tokens, kv_heads, head_dim].
+ *   token_seq: int32 [num_tokens] sequence of each token, or NULL for token i
+ *     -> sequence i (then num_tokens <= batch).
+ *   token_pos: int32 [num_tokens] position of each token, or NULL for
+ *     context_lens[seq] - 1 (the decode step: context_lens counts the token
+ *     being appended).
+ *   block_tables: int32 [batch, max_blocks]; context_lens: int32 [batch]
+ *     (read only when token_pos is NULL).
+ *   Token at position p of sequence s goes to block
+ *   block_tables[s][p / block_size], slot p % block_size, for every kv head.
+ *   bf16 pools store the input bits unchanged; fp8 pools store
+ *   e4m3fn(round-to-nearest-even, saturating at +-448)(x / scale[kv_head])
+ *   with the quotient rounded to binary32 first.
+ *   Block allocation (and copy-on-write of shared blocks) is the caller's job:
+ *   the entry must already name a block the sequence owns.
+ *   Two tokens written to the same slot in one call race (either may win).
+ *   num_tokens == 0 is a no-op.
+ */
+kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, int num_tokens,
+                          const int32_t* token_seq, const int32_t* token_pos,
+                          const int32_t* block_tables, int max_blocks,
+                          const int32_t* context_lens, int batch, void* stream);
+
+/*
+ * Resolves the split-KV plan paged_decode_attention will use for these
+ * sizes: *split_tokens (a multiple of block_size) and *max_splits (the most
+ * chunks any sequence can have, ceil(max_blocks * block_size / split_tokens)).
+ * kv_split_tokens: 0 = automatic (from batch, heads, max_blocks and the SM
+ * count), else a positive multiple of block_size.  Either output may be NULL.
+ */
+kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                            int kv_split_tokens, int* split_tokens, int* max_splits);
+
+/*
+ * Bytes of device workspace paged_decode_attention needs for these sizes
+ * (fp32 partial outputs, maxima and sums of the split-KV chunks); 0 when
+ * every sequence fits one chunk.
+ */
+kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_heads,
+                                      int max_blocks, int kv_split_tokens, size_t* bytes);
+
+/*
+ * paged_decode_attention -- single-query attention for every sequence of a
+ * ragged batch, reading the cache in place through the block tables.
+ *   q: bf16 [batch, q_heads, 1, head_dim] (the new token's query).
+ *   Query head h uses kv head h / (q_heads / kv_heads): contiguous groups of
+ *   g = q_heads / kv_heads query heads share one kv head (GQA; g = 1 is MHA),
+ *   and all g heads of a group are computed from one read of that head's K/V.
+ *   block_tables: int32 [batch, max_blocks]; context_lens: int32 [batch],
+ *   counting the token appended in this step; tokens 0 .. ctx-1 of sequence b
+ *   are at block_tables[b][t / block_size], slot t % block_size.  Slots at or
+ *   past ctx in the last block are never used.  Entries past a sequence's
+ *   blocks are not read.  ctx == 0 gives out = 0 and lse = -inf.
+ *   out[b, h, :] = sum_t softmax_t(scale * q[b,h,:] . K[t, h/g, :]) V[t, h/g, :]
+ *     as bf16 [batch, q_heads, head_dim] (round to nearest even), fp32
+ *     accumulation; for the fp8 cache K and V are the dequantised values
+ *     code * scale[kv_head].
+ *   lse_out: optional float32 [batch, q_heads], natural-log log-sum-exp of the
+ *     scaled scores (NULL to skip).
+ *   kv_split_tokens: split-KV chunk in tokens (0 = automatic; else a positive
+ *     multiple of block_size).  Chunk j of a sequence covers tokens
+ *     [j * split, (j+1) * split); chunks are merged by log-sum-exp in a second
+ *     kernel.  The result does not depend on the split up to rounding.
+ *   workspace: device memory of at least paged_decode_workspace_size() bytes
+ *     (may be NULL when that size is 0); contents need no initialisation.
+ *   q_heads must be a positive multiple of the pool's kv_heads.
+ *   Concurrent calls that share a workspace on different streams race.
+ */
+kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                 const int32_t* block_tables, int max_blocks,
+                                 const int32_t* context_lens, int batch, float scale,
+                                 int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                 void* out, float* lse_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV_PAGED_H */

@@ -1,0 +1,264 @@
+"""Paged KV cache for the decode step on GB300: Python binding of libkvpaged.so.
+
+The functions mirror the C ABI in include/kv_paged.h one to one and only
+marshal arguments (torch tensors -> device pointers, the current stream).
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU path, and importing a function without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
+    "paged_decode_workspace_size", "paged_decode_attention", "library_path", "load_library",
+    "DEVERR_BLOCK_ID", "DEVERR_CONTEXT", "DEVERR_SEQ", "DEVERR_POSITION", "DEVERR_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkvpaged.so")
+
+KV_OK = 0
+KV_ERR_INVALID_ARG = 1
+KV_ERR_OUT_OF_MEMORY = 2
+KV_ERR_OUT_OF_BLOCKS = 3
+KV_ERR_UNSUPPORTED = 4
+KV_ERR_CUDA = 5
+KV_ERR_DEVICE_CHECK = 6
+DEVERR_BLOCK_ID = 0x1
+DEVERR_CONTEXT = 0x2
+DEVERR_SEQ = 0x4
+DEVERR_POSITION = 0x8
+DEVERR_TIMEOUT = 0x10
+_DTYPES = {"bf16": 0, "fp8_e4m3": 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib.kv_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libkvpaged.so (built by __graft_entry__.build()); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "kv_abi_version": ([], I),
+            "kv_status_string": ([I], ctypes.c_char_p),
+            "kv_pool_create": ([I, I, I, I, I, I, ctypes.POINTER(P)], I),
+            "kv_pool_destroy": ([P], I),
+            "kv_pool_tensors": ([P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P),
+                                 ctypes.POINTER(P)], I),
+            "kv_pool_shape": ([P] + [ctypes.POINTER(I)] * 6, I),
+            "kv_pool_set_scales": ([P, P, P], I),
+            "kv_pool_device_errors": ([P, ctypes.POINTER(ctypes.c_uint32), I], I),
+            "paged_kv_append": ([P, P, P, I, P, P, P, I, P, I, P], I),
+            "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
+            "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != KV_OK:
+        raise KVError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t, dtype, name):
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}, got "
+                         f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+    return t
+
+
+class _CudaBytes:
+    """Exposes a device byte range to torch through __cuda_array_interface__."""
+
+    def __init__(self, ptr: int, shape):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": "|u1",
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+class Pool:
+    """One layer's paged K/V pool (owned by the library)."""
+
+    def __init__(self, handle: int, num_blocks, block_size, kv_heads, head_dim, dtype, device):
+        self._h = ctypes.c_void_p(handle)
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.kv_heads, self.head_dim = kv_heads, head_dim
+        self.dtype, self.device = dtype, device
+        self.elem_bytes = 1 if dtype == "fp8_e4m3" else 2
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise RuntimeError("pool was destroyed")
+        return self._h
+
+    def tensors(self):
+        """Torch views (no copy) of the pool: K, V as raw bytes [num_blocks, bs, Hkv, d*elem]
+        viewed as bf16 or float8_e4m3fn, and the float32 scales [Hkv]."""
+        lib = load_library()
+        k, v, ks, vs = (ctypes.c_void_p() for _ in range(4))
+        _check(lib.kv_pool_tensors(self.handle, ctypes.byref(k), ctypes.byref(v), ctypes.byref(ks),
+                                   ctypes.byref(vs)), "kv_pool_tensors")
+        dev = torch.device("cuda", self.device)
+        shape = (self.num_blocks, self.block_size, self.kv_heads, self.head_dim * self.elem_bytes)
+        kt = torch.as_tensor(_CudaBytes(k.value, shape), device=dev)
+        vt = torch.as_tensor(_CudaBytes(v.value, shape), device=dev)
+        st = torch.as_tensor(_CudaBytes(ks.value, (self.kv_heads * 4,)), device=dev).view(torch.float32)
+        sv = torch.as_tensor(_CudaBytes(vs.value, (self.kv_heads * 4,)), device=dev).view(torch.float32)
+        cache = torch.float8_e4m3fn if self.dtype == "fp8_e4m3" else torch.bfloat16
+        return kt.view(cache), vt.view(cache), st, sv
+
+    def raw_bytes(self):
+        """K and V pools as uint8 views [num_blocks, bs, Hkv, d*elem]."""
+        k, v, _, _ = self.tensors()
+        return k.view(torch.uint8), v.view(torch.uint8)
+
+    def set_scales(self, k_scale=None, v_scale=None):
+        lib = load_library()
+        arr = lambda s: None if s is None else (ctypes.c_float * self.kv_heads)(*[float(x) for x in s])
+        _check(lib.kv_pool_set_scales(self.handle, arr(k_scale), arr(v_scale)), "kv_pool_set_scales")
+
+    def device_errors(self, clear: bool = True) -> int:
+        lib = load_library()
+        bits = ctypes.c_uint32(0)
+        st = lib.kv_pool_device_errors(self.handle, ctypes.byref(bits), int(clear))
+        if st not in (KV_OK, KV_ERR_DEVICE_CHECK):
+            _check(st, "kv_pool_device_errors")
+        return bits.value
+
+    def destroy(self):
+        if self._h:
+            _check(load_library().kv_pool_destroy(self._h), "kv_pool_destroy")
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            if self._h and _lib is not None:
+                _lib.kv_pool_destroy(self._h)
+                self._h = ctypes.c_void_p(None)
+        except Exception:
+            pass
+
+
+def kv_pool_create(num_blocks: int, block_size: int, kv_heads: int, head_dim: int,
+                   dtype: str = "bf16", device: int | None = None) -> Pool:
+    lib = load_library()
+    if device is None:
+        device = torch.cuda.current_device()
+    h = ctypes.c_void_p()
+    _check(lib.kv_pool_create(int(num_blocks), int(block_size), int(kv_heads), int(head_dim),
+                              _DTYPES[dtype], int(device), ctypes.byref(h)), "kv_pool_create")
+    return Pool(h.value, num_blocks, block_size, kv_heads, head_dim, dtype, device)
+
+
+def kv_pool_destroy(pool: Pool):
+    pool.destroy()
+
+
+def paged_kv_append(pool: Pool, k_new, v_new, block_tables, context_lens=None, token_seq=None,
+                    token_pos=None, stream=None):
+    """Write the key/value rows [T, Hkv, d] (bf16) of T tokens into the pool."""
+    lib = load_library()
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    _need(token_seq, torch.int32, "token_seq")
+    _need(token_pos, torch.int32, "token_pos")
+    batch, max_blocks = block_tables.shape
+    n = k_new.shape[0]
+    _check(lib.paged_kv_append(pool.handle, _ptr(k_new), _ptr(v_new), int(n), _ptr(token_seq),
+                               _ptr(token_pos), _ptr(block_tables), int(max_blocks),
+                               _ptr(context_lens), int(batch), _stream(stream)), "paged_kv_append")
+
+
+def paged_decode_plan(pool: Pool, batch: int, q_heads: int, max_blocks: int,
+                      kv_split_tokens: int = 0):
+    lib = load_library()
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(lib.paged_decode_plan(pool.handle, int(batch), int(q_heads), int(max_blocks),
+                                 int(kv_split_tokens), ctypes.byref(a), ctypes.byref(b)),
+           "paged_decode_plan")
+    return a.value, b.value
+
+
+def paged_decode_workspace_size(pool: Pool, batch: int, q_heads: int, max_blocks: int,
+                                kv_split_tokens: int = 0) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t()
+    _check(lib.paged_decode_workspace_size(pool.handle, int(batch), int(q_heads), int(max_blocks),
+                                           int(kv_split_tokens), ctypes.byref(n)),
+           "paged_decode_workspace_size")
+    return n.value
+
+
+def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: float | None = None,
+                           kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
+                           stream=None):
+    """Decode attention; q bf16 [B, Hq, 1, d] or [B, Hq, d].  Returns out (shape of q)."""
+    lib = load_library()
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    batch, q_heads = q.shape[0], q.shape[1]
+    d = q.shape[-1]
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = paged_decode_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_decode_attention(pool.handle, _ptr(q), int(q_heads), _ptr(block_tables),
+                                      int(max_blocks), _ptr(context_lens), int(batch),
+                                      float(scale), int(kv_split_tokens), _ptr(workspace),
+                                      int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
+           "paged_decode_attention")
+    return out

@@ -1,0 +1,469 @@
+// api.cu -- host layer of the C ABI: the pool object, argument validation,
+// the split-KV plan and kernel launches.  Nothing here allocates or
+// synchronises on the append / decode path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <mutex>
+#include <new>
+
+#include "kernels.h"
+#include "kv_paged.h"
+
+struct kv_pool {
+    int num_blocks, block_size, kv_heads, head_dim, device;
+    kv_dtype dtype;
+    size_t elem;            // bytes per cached element
+    size_t pool_bytes;      // bytes of the K pool (= bytes of the V pool)
+    void* base;             // the single allocation
+    uint8_t* k;
+    uint8_t* v;
+    float* k_scale;
+    float* v_scale;
+    uint32_t* err;
+    CUtensorMap tmk, tmv;   // 5-D tile maps of the K and V pools
+    int num_sms;
+};
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+bool variant_supported(kv_dtype dtype, int head_dim, int block_size)
+{
+    if (block_size != 16 && block_size != 32) return false;
+    if (dtype == KV_DTYPE_BF16) return head_dim == 64 || head_dim == 128;
+    if (dtype == KV_DTYPE_FP8_E4M3) return head_dim == 128;
+    return false;
+}
+
+// Tile map of one pool half: dims (innermost first) = 128-byte row piece,
+// pieces per token row, kv head, slot, block; a box is one block of one kv
+// head, written to shared memory with the 128-byte swizzle.
+kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return KV_ERR_CUDA;
+    const cuuint64_t row = static_cast<cuuint64_t>(p->head_dim) * p->elem;
+    const cuuint64_t per_piece = 128 / p->elem;
+    const cuuint64_t dims[5] = {per_piece, row / 128, static_cast<cuuint64_t>(p->kv_heads),
+                                static_cast<cuuint64_t>(p->block_size),
+                                static_cast<cuuint64_t>(p->num_blocks)};
+    const cuuint64_t strides[4] = {128, row, row * p->kv_heads, row * p->kv_heads * p->block_size};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(per_piece),
+                               static_cast<cuuint32_t>(row / 128), 1,
+                               static_cast<cuuint32_t>(p->block_size), 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapDataType dt = p->dtype == KV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = fn(map, dt, 5, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
+}
+
+struct Plan {
+    int group, head_tile, head_groups, split_blocks, max_splits;
+};
+
+// Split-KV plan.  Automatic choice: aim for about four waves of three resident
+// CTAs per SM over the worst case (every sequence at max_blocks), with chunks
+// of at least 32 blocks so each CTA amortises its set-up.
+kv_status make_plan(const kv_pool* pl, int batch, int q_heads, int max_blocks, int split_tokens,
+                    Plan* out)
+{
+    if (pl == nullptr || batch < 0 || q_heads <= 0 || max_blocks <= 0 || split_tokens < 0)
+        return KV_ERR_INVALID_ARG;
+    if (q_heads % pl->kv_heads != 0) return KV_ERR_INVALID_ARG;
+    if (split_tokens % pl->block_size != 0) return KV_ERR_INVALID_ARG;
+    if (static_cast<long long>(max_blocks) * pl->block_size > std::numeric_limits<int>::max())
+        return KV_ERR_INVALID_ARG;
+    Plan p;
+    p.group = q_heads / pl->kv_heads;
+    p.head_tile = kvp::head_tile_for_group(p.group);
+    p.head_groups = (p.group + p.head_tile - 1) / p.head_tile;
+    if (split_tokens > 0) {
+        p.split_blocks = split_tokens / pl->block_size;
+    } else {
+        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * pl->kv_heads *
+                                p.head_groups;
+        const long long work = units * max_blocks;
+        const long long target = static_cast<long long>(pl->num_sms > 0 ? pl->num_sms : 148) * 12;
+        long long sb = (work + target - 1) / target;
+        if (sb < 32) sb = 32;
+        if (sb > max_blocks) sb = max_blocks;
+        p.split_blocks = static_cast<int>(sb);
+    }
+    if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
+    p.max_splits = (max_blocks + p.split_blocks - 1) / p.split_blocks;
+    *out = p;
+    return KV_OK;
+}
+
+size_t workspace_bytes_for(const kv_pool* pl, int batch, int q_heads, const Plan& p)
+{
+    if (p.max_splits <= 1) return 0;
+    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
+    return round_up(n * pl->head_dim * sizeof(float), kAlign) + n * 2 * sizeof(float);
+}
+
+kv_status check_device(const kv_pool* pl)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+    return dev == pl->device ? KV_OK : KV_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kv_abi_version(void) { return KV_PAGED_ABI_VERSION; }
+
+const char* kv_status_string(kv_status s)
+{
+    switch (s) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case KV_ERR_OUT_OF_BLOCKS: return "out of KV cache blocks";
+    case KV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KV_ERR_CUDA: return "CUDA error";
+    case KV_ERR_DEVICE_CHECK: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+kv_status kv_pool_create(int num_blocks, int block_size, int kv_heads, int head_dim,
+                         kv_dtype dtype, int device, kv_pool** out)
+{
+    if (out == nullptr) return KV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_blocks <= 0 || block_size <= 0 || kv_heads <= 0 || head_dim <= 0 || device < 0)
+        return KV_ERR_INVALID_ARG;
+    if (dtype != KV_DTYPE_BF16 && dtype != KV_DTYPE_FP8_E4M3) return KV_ERR_INVALID_ARG;
+    if (!variant_supported(dtype, head_dim, block_size)) return KV_ERR_UNSUPPORTED;
+    const size_t elem = dtype == KV_DTYPE_BF16 ? 2 : 1;
+    const long double bytes = static_cast<long double>(num_blocks) * block_size * kv_heads *
+                              head_dim * elem;
+    if (bytes >= static_cast<long double>(1ull << 40)) return KV_ERR_UNSUPPORTED;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) return KV_ERR_CUDA;
+    DeviceGuard guard(device);
+    if (!guard.ok) return KV_ERR_CUDA;
+
+    kv_pool* p = new (std::nothrow) kv_pool();
+    if (p == nullptr) return KV_ERR_OUT_OF_MEMORY;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->kv_heads = kv_heads;
+    p->head_dim = head_dim;
+    p->device = device;
+    p->dtype = dtype;
+    p->elem = elem;
+    p->pool_bytes = static_cast<size_t>(bytes);
+    const size_t half = round_up(p->pool_bytes, kAlign);
+    const size_t scales = round_up(sizeof(float) * kv_heads, kAlign);
+    const size_t total = 2 * half + 2 * scales + kAlign;
+    if (cudaMalloc(&p->base, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return KV_ERR_OUT_OF_MEMORY;
+    }
+    uint8_t* b = static_cast<uint8_t*>(p->base);
+    p->k = b;
+    p->v = b + half;
+    p->k_scale = reinterpret_cast<float*>(b + 2 * half);
+    p->v_scale = reinterpret_cast<float*>(b + 2 * half + scales);
+    p->err = reinterpret_cast<uint32_t*>(b + 2 * half + 2 * scales);
+
+    kv_status st = KV_OK;
+    if (cudaMemset(p->base, 0, total) != cudaSuccess) st = KV_ERR_CUDA;
+    if (st == KV_OK) {
+        float* ones = new (std::nothrow) float[kv_heads];
+        if (ones == nullptr) {
+            st = KV_ERR_OUT_OF_MEMORY;
+        } else {
+            for (int h = 0; h < kv_heads; ++h) ones[h] = 1.0f;
+            if (cudaMemcpy(p->k_scale, ones, sizeof(float) * kv_heads, cudaMemcpyHostToDevice) !=
+                    cudaSuccess ||
+                cudaMemcpy(p->v_scale, ones, sizeof(float) * kv_heads, cudaMemcpyHostToDevice) !=
+                    cudaSuccess)
+                st = KV_ERR_CUDA;
+            delete[] ones;
+        }
+    }
+    if (st == KV_OK && cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device) !=
+                           cudaSuccess)
+        st = KV_ERR_CUDA;
+    if (st == KV_OK) st = encode_pool_map(p, p->k, &p->tmk);
+    if (st == KV_OK) st = encode_pool_map(p, p->v, &p->tmv);
+    if (st == KV_OK) {
+        const bool fp8 = dtype == KV_DTYPE_FP8_E4M3;
+        for (int nt : {8, 16}) {
+            cudaError_t e = fp8 ? kvp::prepare_decode_fp8(head_dim, block_size, nt)
+                                : kvp::prepare_decode_bf16(head_dim, block_size, nt);
+            if (e != cudaSuccess) st = KV_ERR_CUDA;
+        }
+    }
+    if (st == KV_OK && cudaDeviceSynchronize() != cudaSuccess) st = KV_ERR_CUDA;
+    if (st != KV_OK) {
+        cudaGetLastError();
+        cudaFree(p->base);
+        delete p;
+        return st;
+    }
+    *out = p;
+    return KV_OK;
+}
+
+kv_status kv_pool_destroy(kv_pool* pool)
+{
+    if (pool == nullptr) return KV_OK;
+    kv_status st = KV_OK;
+    {
+        DeviceGuard guard(pool->device);
+        if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) st = KV_ERR_CUDA;
+        if (cudaFree(pool->base) != cudaSuccess) st = KV_ERR_CUDA;
+    }
+    delete pool;
+    return st;
+}
+
+kv_status kv_pool_tensors(const kv_pool* pool, void** k_pool, void** v_pool, float** k_scale,
+                          float** v_scale)
+{
+    if (pool == nullptr) return KV_ERR_INVALID_ARG;
+    if (k_pool) *k_pool = pool->k;
+    if (v_pool) *v_pool = pool->v;
+    if (k_scale) *k_scale = pool->k_scale;
+    if (v_scale) *v_scale = pool->v_scale;
+    return KV_OK;
+}
+
+kv_status kv_pool_shape(const kv_pool* pool, int* num_blocks, int* block_size, int* kv_heads,
+                        int* head_dim, kv_dtype* dtype, int* device)
+{
+    if (pool == nullptr) return KV_ERR_INVALID_ARG;
+    if (num_blocks) *num_blocks = pool->num_blocks;
+    if (block_size) *block_size = pool->block_size;
+    if (kv_heads) *kv_heads = pool->kv_heads;
+    if (head_dim) *head_dim = pool->head_dim;
+    if (dtype) *dtype = pool->dtype;
+    if (device) *device = pool->device;
+    return KV_OK;
+}
+
+kv_status kv_pool_set_scales(kv_pool* pool, const float* k_scale_host, const float* v_scale_host)
+{
+    if (pool == nullptr) return KV_ERR_INVALID_ARG;
+    for (const float* s : {k_scale_host, v_scale_host}) {
+        if (s == nullptr) continue;
+        for (int h = 0; h < pool->kv_heads; ++h)
+            if (!(std::isfinite(s[h]) && s[h] > 0.f)) return KV_ERR_INVALID_ARG;
+    }
+    DeviceGuard guard(pool->device);
+    if (!guard.ok) return KV_ERR_CUDA;
+    const size_t n = sizeof(float) * pool->kv_heads;
+    if (k_scale_host && cudaMemcpy(pool->k_scale, k_scale_host, n, cudaMemcpyHostToDevice) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (v_scale_host && cudaMemcpy(pool->v_scale, v_scale_host, n, cudaMemcpyHostToDevice) != cudaSuccess)
+        return KV_ERR_CUDA;
+    return KV_OK;
+}
+
+kv_status kv_pool_device_errors(kv_pool* pool, uint32_t* bits, int clear)
+{
+    if (pool == nullptr || bits == nullptr) return KV_ERR_INVALID_ARG;
+    DeviceGuard guard(pool->device);
+    if (!guard.ok || cudaDeviceSynchronize() != cudaSuccess) return KV_ERR_CUDA;
+    if (cudaMemcpy(bits, pool->err, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KV_ERR_CUDA;
+    if (clear && cudaMemset(pool->err, 0, sizeof(uint32_t)) != cudaSuccess) return KV_ERR_CUDA;
+    return *bits ? KV_ERR_DEVICE_CHECK : KV_OK;
+}
+
+kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, int num_tokens,
+                          const int32_t* token_seq, const int32_t* token_pos,
+                          const int32_t* block_tables, int max_blocks,
+                          const int32_t* context_lens, int batch, void* stream)
+{
+    if (pool == nullptr || num_tokens < 0 || batch < 0 || max_blocks <= 0)
+        return KV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return KV_OK;
+    if (k_new == nullptr || v_new == nullptr || block_tables == nullptr || batch == 0)
+        return KV_ERR_INVALID_ARG;
+    if (token_pos == nullptr && context_lens == nullptr) return KV_ERR_INVALID_ARG;
+    if (token_seq == nullptr && num_tokens > batch) return KV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(block_tables, 4) ||
+        !aligned(token_seq, 4) || !aligned(token_pos, 4) || !aligned(context_lens, 4))
+        return KV_ERR_INVALID_ARG;
+    kv_status st = check_device(pool);
+    if (st != KV_OK) return st;
+    kvp::AppendParams p;
+    p.k_new = static_cast<const uint16_t*>(k_new);
+    p.v_new = static_cast<const uint16_t*>(v_new);
+    p.token_seq = token_seq;
+    p.token_pos = token_pos;
+    p.tables = block_tables;
+    p.ctx = context_lens;
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.k_scale = pool->k_scale;
+    p.v_scale = pool->v_scale;
+    p.err = pool->err;
+    p.num_tokens = num_tokens;
+    p.batch = batch;
+    p.max_blocks = max_blocks;
+    p.num_blocks = pool->num_blocks;
+    p.block_size = pool->block_size;
+    p.kv_heads = pool->kv_heads;
+    p.head_dim = pool->head_dim;
+    p.fp8 = pool->dtype == KV_DTYPE_FP8_E4M3;
+    return kvp::launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
+                                                                                   : KV_ERR_CUDA;
+}
+
+kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                            int kv_split_tokens, int* split_tokens, int* max_splits)
+{
+    Plan p;
+    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    if (st != KV_OK) return st;
+    if (split_tokens) *split_tokens = p.split_blocks * pool->block_size;
+    if (max_splits) *max_splits = p.max_splits;
+    return KV_OK;
+}
+
+kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_heads,
+                                      int max_blocks, int kv_split_tokens, size_t* bytes)
+{
+    if (bytes == nullptr) return KV_ERR_INVALID_ARG;
+    Plan p;
+    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    if (st != KV_OK) return st;
+    *bytes = workspace_bytes_for(pool, batch, q_heads, p);
+    return KV_OK;
+}
+
+kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                 const int32_t* block_tables, int max_blocks,
+                                 const int32_t* context_lens, int batch, float scale,
+                                 int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                 void* out, float* lse_out, void* stream)
+{
+    Plan plan;
+    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
+    if (st != KV_OK) return st;
+    if (batch == 0) return KV_OK;
+    if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
+        return KV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4) || !aligned(lse_out, 4) || !aligned(workspace, 16))
+        return KV_ERR_INVALID_ARG;
+    if (batch > 65535 || static_cast<long long>(pool->kv_heads) * plan.head_groups > 65535)
+        return KV_ERR_UNSUPPORTED;
+    const size_t need = workspace_bytes_for(pool, batch, q_heads, plan);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KV_ERR_INVALID_ARG;
+    st = check_device(pool);
+    if (st != KV_OK) return st;
+
+    const size_t n = static_cast<size_t>(batch) * q_heads * plan.max_splits;
+    kvp::DecodeParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.tables = block_tables;
+    p.ctx = context_lens;
+    p.k_scale = pool->k_scale;
+    p.v_scale = pool->v_scale;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse_out;
+    p.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
+    p.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                    round_up(n * pool->head_dim * sizeof(float), kAlign))
+                         : nullptr;
+    p.err = pool->err;
+    p.batch = batch;
+    p.q_heads = q_heads;
+    p.kv_heads = pool->kv_heads;
+    p.group = plan.group;
+    p.head_groups = plan.head_groups;
+    p.max_blocks = max_blocks;
+    p.num_blocks = pool->num_blocks;
+    p.split_blocks = plan.split_blocks;
+    p.max_splits = plan.max_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    const dim3 grid(static_cast<unsigned>(plan.max_splits),
+                    static_cast<unsigned>(pool->kv_heads * plan.head_groups),
+                    static_cast<unsigned>(batch));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pool->dtype == KV_DTYPE_BF16
+                        ? kvp::launch_decode_bf16(pool->head_dim, pool->block_size, plan.head_tile,
+                                                  grid, pool->tmk, pool->tmv, p, s)
+                        : kvp::launch_decode_fp8(pool->head_dim, pool->block_size, plan.head_tile,
+                                                 grid, pool->tmk, pool->tmv, p, s);
+    if (e != cudaSuccess) return KV_ERR_CUDA;
+    if (plan.max_splits > 1) {
+        kvp::MergeParams m;
+        m.part_o = p.part_o;
+        m.part_ml = p.part_ml;
+        m.ctx = context_lens;
+        m.out = p.out;
+        m.lse = lse_out;
+        m.batch = batch;
+        m.q_heads = q_heads;
+        m.head_dim = pool->head_dim;
+        m.block_size = pool->block_size;
+        m.max_blocks = max_blocks;
+        m.split_blocks = plan.split_blocks;
+        m.max_splits = plan.max_splits;
+        if (kvp::launch_merge(m, s) != cudaSuccess) return KV_ERR_CUDA;
+    }
+    return KV_OK;
+}
+
+}  // extern "C"

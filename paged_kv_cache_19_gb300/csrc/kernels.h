@@ -1,0 +1,75 @@
+// kernels.h -- parameter blocks and launchers shared by the host layer and the
+// CUDA translation units.  Internal to the library (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvp {
+
+// One CTA of the main decode kernel covers (sequence, kv head, head group,
+// split).  All pointers are device pointers.
+struct DecodeParams {
+    const uint16_t* q;        // bf16 [batch, q_heads, head_dim]
+    const int32_t* tables;    // [batch, max_blocks]
+    const int32_t* ctx;       // [batch]
+    const float* k_scale;     // [kv_heads] (fp8 cache)
+    const float* v_scale;     // [kv_heads] (fp8 cache)
+    uint16_t* out;            // bf16 [batch, q_heads, head_dim]
+    float* lse;               // [batch, q_heads] or null
+    float* part_o;            // [batch, q_heads, max_splits, head_dim]
+    float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum) in log2 units
+    uint32_t* err;            // device error word
+    int batch, q_heads, kv_heads, group, head_groups;
+    int max_blocks, num_blocks;
+    int split_blocks, max_splits;
+    float scale_log2;         // softmax scale * log2(e)
+};
+
+struct MergeParams {
+    const float* part_o;
+    const float* part_ml;
+    const int32_t* ctx;
+    uint16_t* out;
+    float* lse;
+    int batch, q_heads, head_dim, block_size, max_blocks;
+    int split_blocks, max_splits;
+};
+
+struct AppendParams {
+    const uint16_t* k_new;    // bf16 [num_tokens, kv_heads, head_dim]
+    const uint16_t* v_new;
+    const int32_t* token_seq; // or null
+    const int32_t* token_pos; // or null
+    const int32_t* tables;
+    const int32_t* ctx;
+    uint8_t* k_pool;
+    uint8_t* v_pool;
+    const float* k_scale;
+    const float* v_scale;
+    uint32_t* err;
+    int num_tokens, batch, max_blocks, num_blocks, block_size, kv_heads, head_dim;
+    int fp8;
+};
+
+// Query-head tile of one CTA: 8 or 16 heads of a GQA group (padding unused rows).
+inline int head_tile_for_group(int group) { return group <= 8 ? 8 : 16; }
+
+// Dynamic shared memory of one main-kernel CTA (stages + barriers + alignment
+// slack); 0 when no variant exists for these sizes.
+int smem_decode_bf16(int head_dim, int block_size, int head_tile);
+int smem_decode_fp8(int head_dim, int block_size, int head_tile);
+// Raises the variant's dynamic shared-memory limit (once, at pool creation).
+cudaError_t prepare_decode_bf16(int head_dim, int block_size, int head_tile);
+cudaError_t prepare_decode_fp8(int head_dim, int block_size, int head_tile);
+cudaError_t launch_decode_bf16(int head_dim, int block_size, int head_tile, dim3 grid,
+                               const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 grid,
+                              const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+
+}  // namespace kvp

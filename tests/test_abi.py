@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+function include/kv_paged.h declares, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_19_gb300 as kp
+from paged_kv_cache_19_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return kp.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kv_paged.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_expected_calls():
+    names = declared_functions()
+    for must in ("kv_pool_create", "paged_kv_append", "paged_decode_attention"):
+        assert must in names
+    assert len(names) >= 12
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kv_abi_version() == 1
+    for code in range(7):
+        assert lib.kv_status_string(code)
+    assert lib.kv_status_string(99) == b"unknown status"
+
+
+def test_pool_create_validates_on_the_host(lib):
+    h = ctypes.c_void_p(123)
+    assert lib.kv_pool_create(0, 16, 8, 128, 0, 0, ctypes.byref(h)) == kp.KV_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.kv_pool_create(64, 16, 8, 128, 7, 0, ctypes.byref(h)) == kp.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_create(64, 24, 8, 128, 0, 0, ctypes.byref(h)) == kp.KV_ERR_UNSUPPORTED
+    assert lib.kv_pool_create(64, 16, 8, 96, 0, 0, ctypes.byref(h)) == kp.KV_ERR_UNSUPPORTED
+    assert lib.kv_pool_create(64, 16, 8, 64, 1, 0, ctypes.byref(h)) == kp.KV_ERR_UNSUPPORTED
+    assert lib.kv_pool_create(1 << 30, 32, 64, 128, 0, 0, ctypes.byref(h)) == kp.KV_ERR_UNSUPPORTED
+    assert lib.kv_pool_create(64, 16, 8, 128, 0, 0, None) == kp.KV_ERR_INVALID_ARG
+
+
+def test_calls_on_a_null_pool_are_rejected(lib):
+    n = ctypes.c_size_t()
+    assert lib.paged_decode_workspace_size(None, 1, 8, 4, 0, ctypes.byref(n)) == kp.KV_ERR_INVALID_ARG
+    assert lib.paged_kv_append(None, None, None, 1, None, None, None, 1, None, 1, None) == \
+        kp.KV_ERR_INVALID_ARG
+    assert lib.paged_decode_attention(None, None, 8, None, 4, None, 1, 1.0, 0, None, 0, None, None,
+                                      None) == kp.KV_ERR_INVALID_ARG
+    assert lib.kv_pool_destroy(None) == kp.KV_OK
+    bits = ctypes.c_uint32()
+    assert lib.kv_pool_device_errors(None, ctypes.byref(bits), 0) == kp.KV_ERR_INVALID_ARG
+
+
+def test_pool_create_without_a_gpu_reports_a_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    assert lib.kv_pool_create(64, 16, 8, 128, 0, 0, ctypes.byref(h)) == kp.KV_ERR_CUDA
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(kp, "_lib", None)
+    monkeypatch.setattr(kp, "_LIB_PATH", "/nonexistent/libkvpaged.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        kp.load_library()
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_19_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Append, indexing and fp8 codes are compared bit for bit; attention outputs
+within max |err| <= 2e-2 and relative L2 <= 5e-3 (bf16 storage, fp32
+accumulation); for the fp8 cache also within 6e-2 of the oracle on the
+unquantised values.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_19_gb300 as kp
+import workloads
+from gpu_util import (FP8_VS_UNQUANTISED_MAX_ABS, LSE_ABS, MAX_ABS, REL_L2, Staged, bf16_tensor,
+                      compare, i32)
+
+pytestmark = pytest.mark.gpu
+
+C = workloads.custom
+SMALL = {
+    "tiny": workloads.CONFIGS["tiny"],
+    "g4_d128_bs16": C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                      ctx=[1, 16, 203], seed=101),
+    "g8_split64": C(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,
+                    ctx=[37, 300, 1000], seed=102, split_tokens=64),
+    "g1_d64_bs32": C(batch=4, q_heads=4, kv_heads=4, head_dim=64, block_size=32,
+                     ctx=[5, 33, 64, 95], seed=103),
+    "g16_nt16": C(batch=2, q_heads=32, kv_heads=2, head_dim=128, block_size=16,
+                  ctx=[100, 257], seed=104),
+    "g32_two_head_groups": C(batch=2, q_heads=32, kv_heads=1, head_dim=64, block_size=16,
+                             ctx=[70, 500], seed=105, split_tokens=128),
+    "g12_padded_bs32": C(batch=3, q_heads=24, kv_heads=2, head_dim=128, block_size=32,
+                         ctx=[31, 32, 333], seed=106),
+    "g2_d64": C(batch=5, q_heads=4, kv_heads=2, head_dim=64, block_size=16,
+                ctx=[2, 17, 48, 129, 700], seed=107, split_tokens=96),
+    "prefix_shared": C(batch=8, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                       ctx=[20, 70, 64, 129, 65, 200, 16, 90], seed=108, prefix_group=4,
+                       prefix_tokens=64),
+    "fp8_g1_bs32": C(batch=5, q_heads=4, kv_heads=4, head_dim=128, block_size=32,
+                     ctx=[1, 31, 32, 33, 200], seed=109, cache_dtype="fp8_e4m3"),
+    "fp8_g4_split32": C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                        ctx=[3, 150, 400], seed=110, cache_dtype="fp8_e4m3", split_tokens=32),
+    "fp8_g16": C(batch=2, q_heads=32, kv_heads=2, head_dim=128, block_size=32,
+                 ctx=[64, 300], seed=111, cache_dtype="fp8_e4m3"),
+    "long_ragged_auto_split": C(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,
+                                ctx=[5000, 17, 2500], seed=112),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(SMALL))
+def staged(request):
+    w = workloads.make(SMALL[request.param])
+    st = Staged(w)
+    yield st
+    st.destroy()
+
+
+def test_append_pool_image_bit_exact(staged):
+    w = staged.w
+    kimg, vimg = oracle.pool_image(w, after_step=True)
+    kr, vr = staged.pool.raw_bytes()
+    assert np.array_equal(kr.cpu().numpy(), kimg)
+    assert np.array_equal(vr.cpu().numpy(), vimg)
+    assert staged.pool.device_errors() == 0
+
+
+def test_decode_matches_oracle(staged):
+    w = staged.w
+    out, lse = staged.decode()
+    ref, ref_lse = oracle.decode_workload(w)
+    max_abs, rel, got = compare(out, ref)
+    assert np.isfinite(got).all()
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= LSE_ABS
+    if w.spec.cache_dtype == "fp8_e4m3":
+        raw, _ = oracle.decode_workload(w, cache_dtype="bf16")
+        assert np.max(np.abs(got - raw)) <= FP8_VS_UNQUANTISED_MAX_ABS
+    assert staged.pool.device_errors() == 0
+
+
+def test_decode_is_invariant_to_the_split(staged):
+    w = staged.w
+    a, la = staged.decode(split_tokens=w.spec.block_size)          # one block per chunk
+    b, lb = staged.decode(split_tokens=w.spec.block_size * w.max_blocks)   # one chunk
+    ref, _ = oracle.decode_workload(w)
+    for out in (a, b):
+        max_abs, rel, _ = compare(out, ref)
+        assert max_abs <= MAX_ABS and rel <= REL_L2
+    assert torch.allclose(la, lb, atol=LSE_ABS, rtol=0)
+
+
+def test_block_permutation_gives_identical_bits():
+    w = workloads.make(SMALL["g4_d128_bs16"])
+    st = Staged(w)
+    out1, lse1 = st.decode(split_tokens=32)
+    perm = np.random.default_rng(9).permutation(w.num_blocks)
+    kr, vr = st.pool.raw_bytes()
+    idx = torch.from_numpy(np.argsort(perm)).cuda()          # new block j holds old block argsort[j]
+    kr.copy_(kr[idx].clone())
+    vr.copy_(vr[idx].clone())
+    t2 = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1).astype(np.int32)
+    st.tables = i32(t2)
+    out2, lse2 = st.decode(split_tokens=32)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    st.destroy()
+
+
+def test_batch_independence_bit_exact():
+    w = workloads.make(SMALL["g8_split64"])
+    st = Staged(w)
+    full, _ = st.decode(split_tokens=64)
+    for b in range(w.batch):
+        out = torch.empty_like(st.q[b:b + 1])
+        kp.paged_decode_attention(st.pool, st.q[b:b + 1], st.tables[b:b + 1], st.ctx[b:b + 1],
+                                  w.scale, kv_split_tokens=64, out=out)
+        assert torch.equal(out.view(torch.int16), full[b:b + 1].view(torch.int16))
+    st.destroy()
+
+
+def test_empty_context_gives_zero_output_and_minus_inf_lse():
+    spec = C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16, ctx=[5, 40, 9], seed=120)
+    w = workloads.make(spec)
+    st = Staged(w)
+    st.ctx = i32(np.array([5, 0, 9], dtype=np.int32))
+    out, lse = st.decode()
+    ref, _ = oracle.decode_workload(w, seqs=[0, 2])
+    assert torch.count_nonzero(out[1].float()) == 0
+    assert torch.isneginf(lse[1]).all()
+    max_abs, rel, _ = compare(out[[0, 2]], ref)
+    assert max_abs <= MAX_ABS and rel <= REL_L2
+    st.destroy()
+
+
+def test_bad_block_id_is_skipped_and_reported():
+    spec = C(batch=2, q_heads=8, kv_heads=2, head_dim=128, block_size=16, ctx=[40, 40], seed=121)
+    w = workloads.make(spec)
+    st = Staged(w)
+    assert st.pool.device_errors() == 0
+    t = w.block_tables.copy()
+    t[1, 1] = w.num_blocks + 7          # outside the pool
+    st.tables = i32(t)
+    out, _ = st.decode()
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() & kp.DEVERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    ref, _ = oracle.decode_workload(w, seqs=[0])
+    max_abs, rel, _ = compare(out[:1], ref)           # the other sequence is untouched
+    assert max_abs <= MAX_ABS and rel <= REL_L2
+    st.ctx = i32(np.array([40, 10_000], dtype=np.int32))     # past max_blocks * block_size
+    st.decode()
+    assert st.pool.device_errors() & kp.DEVERR_CONTEXT
+    st.destroy()
+
+
+def test_append_rejects_bad_addresses_on_device():
+    spec = C(batch=2, q_heads=2, kv_heads=2, head_dim=64, block_size=16, ctx=[3, 20], seed=122)
+    w = workloads.make(spec)
+    st = Staged(w)
+    before = [x.clone() for x in st.pool.raw_bytes()]
+    kn = bf16_tensor(w.k_new[:1])
+    kp.paged_kv_append(st.pool, kn, kn, st.tables, st.ctx, token_seq=i32([5]), token_pos=i32([0]))
+    assert st.pool.device_errors() & kp.DEVERR_SEQ
+    kp.paged_kv_append(st.pool, kn, kn, st.tables, st.ctx, token_seq=i32([0]), token_pos=i32([-1]))
+    assert st.pool.device_errors() & kp.DEVERR_POSITION
+    bad = w.block_tables.copy()
+    bad[0, 0] = -3
+    kp.paged_kv_append(st.pool, kn, kn, i32(bad), st.ctx, token_seq=i32([0]), token_pos=i32([0]))
+    assert st.pool.device_errors() & kp.DEVERR_BLOCK_ID
+    after = st.pool.raw_bytes()
+    assert all(torch.equal(a, b) for a, b in zip(before, after))
+    st.destroy()
+
+
+def test_host_validation_rejects_before_launch():
+    spec = C(batch=2, q_heads=8, kv_heads=2, head_dim=128, block_size=16, ctx=[3, 20], seed=123)
+    w = workloads.make(spec)
+    st = Staged(w)
+    bad_heads = torch.zeros(2, 7, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kp.KVError) as e:
+        kp.paged_decode_attention(st.pool, bad_heads, st.tables, st.ctx)
+    assert e.value.status == kp.KV_ERR_INVALID_ARG
+    with pytest.raises(kp.KVError):
+        kp.paged_decode_attention(st.pool, st.q, st.tables, st.ctx, kv_split_tokens=24)
+    need = kp.paged_decode_workspace_size(st.pool, 2, 8, w.max_blocks, 16)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kp.KVError):
+        kp.paged_decode_attention(st.pool, st.q, st.tables, st.ctx, kv_split_tokens=16,
+                                  workspace=small)
+    storage = torch.empty(st.q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    misaligned = storage[1:1 + st.q.numel()].view(st.q.shape)
+    with pytest.raises(kp.KVError):
+        kp.paged_decode_attention(st.pool, misaligned, st.tables, st.ctx)
+    with pytest.raises(kp.KVError):
+        kp.kv_pool_create(10, 24, 2, 128)                            # block size not supported
+    assert st.pool.device_errors() == 0
+    st.destroy()
+
+
+def test_fp8_append_codes_match_the_oracle_encoder_on_every_bf16_value():
+    bits = np.arange(65536, dtype=np.uint16)
+    x = workloads.bf16_bits_to_f32(bits)
+    bits = bits[~np.isnan(x)]                       # NaN inputs are outside the encoder's domain
+    bits = np.concatenate([bits, bits[: (-bits.size) % 128]])
+    tokens = bits.size // 128
+    for scale in (1.0, 0.37, 3.5e-3):
+        pool = kp.kv_pool_create(tokens // 16 + 1, 16, 1, 128, "fp8_e4m3")
+        pool.set_scales([scale], [scale])
+        table = i32(np.arange(tokens // 16 + 1, dtype=np.int32)[None, :])
+        kn = bf16_tensor(bits.reshape(tokens, 1, 128))
+        kp.paged_kv_append(pool, kn, kn, table, i32([tokens]), token_seq=i32(np.zeros(tokens)),
+                           token_pos=i32(np.arange(tokens)))
+        kr, _ = pool.raw_bytes()
+        got = kr.cpu().numpy().reshape(-1)[: bits.size]
+        want = oracle.e4m3_quantize(bits, np.float32(scale))
+        assert np.array_equal(got, want)
+        pool.destroy()
+
+
+# ----------------------------------------------------------------- full-size configurations
+FULL = ["tiny", "llama3_8b", "long_context", "ragged_prefix", "mha_fp8"]
+
+
+def _sample(w, k=4):
+    ctx = w.context_lens
+    picks = {int(np.argmax(ctx)), int(np.argmin(ctx))}
+    picks.update(int(x) for x in np.random.default_rng(5).choice(w.batch, size=min(k, w.batch),
+                                                                  replace=False))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config_sampled_parity(name):
+    """At the benchmark's sizes and launch configuration: the appended slots bit for bit,
+    sampled sequences against the oracle, and properties of every output."""
+    w = workloads.make(workloads.CONFIGS[name])
+    st = Staged(w, step_append=False)
+    st.append_step()
+    out, lse = st.decode()
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() == 0
+    s = w.spec
+    # appended slots
+    b_idx = np.arange(w.batch)
+    pos = w.context_lens - 1
+    blk = w.block_tables[b_idx, pos // s.block_size]
+    slot = pos % s.block_size
+    kr, vr = st.pool.raw_bytes()
+    got_k = kr[torch.from_numpy(blk.astype(np.int64)).cuda(),
+               torch.from_numpy(slot.astype(np.int64)).cuda()].cpu().numpy()
+    got_v = vr[torch.from_numpy(blk.astype(np.int64)).cuda(),
+               torch.from_numpy(slot.astype(np.int64)).cuda()].cpu().numpy()
+    if s.cache_dtype == "bf16":
+        want_k = w.k_new.view(np.uint8).reshape(got_k.shape)
+        want_v = w.v_new.view(np.uint8).reshape(got_v.shape)
+    else:
+        want_k = np.stack([oracle.e4m3_quantize(w.k_new[:, h], w.k_scale[h]) for h in range(s.kv_heads)], 1)
+        want_v = np.stack([oracle.e4m3_quantize(w.v_new[:, h], w.v_scale[h]) for h in range(s.kv_heads)], 1)
+    assert np.array_equal(got_k, want_k) and np.array_equal(got_v, want_v)
+    # every output: finite, and inside the range of its head's values (a convex combination)
+    o = out.float()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    vmax = float(np.abs(workloads.bf16_bits_to_f32(w.v)).max())
+    assert float(o.abs().max()) <= vmax * 1.01 + 1e-3
+    # sampled sequences against the oracle
+    seqs = _sample(w)
+    ref, ref_lse = oracle.decode_workload(w, seqs=seqs, threads=os.cpu_count() or 1)
+    max_abs, rel, got = compare(out[seqs], ref)
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (seqs, max_abs, rel)
+    assert np.max(np.abs(lse[seqs].cpu().numpy() - ref_lse)) <= LSE_ABS
+    if s.cache_dtype == "fp8_e4m3":
+        raw, _ = oracle.decode_workload(w, seqs=seqs, threads=os.cpu_count() or 1, cache_dtype="bf16")
+        assert np.max(np.abs(got - raw)) <= FP8_VS_UNQUANTISED_MAX_ABS
+    st.destroy()

@@ -147,7 +147,7 @@ def _sdpa_causal(Q, K, V):
 
 @pytest.mark.parametrize("hq,hkv,d,T", [(4, 4, 16, 37), (8, 2, 32, 50), (6, 1, 8, 20)])
 def test_decode_equals_full_causal_attention(hq, hkv, d, T):
-    """Decoding with a cache gives row t of full causal attention (pages: "max |cached - full|")."""
+    """Decoding with a cache gives row t of full causal attention (the first page's self-check)."""
     Q = _f64(_bf16((T, hq, d), 11))
     K = _f64(_bf16((T, hkv, d), 12))
     V = _f64(_bf16((T, hkv, d), 13))
