@@ -1,0 +1,526 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV decode step (append + paged decode attention).
+
+One step = paged_kv_append of every sequence's new K/V, then
+paged_decode_attention over the whole ragged batch, on the Llama-3-8B-shaped
+layer by default (batch 64, GQA 32/8, head_dim 128, block_size 16, contexts
+uniform in [512, 4096], bf16 N(0,1), blocks randomly permuted in a pool of
+total blocks + 10%).  Prints one JSON line.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl reference]
+
+value: whole-step algorithmic bytes / step time (GB/s), inputs resident in HBM.
+e2e:   the same, measured with host (pinned) inputs and output copied inside the
+       timed region.
+--impl reference: the float64 CPU oracle on the host cores, each step a
+       bounded sample of the same workload.
+With torchrun (N > 1) every rank runs its own batch on its own GPU (weak
+scaling, no collective on the data path); the barrier and the max-over-ranks
+timing use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+from workloads import accounting  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "paged decode step (append + decode attention): achieved algorithmic HBM GB/s"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="llama3_8b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--split-tokens", type=int, default=None,
+                    help="override the split-KV chunk (0 = automatic)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_19_gb300", "csrc", "*")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per decode launch recorded by an ncu capture of the current kernels.
+
+    A profile summary under profiles/ states `kernel_source_sha:` and
+    `dram_bytes_per_launch:` for a workload; it counts only while the sources
+    are unchanged."""
+    sha = kernel_source_sha()
+    for path in glob.glob(os.path.join(PROFILES, "*.md")) + glob.glob(os.path.join(PROFILES, "*.txt")):
+        text = open(path).read()
+        m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+        m_cfg = re.search(r"bench_config:\s*(\w+)", text)
+        m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        if m_sha and m_b and m_cfg and m_sha.group(1) == sha and m_cfg.group(1) == config:
+            return int(m_b.group(1)), os.path.relpath(path, ROOT)
+    return None, None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, with host timestamps."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if not inside:             # region shorter than the sampling period: nearest samples
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            window = "nearest to the timed region"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(p[0]) for _, p in inside]
+        reasons = set()
+        for _, p in inside:
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"], p[3:]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": num(inside[0][1][1]),
+                "power_w_max": max(num(p[2]) for _, p in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
+
+
+def dist_setup(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_spec(config: str, rank: int):
+    spec = workloads.CONFIGS[config]
+    return spec if rank == 0 else replace(spec, seed=spec.seed + 100_000 * rank)
+
+
+def workload_config(w, split_tokens, max_splits, world):
+    s = w.spec
+    kv = accounting.decode_bytes(w, split_tokens)
+    return {
+        "workload": s.name, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
+        "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": s.cache_dtype,
+        "context_tokens": w.total_tokens, "ctx_min": int(w.context_lens.min()),
+        "ctx_max": int(w.context_lens.max()), "num_blocks": w.num_blocks,
+        "split_tokens": split_tokens, "max_splits": max_splits,
+        "kv_bytes_logical": kv["kv_logical"], "kv_bytes_unique": kv["kv_unique"],
+        "l2": (f"no flush: the KV pool read per step ({kv['kv_logical'] / 1e6:.0f} MB) is larger "
+               f"than the 129 MB L2" if kv["kv_logical"] > L2_BYTES else
+               "working set smaller than L2: numbers include L2 hits"),
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "seed": s.seed,
+    }
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+def oracle_step_sample(w, seqs, threads):
+    """One oracle step on a sample of sequences: append their new tokens, then decode them."""
+    import oracle
+    s = w.spec
+    # append: the sampled sequences' target blocks, remapped into a small pool image
+    pos = w.context_lens[seqs] - 1
+    blocks = w.block_tables[seqs, pos // s.block_size]
+    uniq, inv = np.unique(blocks, return_inverse=True)
+    table = np.zeros((len(seqs), w.max_blocks), dtype=np.int32)
+    table[np.arange(len(seqs)), pos // s.block_size] = inv.astype(np.int32)
+    shape = (uniq.size, s.block_size, s.kv_heads, s.head_dim * w.elem_bytes)
+    kp_img = np.full(shape, 0xFF, dtype=np.uint8)
+    vp_img = np.full(shape, 0xFF, dtype=np.uint8)
+    oracle.append(kp_img, vp_img, s.cache_dtype, s.block_size, w.k_new[seqs], w.v_new[seqs], table,
+                  w.context_lens[seqs], k_scale=w.k_scale, v_scale=w.v_scale)
+    return oracle.decode_workload(w, seqs=seqs, threads=threads)
+
+
+def sample_bytes(w, seqs):
+    s = w.spec
+    row = 2 * s.kv_heads * s.head_dim * w.elem_bytes
+    kv = int(w.context_lens[seqs].astype(np.int64).sum()) * row
+    qo = 2 * len(seqs) * s.q_heads * s.head_dim * 2
+    app = len(seqs) * s.kv_heads * s.head_dim * (4 + 2 * w.elem_bytes)
+    return kv + qo + app, int(w.context_lens[seqs].astype(np.int64).sum())
+
+
+def cpu_baseline(w, target_s: float, gpu_out=None):
+    """The oracle as it stands on the host cores, on a bounded sample of the workload."""
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(0).permutation(w.batch)
+    n = min(w.batch, threads)
+    t0 = time.perf_counter()
+    out, _ = oracle_step_sample(w, order[:n], threads)
+    dt = time.perf_counter() - t0
+    seqs = order[:n]
+    if dt < target_s / 4 and n < w.batch:        # grow the sample towards the target time
+        n2 = int(min(w.batch, max(n + 1, n * target_s / max(dt, 1e-3) / 2)))
+        seqs = order[:n2]
+        t0 = time.perf_counter()
+        out, _ = oracle_step_sample(w, seqs, threads)
+        dt = time.perf_counter() - t0
+    nbytes, ntok = sample_bytes(w, seqs)
+    res = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+           "kind": "oracle",
+           "sample": (f"append + decode of {len(seqs)} of {w.batch} sequences ({ntok} cached "
+                      f"tokens, all {w.spec.q_heads} query heads), float64 C oracle, "
+                      f"{threads} threads, {dt:.2f} s"),
+           "kv_tokens_per_s": round(ntok / dt, 1)}
+    if gpu_out is not None:
+        got = gpu_out[seqs].float().cpu().double().numpy()
+        err = got - out
+        res["sample_max_abs_err_vs_gpu"] = float(np.max(np.abs(err)))
+        res["sample_rel_l2_err_vs_gpu"] = float(np.linalg.norm(err) / np.linalg.norm(out))
+    return res
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workloads.make(workloads.CONFIGS[args.config])
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(0).permutation(w.batch)
+    # size each step so that warm-up + timed steps fit about two minutes
+    t0 = time.perf_counter()
+    oracle_step_sample(w, order[:1], threads)
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.batch, threads * budget / per_seq)))
+    steps_seqs = [np.take(order, np.arange(i * n, i * n + n), mode="wrap")
+                  for i in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        oracle_step_sample(w, steps_seqs[i], threads)
+    total_bytes = 0
+    total_tok = 0
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        oracle_step_sample(w, steps_seqs[i], threads)
+        b, tok = sample_bytes(w, steps_seqs[i])
+        total_bytes += b
+        total_tok += tok
+    dt = time.perf_counter() - t0
+    value = total_bytes / dt / 1e9
+    sample = (f"each step: append + decode of {n} of {w.batch} sequences, float64 C oracle, "
+              f"{threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC,
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "kv_tokens_per_s": round(total_tok / dt, 1),
+        "config": {"workload": w.spec.name, "batch": w.spec.batch, "sample_sequences_per_step": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def stage(w, device):
+    import torch
+    import paged_kv_cache_19_gb300 as kp
+    s = w.spec
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+    pool = kp.kv_pool_create(w.num_blocks, s.block_size, s.kv_heads, s.head_dim, s.cache_dtype,
+                             device=device.index)
+    kr, vr = pool.raw_bytes()
+    kr.fill_(workloads.POISON_BYTE)
+    vr.fill_(workloads.POISON_BYTE)
+    if s.cache_dtype == "fp8_e4m3":
+        pool.set_scales(w.k_scale, w.v_scale)
+    tables, ctx = i32(w.block_tables), i32(w.context_lens)
+    chunk = 1 << 16
+    for a in range(0, w.prefill_seq.size, chunk):
+        rows = w.prefill_row[a:a + chunk]
+        kp.paged_kv_append(pool, bf16(w.k[rows]), bf16(w.v[rows]), tables, ctx,
+                           token_seq=i32(w.prefill_seq[a:a + chunk]),
+                           token_pos=i32(w.prefill_pos[a:a + chunk]))
+    return pool, tables, ctx, bf16(w.q), bf16(w.k_new), bf16(w.v_new)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import paged_kv_cache_19_gb300 as kp
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    kp.load_library()
+    w = workloads.make(rank_spec(args.config, rank))
+    s = w.spec
+    split_req = s.split_tokens if args.split_tokens is None else args.split_tokens
+    pool, tables, ctx, q, k_new, v_new = stage(w, device)
+    split_tokens, max_splits = kp.paged_decode_plan(pool, s.batch, s.q_heads, w.max_blocks, split_req)
+    ws_bytes = kp.paged_decode_workspace_size(pool, s.batch, s.q_heads, w.max_blocks, split_req)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kp.paged_kv_append(pool, k_new, v_new, tables, ctx, stream=stream)
+        kp.paged_decode_attention(pool, q, tables, ctx, w.scale, kv_split_tokens=split_req,
+                                  workspace=workspace, out=out, lse=lse, stream=stream)
+
+    dec_bytes = accounting.decode_bytes(w, split_tokens)
+    app_bytes = accounting.append_bytes(w)
+    step_bytes = dec_bytes["total"] + app_bytes
+    launches_per_step = 2 + (1 if max_splits > 1 else 0)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert pool.device_errors() == 0, "device-side error during warm-up"
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(device).uuid)
+        gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = str(local)
+    sampler = None if args.no_clocks else ClockSampler(gpu_uuid)
+    if sampler is not None:
+        time.sleep(0.3)
+
+    # ---- timed region: K steps, per-decode events on the launching stream
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    host0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        kp.paged_kv_append(pool, k_new, v_new, tables, ctx, stream=stream)
+        dec_ev[i][0].record(stream)
+        kp.paged_decode_attention(pool, q, tables, ctx, w.scale, kv_split_tokens=split_req,
+                                  workspace=workspace, out=out, lse=lse, stream=stream)
+        dec_ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    host1 = time.time()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    total_ms_max = max_over_ranks(total_ms, world)
+    assert pool.device_errors() == 0, "device-side error during the timed region"
+    if sampler is not None:
+        time.sleep(0.2)
+        sampler.stop()
+        clocks = sampler.summary(host0, host1)
+    else:
+        clocks = None
+
+    all_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    value = all_bytes / (total_ms_max / 1e3) / 1e9
+    kv_tok = sum_over_ranks(w.total_tokens * args.steps, world) / (total_ms_max / 1e3)
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = dec_bytes["total"] / (dec_avg_ms / 1e3) / 1e9
+    traffic, traffic_src = profiled_traffic(args.config)
+
+    # ---- end to end: host (pinned) inputs copied in and the output copied out every step
+    e2e = None
+    if not args.no_e2e:
+        h = {name: t.cpu().pin_memory() for name, t in
+             (("q", q), ("k_new", k_new), ("v_new", v_new), ("tables", tables), ("ctx", ctx))}
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        d = {name: torch.empty_like(t, device=device) for name, t in h.items()}
+        bi = sum(t.numel() * t.element_size() for t in h.values())
+        bo = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for name in d:
+                d[name].copy_(h[name], non_blocking=True)
+            kp.paged_kv_append(pool, d["k_new"], d["v_new"], d["tables"], d["ctx"], stream=stream)
+            kp.paged_decode_attention(pool, d["q"], d["tables"], d["ctx"], w.scale,
+                                      kv_split_tokens=split_req, workspace=workspace, out=out,
+                                      lse=lse, stream=stream)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": round(all_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": round(e2e_ms / args.steps, 5)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds, gpu_out=out)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if s.cache_dtype == "bf16" else "fp8_e4m3 cache, bf16 q/out",
+            "data": "synthetic (seeded N(0,1) bf16, no trained weights)",
+            "config": workload_config(w, split_tokens, max_splits, world),
+            "pct_of_peak": round(100 * value / peak, 2),
+            "kv_tokens_per_s": round(kv_tok, 1),
+            "decode_ms_per_call": round(dec_avg_ms, 5),
+            "roofline": {"kernel": "paged_decode_attention (main kernel" +
+                         (" + LSE merge)" if max_splits > 1 else ")"),
+                         "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "algorithmic_bytes_per_launch": dec_bytes["total"],
+                         "algorithmic_bytes_unique_per_launch": dec_bytes["total_unique"]},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    pool.destroy()
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,69 @@
+"""Algorithmic byte and FLOP counts of the decode step (for throughput and roofline).
+
+The counts are the minimum traffic the step needs, from the definitions:
+every cached K and V element of the tokens 0 .. ctx-1 of each sequence read
+once, q read, the output written, the block-table entries and context lengths
+read, and the split-KV partials written and read back.  Bytes per token of
+cache follow k = 2 * layers * kv_heads * head_dim * bytes_per_value
+(learn.mohebi.ai lesson 12, section 3 "KV-cache memory"; xuewyang.github.io/
+posts/kv, "How big is the cache?"), with one layer per pool here.
+FLOPs follow the decode-step proposition of the same lesson (proof, step 3):
+2 C d_h for the scores and 2 C d_h for the weighted values, per query head.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, bytes_per_value: int) -> int:
+    return 2 * layers * kv_heads * head_dim * bytes_per_value
+
+
+def _nb(w):
+    bs = w.spec.block_size
+    return (w.context_lens.astype(np.int64) + bs - 1) // bs
+
+
+def unique_kv_tokens(w) -> int:
+    """Cached tokens counting each physically shared block once."""
+    s = w.spec
+    total = int(w.context_lens.astype(np.int64).sum())
+    if not w.shared_block.any():
+        return total
+    shared_entries = int(w.shared_block.sum())
+    shared_ids = np.unique(w.block_tables[w.shared_block])
+    return total - shared_entries * s.block_size + int(shared_ids.size) * s.block_size
+
+
+def decode_bytes(w, split_tokens: int) -> dict:
+    """Algorithmic bytes of one paged_decode_attention call."""
+    s = w.spec
+    e = w.elem_bytes
+    ctx = w.context_lens.astype(np.int64)
+    nb = _nb(w)
+    row = 2 * s.kv_heads * s.head_dim * e                      # K and V of one token
+    kv_logical = int(ctx.sum()) * row
+    kv_unique = unique_kv_tokens(w) * row
+    qo = 2 * w.batch * s.q_heads * s.head_dim * 2               # q read + out written (bf16)
+    meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * w.batch * s.q_heads   # tables, ctx, lse
+    sb = max(1, split_tokens // s.block_size)
+    nsplit = np.maximum(1, (nb + sb - 1) // sb)
+    multi = nsplit > 1
+    partial = int((nsplit[multi] * s.q_heads).sum()) * (s.head_dim + 2) * 4 * 2
+    scales = 2 * 4 * s.kv_heads if s.cache_dtype == "fp8_e4m3" else 0
+    other = qo + meta + partial + scales
+    return {"kv_logical": kv_logical, "kv_unique": kv_unique, "other": other,
+            "total": kv_logical + other, "total_unique": kv_unique + other,
+            "partials": partial}
+
+
+def append_bytes(w) -> int:
+    """Algorithmic bytes of one paged_kv_append of the step's new tokens."""
+    s = w.spec
+    n = w.batch * s.kv_heads * s.head_dim
+    return 2 * n * 2 + 2 * n * w.elem_bytes + 8 * w.batch
+
+
+def decode_flops(w) -> int:
+    s = w.spec
+    return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads)
