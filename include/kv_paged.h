@@ -209,6 +209,39 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
                                  int kv_split_tokens, void* workspace, size_t workspace_bytes,
                                  void* out, float* lse_out, void* stream);
 
+/*
+ * Allocation-free decode attention.  The paper has no counterpart to this call;
+ * it exists for users of this library who cannot allocate device memory at the
+ * call site: plug-in hosts that give a kernel only its input and output
+ * buffers, engines whose own allocator has already reserved the whole GPU, and
+ * latency-critical paths where cudaMalloc's implicit device-wide
+ * synchronisation would stall other streams.
+ *
+ * Same arguments and result as paged_decode_attention, without the workspace:
+ * the split-KV partials go to a static device array of
+ * KV_NO_ALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.  The call itself allocates
+ * nothing (no cudaMalloc, no library allocator).
+ *   - Returns KV_ERR_UNSUPPORTED, before launching anything, when the partials
+ *     for these sizes (paged_decode_workspace_size) exceed
+ *     KV_NO_ALLOC_SCRATCH_BYTES; pick a larger kv_split_tokens or use
+ *     paged_decode_attention with your own workspace.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array.  Nothing in it needs to start
+ *     at zero (each call writes every partial it reads back), but calls whose
+ *     kernels overlap on the GPU (different streams without ordering) race on
+ *     it and may corrupt each other's results.
+ */
+#define KV_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+
+kv_status paged_decode_attention_noalloc(const kv_pool* pool, const void* q, int q_heads,
+                                         const int32_t* block_tables, int max_blocks,
+                                         const int32_t* context_lens, int batch, float scale,
+                                         int kv_split_tokens, void* out, float* lse_out,
+                                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -467,3 +467,65 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode attention.
+//
+// For callers that cannot allocate device memory themselves: plug-in hosts
+// that hand a kernel only its input and output buffers, engines whose own
+// allocator has reserved the whole GPU up front, and latency-critical paths
+// where cudaMalloc's implicit device-wide synchronisation would stall other
+// streams.  The split-KV partials live in the fixed-size array below, which is
+// part of the library's device image: every GPU that loads the library holds
+// it until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char kv_noalloc_scratch[KV_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of the scratch array on `device` (which must be current).
+// Looked up once per device; the lookup is the only set-up step.
+kv_status scratch_address(int device, void** addr)
+{
+    if (device < 0 || device >= kMaxScratchDevices) return KV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[device] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, kv_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return KV_ERR_CUDA;
+        }
+        g_scratch_addr[device] = p;
+    }
+    *addr = g_scratch_addr[device];
+    return KV_OK;
+}
+
+}  // namespace
+
+extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const void* q, int q_heads,
+                                                    const int32_t* block_tables, int max_blocks,
+                                                    const int32_t* context_lens, int batch,
+                                                    float scale, int kv_split_tokens, void* out,
+                                                    float* lse_out, void* stream)
+{
+    Plan plan;
+    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
+    if (st != KV_OK) return st;
+    if (batch == 0) return KV_OK;
+    const size_t need = workspace_bytes_for(pool, batch, q_heads, plan);
+    if (need > KV_NO_ALLOC_SCRATCH_BYTES) return KV_ERR_UNSUPPORTED;
+    st = check_device(pool);
+    if (st != KV_OK) return st;
+    void* scratch = nullptr;
+    if (need > 0) {
+        st = scratch_address(pool->device, &scratch);
+        if (st != KV_OK) return st;
+    }
+    return paged_decode_attention(pool, q, q_heads, block_tables, max_blocks, context_lens, batch,
+                                  scale, kv_split_tokens, scratch, need, out, lse_out, stream);
+}
