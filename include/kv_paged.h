@@ -163,15 +163,18 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
  * sizes: *split_tokens (a multiple of block_size) and *max_splits (the most
  * chunks any sequence can have, ceil(max_blocks * block_size / split_tokens)).
  * kv_split_tokens: 0 = automatic (from batch, heads, max_blocks and the SM
- * count), else a positive multiple of block_size.  Either output may be NULL.
+ * count; between 16 and 64 blocks), else a positive multiple of block_size.
+ * KV_ERR_UNSUPPORTED when max_splits would exceed 65535.  Either output may
+ * be NULL.
  */
 kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                             int kv_split_tokens, int* split_tokens, int* max_splits);
 
 /*
  * Bytes of device workspace paged_decode_attention needs for these sizes
- * (fp32 partial outputs, maxima and sums of the split-KV chunks); 0 when
- * every sequence fits one chunk.
+ * (fp32 partial outputs, maxima and sums of the split-KV chunks, and one
+ * 32-bit chunk counter per (sequence, kv head, head tile)); 0 when every
+ * sequence fits one chunk.
  */
 kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_heads,
                                       int max_blocks, int kv_split_tokens, size_t* bytes);
@@ -199,7 +202,11 @@ kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_head
  *     [j * split, (j+1) * split); chunks are merged by log-sum-exp in a second
  *     kernel.  The result does not depend on the split up to rounding.
  *   workspace: device memory of at least paged_decode_workspace_size() bytes
- *     (may be NULL when that size is 0); contents need no initialisation.
+ *     (may be NULL when that size is 0).  It must be zero-filled before its
+ *     first use: it holds the counters that tell the last chunk of a sequence
+ *     to merge the others, and every successful call leaves them at zero
+ *     again.  After a call that raised KV_DEVERR_TIMEOUT, zero it before
+ *     reuse.  One kernel launch per call: the merge happens inside it.
  *   q_heads must be a positive multiple of the pool's kv_heads.
  *   Concurrent calls that share a workspace on different streams race.
  */
@@ -229,10 +236,12 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
  *     stream capture.
- *   - All calls on a device share the one array.  Nothing in it needs to start
- *     at zero (each call writes every partial it reads back), but calls whose
- *     kernels overlap on the GPU (different streams without ordering) race on
- *     it and may corrupt each other's results.
+ *   - All calls on a device share the one array, which keeps what the last
+ *     call left.  The chunk counters that must start at zero are cleared by
+ *     each call on its stream before its kernel; the partial results need no
+ *     clearing.  Calls whose kernels overlap on the GPU (different streams
+ *     without ordering) race on the array and may corrupt each other's
+ *     results.
  */
 #define KV_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 

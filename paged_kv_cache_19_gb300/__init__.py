@@ -253,7 +253,8 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
         scale = 1.0 / math.sqrt(d)
     if workspace is None:
         need = paged_decode_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+        # zero-filled: it holds the per-sequence chunk counters of the in-kernel merge
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
     _need(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel()
     _check(lib.paged_decode_attention(pool.handle, _ptr(q), int(q_heads), _ptr(block_tables),

@@ -108,9 +108,10 @@ struct Plan {
     int group, head_tile, head_groups, split_blocks, max_splits;
 };
 
-// Split-KV plan.  Automatic choice: aim for about four waves of three resident
-// CTAs per SM over the worst case (every sequence at max_blocks), with chunks
-// of at least 32 blocks so each CTA amortises its set-up.
+// Split-KV plan.  Automatic chunk size: about four waves of three resident
+// CTAs per SM over the worst case (every sequence at max_blocks), kept between
+// 16 and 64 blocks -- long enough to amortise a CTA's start, short enough that
+// the last CTAs to start (the remainder chunks, launched last) end soon.
 kv_status make_plan(const kv_pool* pl, int batch, int q_heads, int max_blocks, int split_tokens,
                     Plan* out)
 {
@@ -132,21 +133,39 @@ kv_status make_plan(const kv_pool* pl, int batch, int q_heads, int max_blocks, i
         const long long work = units * max_blocks;
         const long long target = static_cast<long long>(pl->num_sms > 0 ? pl->num_sms : 148) * 12;
         long long sb = (work + target - 1) / target;
-        if (sb < 32) sb = 32;
-        if (sb > max_blocks) sb = max_blocks;
+        if (sb < 16) sb = 16;
+        if (sb > 64) sb = 64;
         p.split_blocks = static_cast<int>(sb);
     }
     if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
     p.max_splits = (max_blocks + p.split_blocks - 1) / p.split_blocks;
+    if (p.max_splits > 65535) return KV_ERR_UNSUPPORTED;      // grid z limit
     *out = p;
     return KV_OK;
 }
 
+// Workspace layout (only when a sequence can have several chunks): partial
+// outputs [batch, q_heads, max_splits, d], (max, sum) pairs [batch, q_heads,
+// max_splits, 2], then one ticket per (sequence, kv head, head tile).
+struct WorkspaceLayout {
+    size_t part_o, part_ml, tickets, ticket_bytes, total;
+};
+
+WorkspaceLayout workspace_layout(const kv_pool* pl, int batch, int q_heads, const Plan& p)
+{
+    WorkspaceLayout w{0, 0, 0, 0, 0};
+    if (p.max_splits <= 1) return w;
+    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
+    w.part_ml = round_up(n * pl->head_dim * sizeof(float), kAlign);
+    w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
+    w.ticket_bytes = static_cast<size_t>(batch) * pl->kv_heads * p.head_groups * sizeof(int);
+    w.total = w.tickets + w.ticket_bytes;
+    return w;
+}
+
 size_t workspace_bytes_for(const kv_pool* pl, int batch, int q_heads, const Plan& p)
 {
-    if (p.max_splits <= 1) return 0;
-    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
-    return round_up(n * pl->head_dim * sizeof(float), kAlign) + n * 2 * sizeof(float);
+    return workspace_layout(pl, batch, q_heads, p).total;
 }
 
 kv_status check_device(const kv_pool* pl)
@@ -406,13 +425,13 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
         !aligned(context_lens, 4) || !aligned(lse_out, 4) || !aligned(workspace, 16))
         return KV_ERR_INVALID_ARG;
     if (batch > 65535 || static_cast<long long>(pool->kv_heads) * plan.head_groups > 65535)
-        return KV_ERR_UNSUPPORTED;
+        return KV_ERR_UNSUPPORTED;                  // grid x / y limits
     const size_t need = workspace_bytes_for(pool, batch, q_heads, plan);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KV_ERR_INVALID_ARG;
     st = check_device(pool);
     if (st != KV_OK) return st;
 
-    const size_t n = static_cast<size_t>(batch) * q_heads * plan.max_splits;
+    const WorkspaceLayout wl = workspace_layout(pool, batch, q_heads, plan);
     kvp::DecodeParams p;
     p.q = static_cast<const uint16_t*>(q);
     p.tables = block_tables;
@@ -421,10 +440,10 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     p.v_scale = pool->v_scale;
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse_out;
-    p.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
-    p.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                    round_up(n * pool->head_dim * sizeof(float), kAlign))
-                         : nullptr;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part_o = need > 0 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
+    p.part_ml = need > 0 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
+    p.tickets = need > 0 ? reinterpret_cast<int*>(ws + wl.tickets) : nullptr;
     p.err = pool->err;
     p.batch = batch;
     p.q_heads = q_heads;
@@ -437,32 +456,16 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
 
-    const dim3 grid(static_cast<unsigned>(plan.max_splits),
-                    static_cast<unsigned>(pool->kv_heads * plan.head_groups),
-                    static_cast<unsigned>(batch));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // chunk-major grid: x = (kv head, head tile), y = sequence, z = chunk
+    const dim3 grid(static_cast<unsigned>(pool->kv_heads * plan.head_groups),
+                    static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));
     cudaError_t e = pool->dtype == KV_DTYPE_BF16
                         ? kvp::launch_decode_bf16(pool->head_dim, pool->block_size, plan.head_tile,
                                                   grid, pool->tmk, pool->tmv, p, s)
                         : kvp::launch_decode_fp8(pool->head_dim, pool->block_size, plan.head_tile,
                                                  grid, pool->tmk, pool->tmv, p, s);
     if (e != cudaSuccess) return KV_ERR_CUDA;
-    if (plan.max_splits > 1) {
-        kvp::MergeParams m;
-        m.part_o = p.part_o;
-        m.part_ml = p.part_ml;
-        m.ctx = context_lens;
-        m.out = p.out;
-        m.lse = lse_out;
-        m.batch = batch;
-        m.q_heads = q_heads;
-        m.head_dim = pool->head_dim;
-        m.block_size = pool->block_size;
-        m.max_blocks = max_blocks;
-        m.split_blocks = plan.split_blocks;
-        m.max_splits = plan.max_splits;
-        if (kvp::launch_merge(m, s) != cudaSuccess) return KV_ERR_CUDA;
-    }
     return KV_OK;
 }
 
@@ -525,6 +528,15 @@ extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const v
     if (need > 0) {
         st = scratch_address(pool->device, &scratch);
         if (st != KV_OK) return st;
+        // The per-unit chunk counts in the scratch must start at zero, whatever
+        // an earlier (possibly failed) call left there.
+        const WorkspaceLayout wl = workspace_layout(pool, batch, q_heads, plan);
+        if (wl.ticket_bytes > 0 &&
+            cudaMemsetAsync(static_cast<uint8_t*>(scratch) + wl.tickets, 0, wl.ticket_bytes,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            cudaGetLastError();
+            return KV_ERR_CUDA;
+        }
     }
     return paged_decode_attention(pool, q, q_heads, block_tables, max_blocks, context_lens, batch,
                                   scale, kv_split_tokens, scratch, need, out, lse_out, stream);

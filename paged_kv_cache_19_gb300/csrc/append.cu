@@ -1,85 +1,8 @@
-// merge_append.cu -- split-KV log-sum-exp merge and the paged KV append.
+// append.cu -- the paged KV append.
 #include "device_common.cuh"
 #include "kernels.h"
 
 namespace kvp {
-
-// ---------------------------------------------------------------------------
-// Merge of the split-KV chunks of one (sequence, query head) per warp.
-// Chunk j carries its normalised output o_j, its running max m_j and its sum
-// l_j = sum exp2(s - m_j) (log2 units).  With M = max_j m_j over non-empty
-// chunks and w_j = l_j 2^(m_j - M):
-//   out = sum_j w_j o_j / sum_j w_j,   lse = (M + log2 sum_j w_j) ln 2.
-// This is the standard identity behind split-KV decoding (learn.mohebi.ai
-// lesson 12, section 6: long contexts spread the cache read over all SMs).
-// Sequences that fit one chunk were finished by the main kernel.
-// ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128) paged_decode_merge(const MergeParams p)
-{
-    constexpr int PER = D / 32;
-    const int gw = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.batch * p.q_heads) return;
-    const int b = gw / p.q_heads;
-    int ctx = __ldg(p.ctx + b);
-    const int cap = p.max_blocks * p.block_size;
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int nblk = (ctx + p.block_size - 1) / p.block_size;
-    const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
-    if (nsplit <= 1) return;
-
-    const size_t bh = static_cast<size_t>(gw);            // == b * q_heads + h
-    const float* ml = p.part_ml + bh * p.max_splits * 2;
-    float M = -INFINITY;
-    for (int j = lane; j < nsplit; j += 32) {
-        const float lj = ml[2 * j + 1];
-        if (lj > 0.f) M = fmaxf(M, ml[2 * j]);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
-
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float W = 0.f;
-    const float* ob = p.part_o + bh * p.max_splits * D + lane * PER;
-    for (int j = 0; j < nsplit; ++j) {
-        const float lj = ml[2 * j + 1];
-        if (!(lj > 0.f)) continue;                        // empty chunk: m = -inf, l = 0
-        const float wj = lj * fast_exp2(ml[2 * j] - M);
-        W += wj;
-        const float* oj = ob + static_cast<size_t>(j) * D;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(oj);
-            acc[0] += wj * v.x;
-            acc[1] += wj * v.y;
-            acc[2] += wj * v.z;
-            acc[3] += wj * v.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] += wj * oj[e];
-        }
-    }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + bh * D + lane * PER);
-#pragma unroll
-    for (int e = 0; e < PER; e += 2) dst[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-    if (p.lse != nullptr && lane == 0)
-        p.lse[bh] = W > 0.f ? (M + __log2f(W)) * 0.69314718055994531f : -INFINITY;
-}
-
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t s)
-{
-    const long warps = static_cast<long>(p.batch) * p.q_heads;
-    const int threads = 128;
-    const long blocks = (warps * 32 + threads - 1) / threads;
-    if (p.head_dim == 128)
-        paged_decode_merge<128><<<static_cast<unsigned>(blocks), threads, 0, s>>>(p);
-    else
-        paged_decode_merge<64><<<static_cast<unsigned>(blocks), threads, 0, s>>>(p);
-    return cudaGetLastError();
-}
 
 // ---------------------------------------------------------------------------
 // Append: token i goes to sequence token_seq[i] (or i) at position

@@ -31,7 +31,7 @@ int smem_decode_fp8(int head_dim, int block_size, int head_tile)
 {
 #define KVP_CASE(D_, BS_, NT_) \
     if (head_dim == D_ && block_size == BS_ && head_tile == NT_) \
-        return DecodeCfg<true, D_, BS_, NT_>::SMEM;
+        return GridCfg<true, D_, BS_, NT_>::SMEM;
     KVP_FP8_VARIANTS(KVP_CASE)
 #undef KVP_CASE
     return 0;

@@ -21,20 +21,11 @@ struct DecodeParams {
     float* part_o;            // [batch, q_heads, max_splits, head_dim]
     float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum) in log2 units
     uint32_t* err;            // device error word
+    int* tickets;             // per-unit count of finished chunks; zero between calls
     int batch, q_heads, kv_heads, group, head_groups;
     int max_blocks, num_blocks;
     int split_blocks, max_splits;
     float scale_log2;         // softmax scale * log2(e)
-};
-
-struct MergeParams {
-    const float* part_o;
-    const float* part_ml;
-    const int32_t* ctx;
-    uint16_t* out;
-    float* lse;
-    int batch, q_heads, head_dim, block_size, max_blocks;
-    int split_blocks, max_splits;
 };
 
 struct AppendParams {
@@ -69,7 +60,6 @@ cudaError_t launch_decode_bf16(int head_dim, int block_size, int head_tile, dim3
 cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 grid,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 
 }  // namespace kvp

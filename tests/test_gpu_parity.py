@@ -90,11 +90,35 @@ def test_decode_is_invariant_to_the_split(staged):
     w = staged.w
     a, la = staged.decode(split_tokens=w.spec.block_size)          # one block per chunk
     b, lb = staged.decode(split_tokens=w.spec.block_size * w.max_blocks)   # one chunk
+    c, lc = staged.decode(split_tokens=0)                          # automatic
     ref, _ = oracle.decode_workload(w)
-    for out in (a, b):
+    for out in (a, b, c):
         max_abs, rel, _ = compare(out, ref)
         assert max_abs <= MAX_ABS and rel <= REL_L2
     assert torch.allclose(la, lb, atol=LSE_ABS, rtol=0)
+    assert torch.allclose(la, lc, atol=LSE_ABS, rtol=0)
+
+
+def test_chunk_counters_return_to_zero(staged):
+    """The in-kernel merge counts finished chunks per (sequence, kv head, head tile)
+    in the workspace and resets the counts: repeated calls on one workspace give
+    identical bits and leave the counters at zero."""
+    w = staged.w
+    s = w.spec
+    split = s.block_size * 2                                       # many chunks per sequence
+    need = kp.paged_decode_workspace_size(staged.pool, w.batch, s.q_heads, w.max_blocks, split)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(staged.q)
+        kp.paged_decode_attention(staged.pool, staged.q, staged.tables, staged.ctx, w.scale,
+                                  kv_split_tokens=split, workspace=ws, out=out)
+        outs.append(out.view(torch.int16).clone())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    g = s.q_heads // s.kv_heads
+    tiles = 1 if g <= 8 else -(-g // 16)
+    counters = ws[need - w.batch * s.kv_heads * tiles * 4:]
+    assert torch.count_nonzero(counters) == 0
 
 
 def test_block_permutation_gives_identical_bits():
@@ -111,6 +135,51 @@ def test_block_permutation_gives_identical_bits():
     out2, lse2 = st.decode(split_tokens=32)
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse1, lse2)
+    st.destroy()
+
+
+def test_block_permutation_gives_identical_bits_with_automatic_chunks():
+    w = workloads.make(SMALL["long_ragged_auto_split"])
+    st = Staged(w)
+    out1, lse1 = st.decode(split_tokens=0)
+    perm = np.random.default_rng(10).permutation(w.num_blocks)
+    kr, vr = st.pool.raw_bytes()
+    idx = torch.from_numpy(np.argsort(perm)).cuda()
+    kr.copy_(kr[idx].clone())
+    vr.copy_(vr[idx].clone())
+    st.tables = i32(np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1))
+    out2, lse2 = st.decode(split_tokens=0)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    st.destroy()
+
+
+def test_many_tiny_and_empty_sequences():
+    """Zero-length sequences between long ones; chunked and one-chunk sequences mixed."""
+    ctx = [0, 1, 0, 3000, 0, 16, 17, 0, 1, 999, 0, 0]
+    spec = C(batch=len(ctx), q_heads=8, kv_heads=2, head_dim=128, block_size=16, seed=124,
+             ctx=[max(c, 1) for c in ctx])
+    w = workloads.make(spec)
+    st = Staged(w)
+    st.ctx = i32(np.array(ctx, dtype=np.int32))
+    out, lse = st.decode(split_tokens=0)
+    live = [i for i, c in enumerate(ctx) if c > 0]
+    dead = [i for i, c in enumerate(ctx) if c == 0]
+    w2 = workloads.make(spec)
+    ref, ref_lse = oracle.decode_workload(w2, seqs=[i for i in live if ctx[i] == max(ctx[i], 1)])
+    max_abs, rel, _ = compare(out[live], ref)
+    assert max_abs <= MAX_ABS and rel <= REL_L2
+    assert torch.count_nonzero(out[dead].float()) == 0 and torch.isneginf(lse[dead]).all()
+    assert st.pool.device_errors() == 0
+    few = np.zeros(len(ctx), dtype=np.int32)
+    few[[1, 3]] = [1, 16]                    # two sequences of one block each
+    st.ctx = i32(few)
+    out3, _ = st.decode(split_tokens=0)
+    assert torch.isfinite(out3.float()).all()
+    v0 = w.seq_v(1)[0]                        # one token: the output is its value, exactly
+    want = np.repeat(v0, 4, axis=0).view(np.int16)
+    assert np.array_equal(out3[1].view(torch.int16).cpu().numpy(), want)
+    assert torch.count_nonzero(out3[[0, 2, 4]].float()) == 0
     st.destroy()
 
 

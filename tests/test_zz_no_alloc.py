@@ -60,6 +60,30 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
     st.destroy()
 
 
+def test_noalloc_automatic_chunks_match_on_two_calls():
+    """Automatic chunk size, several chunks per sequence: the in-kernel merge keeps its
+    chunk counters in the scratch."""
+    fn = _entry(kp.load_library())
+    spec = workloads.custom(batch=5, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                            ctx=[900, 17, 2500, 1, 64], seed=133)
+    w = workloads.make(spec)
+    st = Staged(w)
+    _, max_splits = kp.paged_decode_plan(st.pool, w.batch, spec.q_heads, w.max_blocks, 0)
+    assert max_splits > 1
+    ref_out, ref_lse = st.decode(split_tokens=0)
+    ref = ref_out.float().cpu().double().numpy()
+    for _ in range(2):
+        out = torch.full_like(st.q, float("nan"))
+        lse = torch.full(st.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        assert _call(fn, st, spec.q_heads, st.tables, w.max_blocks, 0, out, lse) == kp.KV_OK
+        torch.cuda.synchronize()
+        max_abs, rel, _ = compare(out, ref)
+        assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+        assert torch.allclose(lse, ref_lse, atol=LSE_ABS, rtol=0)
+    assert st.pool.device_errors() == 0
+    st.destroy()
+
+
 def test_noalloc_refuses_sizes_beyond_its_scratch():
     fn = _entry(kp.load_library())
     spec = workloads.custom(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,

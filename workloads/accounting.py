@@ -36,7 +36,7 @@ def unique_kv_tokens(w) -> int:
 
 
 def decode_bytes(w, split_tokens: int) -> dict:
-    """Algorithmic bytes of one paged_decode_attention call."""
+    """Algorithmic bytes of one paged_decode_attention call with chunks of split_tokens."""
     s = w.spec
     e = w.elem_bytes
     ctx = w.context_lens.astype(np.int64)
