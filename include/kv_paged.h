@@ -163,7 +163,7 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
  * sizes: *split_tokens (a multiple of block_size) and *max_splits (the most
  * chunks any sequence can have, ceil(max_blocks * block_size / split_tokens)).
  * kv_split_tokens: 0 = automatic (from batch, heads, max_blocks and the SM
- * count; between 16 and 64 blocks), else a positive multiple of block_size.
+ * count; between 64 and 192 blocks), else a positive multiple of block_size.
  * KV_ERR_UNSUPPORTED when max_splits would exceed 65535.  Either output may
  * be NULL.
  */

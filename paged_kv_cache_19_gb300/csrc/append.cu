@@ -15,6 +15,8 @@ namespace kvp {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams p)
 {
+    grid_dependency_wait();                        // inputs of the preceding kernel are ready
+    grid_dependents_launch();
     const int i = blockIdx.x;
     const int seq = p.token_seq != nullptr ? __ldg(p.token_seq + i) : i;
     if (seq < 0 || seq >= p.batch) {
@@ -75,8 +77,8 @@ __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
-    paged_kv_append_kernel<<<static_cast<unsigned>(p.num_tokens), 128, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(paged_kv_append_kernel, dim3(static_cast<unsigned>(p.num_tokens)),
+                            dim3(128), 0, s, p);
 }
 
 }  // namespace kvp

@@ -52,21 +52,11 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int kvh = blockIdx.x / p.head_groups;
     const int hg = blockIdx.x - kvh * p.head_groups;
     const int split = blockIdx.z;
-
-    int ctx = __ldg(p.ctx + b);
-    const int cap = p.max_blocks * BS;
-    if (ctx < 0 || ctx > cap) {
-        if (threadIdx.x == 0 && split == 0 && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    const int nblk = (ctx + BS - 1) / BS;
-    const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
-    if (split >= nsplit) return;                     // this sequence has fewer chunks
-    const int blk0 = split * p.split_blocks;
-    const int nb = max(0, min(nblk - blk0, p.split_blocks));
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int blk0 = split * p.split_blocks;
+    const int hq0 = kvh * p.group + hg * NT;           // query head of local head 0
+    const int nh = min(NT, p.group - hg * NT);         // real heads in this tile
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
@@ -75,7 +65,32 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         fence_mbar_init();
     }
-    __syncthreads();
+    grid_dependency_wait();                          // inputs of the preceding kernel are ready
+
+    // Independent loads in flight together: the context length, the chunk's
+    // first 32 table entries (producer) and the query fragments (consumers).
+    const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+    int id_first = -1;
+    if (warp == C::NCW && blk0 + lane < p.max_blocks) id_first = __ldg(trow + lane);
+    uint32_t qf[C::KS][C::NTT][2];
+    float sl2 = 0.f;
+    if (warp < C::NCW)
+        sl2 = load_q_frags<FP8, D, BS, NT>(qf, p.q + (static_cast<size_t>(b) * p.q_heads + hq0) * D,
+                                           nh, lane, p.scale_log2, p.k_scale, kvh);
+    int ctx = __ldg(p.ctx + b);
+    const int cap = p.max_blocks * BS;
+    if (ctx < 0 || ctx > cap) {
+        if (threadIdx.x == 0 && split == 0 && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int nblk = (ctx + BS - 1) / BS;
+    const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
+    const int nb = max(0, min(nblk - blk0, p.split_blocks));
+    __syncthreads();                                 // barriers initialised
+    if (split >= nsplit) {                           // this sequence has fewer chunks
+        grid_dependents_launch();
+        return;
+    }
 
     // ------------------------------------------------------------ producer warp
     if (warp == C::NCW) {
@@ -83,14 +98,13 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             prefetch_tensormap(&tmk);
             prefetch_tensormap(&tmv);
         }
-        const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
         int issued = 0;
         bool ok = true;
         for (int base = 0; base < nb && ok; base += 32) {
             const int j = base + lane;
             int id = -1;
             if (j < nb) {
-                id = __ldg(trow + j);
+                id = base == 0 ? id_first : __ldg(trow + j);
                 if (id < 0 || id >= p.num_blocks) {
                     atomicOr(p.err, KV_DEVERR_BLOCK_ID);
                     id = -1;                          // skipped: never addressed
@@ -128,6 +142,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 issued = it + 1;
             }
         }
+        grid_dependents_launch();                    // every load of this CTA is issued
         // Drain: the CTA must not exit while a copy into its shared memory is
         // in flight.  Only the last NSTAGE loads can still be pending.
         if (lane == 0) {
@@ -143,12 +158,6 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ------------------------------------------------------------ consumer warps
-    const int hq0 = kvh * p.group + hg * NT;           // query head of local head 0
-    const int nh = min(NT, p.group - hg * NT);         // real heads in this tile
-    uint32_t qf[C::KS][C::NTT][2];
-    const float sl2 = load_q_frags<FP8, D, BS, NT>(
-        qf, p.q + (static_cast<size_t>(b) * p.q_heads + hq0) * D, nh, lane, p.scale_log2,
-        p.k_scale, kvh);
     WarpState<C> st;
     reset_state(st);
 
@@ -171,6 +180,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ------------------------------------------------------------ epilogue
+    grid_dependents_launch();
     reduce_row_sums(st);
     named_barrier_sync(1, C::NCW * 32);     // every consumer is done with the stages
     float* red = reinterpret_cast<float*>(smem);
@@ -259,9 +269,9 @@ template <bool FP8, int D, int BS, int NT>
 cudaError_t launch_variant(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv,
                            const DecodeParams& p, cudaStream_t s)
 {
-    paged_decode_main<FP8, D, BS, NT>
-        <<<grid, DecodeCfg<FP8, D, BS, NT>::THREADS, GridCfg<FP8, D, BS, NT>::SMEM, s>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_dependent(paged_decode_main<FP8, D, BS, NT>, grid,
+                            dim3(DecodeCfg<FP8, D, BS, NT>::THREADS),
+                            GridCfg<FP8, D, BS, NT>::SMEM, s, tk, tv, p);
 }
 
 }  // namespace kvp

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace kvp {
 
 // One CTA of the main decode kernel covers (sequence, kv head, head group,
@@ -43,6 +45,33 @@ struct AppendParams {
     int num_tokens, batch, max_blocks, num_blocks, block_size, kv_heads, head_dim;
     int fp8;
 };
+
+// Launch with programmatic stream serialisation: the kernel may begin launching
+// while the preceding kernel in the stream finishes (it waits for that kernel
+// with griddepcontrol.wait before touching memory).  Falls back to an ordinary
+// launch where the attribute is refused.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+        cudaGetLastError();
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    }
+    return e;
+}
 
 // Query-head tile of one CTA: 8 or 16 heads of a GQA group (padding unused rows).
 inline int head_tile_for_group(int group) { return group <= 8 ? 8 : 16; }
