@@ -65,6 +65,9 @@ def _load():
             lib.kvo_decode.argtypes = [P, I, I, I, I, P, P, P, P, I, P, P, ctypes.c_double,
                                        P, I, P, P, I]
             lib.kvo_decode.restype = I
+            lib.kvo_decode_multi.argtypes = [P, I, I, I, I, I, P, P, P, P, I, P, P, ctypes.c_double,
+                                             P, I, P, P]
+            lib.kvo_decode_multi.restype = I
             _lib = lib
     return _lib
 
@@ -239,3 +242,40 @@ def pool_image(w, after_step: bool) -> tuple[np.ndarray, np.ndarray]:
                      w.context_lens, k_scale=w.k_scale, v_scale=w.v_scale)
         assert bad == 0
     return kp, vp
+
+
+def decode_multi(q, k, v, seq_start, context_lens, *, q_heads: int, q_len: int, kv_heads: int,
+                 head_dim: int, scale: float, cache_dtype: str = "bf16", k_scale=None,
+                 v_scale=None, seqs=None):
+    """Attention of q_len new tokens per sequence (causal among themselves).
+
+    q: uint16 bf16 [B, Hq, q_len, d]; the last q_len cached tokens of each sequence are the
+    new ones.  Returns (out float64 [n, Hq, q_len, d], lse float64 [n, Hq, q_len]).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    ss = _c(seq_start, np.int64)
+    cl = _c(context_lens, np.int32)
+    batch = cl.shape[0]
+    sl = None if seqs is None else _c(seqs, np.int32)
+    n = batch if sl is None else sl.shape[0]
+    out = np.zeros((n, q_heads, q_len, head_dim), dtype=np.float64)
+    lse = np.zeros((n, q_heads, q_len), dtype=np.float64)
+    rc = lib.kvo_decode_multi(_ptr(q), batch, q_heads, q_len, kv_heads, head_dim, _ptr(k), _ptr(v),
+                              _ptr(ss), _ptr(cl), _DTYPE[cache_dtype],
+                              _ptr(_c(k_scale, np.float32)), _ptr(_c(v_scale, np.float32)),
+                              float(scale), _ptr(sl), n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("bad multi-query arguments")
+    return out, lse
+
+
+def decode_multi_workload(w, q_multi, q_len: int, seqs=None, cache_dtype: str | None = None):
+    """Oracle attention of q_len new tokens per sequence of a workload (q_multi [B, Hq, q_len, d])."""
+    s = w.spec
+    return decode_multi(q_multi, w.k, w.v, w.seq_start, w.context_lens, q_heads=s.q_heads,
+                        q_len=q_len, kv_heads=s.kv_heads, head_dim=s.head_dim, scale=w.scale,
+                        cache_dtype=cache_dtype or s.cache_dtype, k_scale=w.k_scale,
+                        v_scale=w.v_scale, seqs=seqs)

@@ -19,6 +19,9 @@
  *       speculative decoding" -- section 3 notation (g = a / n_kv query heads per
  *       KV head) and "PagedAttention (4.1-4.3)" (block-by-block reads merged by
  *       the online-softmax update; split-KV decoding in section 6).
+ *  [P4] 4yush.com "The KV cache and the systems around it" -- "Why the keys and
+ *       values never change": with `start` cached tokens and T new ones, new token
+ *       r sits at position start + r and sees keys 0 .. start + r.
  *  [P5] kongchang.com "Core Mechanics of LLM Inference Serving" -- GQA: 32 query
  *       heads in 8 groups of 4 sharing one KV head.
  *
@@ -409,5 +412,63 @@ int kvo_decode(const uint16_t* q, int batch, int q_heads, int kv_heads, int head
     decode_worker(&J);
     for (int i = 1; i < threads; ++i) pthread_join(tid[i], NULL);
     pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Several new tokens per sequence ([P1] "A KV cache in PyTorch": attn_cached  */
+/* with the shifted mask tril(diagonal = T - t); 4yush.com "Why the keys and   */
+/* values never change": the new token r is at position start + r and sees    */
+/* keys 0 .. start + r)                                                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * q: bf16 [batch, q_heads, q_len, d]; the sequence's last q_len cached tokens
+ * are the new ones, so query i sits at position ctx - q_len + i and attends
+ * over the contiguous prefix of ctx - q_len + i + 1 tokens.  Results in list
+ * order: out [n_list, q_heads, q_len, d], lse [n_list, q_heads, q_len].
+ * A query whose position is negative (ctx < q_len) attends to nothing.
+ */
+int kvo_decode_multi(const uint16_t* q, int batch, int q_heads, int q_len, int kv_heads,
+                     int head_dim, const uint16_t* k, const uint16_t* v,
+                     const int64_t* seq_start, const int32_t* context_lens, int dtype,
+                     const float* k_scale, const float* v_scale, double scale,
+                     const int32_t* seq_list, int n_list, double* out, double* lse)
+{
+    if (kv_heads <= 0 || q_heads % kv_heads != 0 || q_len <= 0) return -1;
+    decode_job J;
+    J.q = q; J.batch = batch; J.q_heads = q_heads; J.kv_heads = kv_heads; J.head_dim = head_dim;
+    J.k = k; J.v = v; J.seq_start = seq_start; J.ctx = context_lens;
+    J.dtype = dtype; J.k_scale = k_scale; J.v_scale = v_scale; J.scale = scale;
+    int n = seq_list ? n_list : batch;
+    size_t row = (size_t)kv_heads * head_dim;
+    double* qi = (double*)malloc(sizeof(double) * (size_t)q_heads * head_dim);
+    double* oi = (double*)malloc(sizeof(double) * (size_t)q_heads * head_dim);
+    double* li = (double*)malloc(sizeof(double) * (size_t)q_heads);
+    for (int idx = 0; idx < n; ++idx) {
+        int b = seq_list ? seq_list[idx] : idx;
+        int ctx = context_lens[b];
+        size_t cnt = (size_t)(ctx > 0 ? ctx : 1) * row;
+        double* kd = (double*)malloc(sizeof(double) * cnt);
+        double* vd = (double*)malloc(sizeof(double) * cnt);
+        if (ctx > 0) load_sequence(&J, b, kd, vd);
+        for (int i = 0; i < q_len; ++i) {
+            int visible = ctx - q_len + i + 1;          /* keys 0 .. position of query i */
+            if (visible < 0) visible = 0;
+            for (int h = 0; h < q_heads; ++h)
+                for (int c = 0; c < head_dim; ++c)
+                    qi[(size_t)h * head_dim + c] = kvo_bf16_value(
+                        q[(((size_t)b * q_heads + h) * q_len + i) * head_dim + c]);
+            kvo_attend(qi, q_heads, kv_heads, head_dim, kd, vd, visible, scale, oi, li);
+            for (int h = 0; h < q_heads; ++h) {
+                for (int c = 0; c < head_dim; ++c)
+                    out[(((size_t)idx * q_heads + h) * q_len + i) * head_dim + c] =
+                        oi[(size_t)h * head_dim + c];
+                if (lse) lse[((size_t)idx * q_heads + h) * q_len + i] = li[h];
+            }
+        }
+        free(kd); free(vd);
+    }
+    free(qi); free(oi); free(li);
     return 0;
 }

@@ -350,3 +350,48 @@ def test_fp8_decode_uses_dequantised_codes():
     blk, slot = w.block_tables[1, 19 // 8], 19 % 8
     assert np.array_equal(kp[blk, slot, 0],
                           oracle.e4m3_quantize(w.seq_k(1)[19, 0], w.k_scale[0]))
+
+
+# --------------------------------------------------------------------------- several new tokens
+def test_multi_query_visibility_matches_the_printed_masks():
+    """With q = 0 every visible key gets the same weight; one-hot values reveal which keys."""
+    rows = _read_golden("p4_shifted_masks.txt")
+    assert len(rows) == 2
+    for start, T, masks in rows:
+        start, T = int(start), int(T)
+        want = np.array([[int(ch) for ch in m] for m in masks.split(";")], dtype=float)
+        ctx = start + T
+        d = 8
+        v = np.zeros((ctx, 1, d), dtype=np.uint16)
+        for t in range(ctx):                                # one-hot rows (bf16 1.0 = 0x3F80)
+            v[t, 0, t] = 0x3F80
+        k = _bf16((ctx, 1, d), 50)
+        q = np.zeros((1, 1, T, d), dtype=np.uint16)
+        out, _ = oracle.decode_multi(q, k, v, np.array([0]), np.array([ctx], np.int32), q_heads=1,
+                                     q_len=T, kv_heads=1, head_dim=d, scale=0.5)
+        seen = (out[0, 0, :, :ctx] > 0).astype(float)
+        assert np.array_equal(seen, want)
+        assert np.allclose(out[0, 0, :, :ctx].sum(axis=1), 1.0)
+
+
+@pytest.mark.parametrize("hq,hkv,t", [(4, 4, 3), (8, 2, 5)])
+def test_multi_query_equals_the_last_rows_of_full_causal_attention(hq, hkv, t):
+    T, d = 29, 16
+    Q = _f64(_bf16((T, hq, d), 51))
+    Kb, Vb = _bf16((T, hkv, d), 52), _bf16((T, hkv, d), 53)
+    K, V = _f64(Kb), _f64(Vb)
+    g = hq // hkv
+    full = _sdpa_causal(Q.transpose(1, 0, 2).copy(), np.repeat(K, g, axis=1).transpose(1, 0, 2).copy(),
+                        np.repeat(V, g, axis=1).transpose(1, 0, 2).copy())           # [hq, T, d]
+    qb = _bf16((T, hq, d), 51)[T - t:].transpose(1, 0, 2)[None].copy()              # [1, hq, t, d]
+    out, _ = oracle.decode_multi(qb, Kb, Vb, np.array([0]), np.array([T], np.int32), q_heads=hq,
+                                 q_len=t, kv_heads=hkv, head_dim=d, scale=1 / math.sqrt(d))
+    assert np.max(np.abs(out[0] - full[:, T - t:])) < 1e-13
+
+
+def test_multi_query_of_one_token_is_the_decode():
+    w = workloads.make(workloads.custom(batch=3, q_heads=8, kv_heads=2, head_dim=16, block_size=8,
+                                        ctx=[1, 9, 30], seed=54))
+    a, la = oracle.decode_workload(w)
+    b, lb = oracle.decode_multi_workload(w, w.q[:, :, None, :], 1)
+    assert np.array_equal(a, b[:, :, 0]) and np.array_equal(la, lb[:, :, 0])
