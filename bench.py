@@ -215,6 +215,7 @@ def workload_config(w, split_tokens, max_splits, world):
     return {
         "workload": s.name, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
         "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": s.cache_dtype,
+        "q_len": s.q_len,
         "context_tokens": w.total_tokens, "ctx_min": int(w.context_lens.min()),
         "ctx_max": int(w.context_lens.max()), "num_blocks": w.num_blocks,
         "split_tokens": split_tokens, "max_splits": max_splits,
@@ -356,7 +357,11 @@ def stage(w, device):
         kp.paged_kv_append(pool, bf16(w.k[rows]), bf16(w.v[rows]), tables, ctx,
                            token_seq=i32(w.prefill_seq[a:a + chunk]),
                            token_pos=i32(w.prefill_pos[a:a + chunk]))
-    return pool, tables, ctx, bf16(w.q), bf16(w.k_new), bf16(w.v_new)
+    step = {"q": bf16(w.q if w.q_len == 1 else w.q_multi), "k": bf16(w.k[w.step_rows]),
+            "v": bf16(w.v[w.step_rows]),
+            "seq": None if w.q_len == 1 else i32(w.step_seq),
+            "pos": None if w.q_len == 1 else i32(w.step_pos)}
+    return pool, tables, ctx, step
 
 
 def run_ours(args, rank, world, local):
@@ -370,18 +375,30 @@ def run_ours(args, rank, world, local):
     w = workloads.make(rank_spec(args.config, rank))
     s = w.spec
     split_req = s.split_tokens if args.split_tokens is None else args.split_tokens
-    pool, tables, ctx, q, k_new, v_new = stage(w, device)
+    pool, tables, ctx, stp = stage(w, device)
+    q = stp["q"]
     split_tokens, max_splits = kp.paged_decode_plan(pool, s.batch, s.q_heads, w.max_blocks, split_req)
-    ws_bytes = kp.paged_decode_workspace_size(pool, s.batch, s.q_heads, w.max_blocks, split_req)
+    ws_bytes = kp.paged_multi_query_workspace_size(pool, s.batch, s.q_heads, s.q_len, w.max_blocks,
+                                                   split_req)
     workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=device)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
 
+    def attend(qq, tt, cc):
+        if s.q_len == 1:
+            kp.paged_decode_attention(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
+                                      workspace=workspace, out=out, lse=lse, stream=stream)
+        else:
+            kp.paged_attention_multi_query(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
+                                           workspace=workspace, out=out, lse=lse, stream=stream)
+
+    def append(kk, vv, tt, cc, sq, ps):
+        kp.paged_kv_append(pool, kk, vv, tt, cc, token_seq=sq, token_pos=ps, stream=stream)
+
     def step():
-        kp.paged_kv_append(pool, k_new, v_new, tables, ctx, stream=stream)
-        kp.paged_decode_attention(pool, q, tables, ctx, w.scale, kv_split_tokens=split_req,
-                                  workspace=workspace, out=out, lse=lse, stream=stream)
+        append(stp["k"], stp["v"], tables, ctx, stp["seq"], stp["pos"])
+        attend(q, tables, ctx)
 
     dec_bytes = accounting.decode_bytes(w, split_tokens)
     app_bytes = accounting.append_bytes(w)
@@ -426,8 +443,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     d_start.record(stream)
     for _ in range(args.steps):
-        kp.paged_decode_attention(pool, q, tables, ctx, w.scale, kv_split_tokens=split_req,
-                                  workspace=workspace, out=out, lse=lse, stream=stream)
+        attend(q, tables, ctx)
     d_end.record(stream)
     torch.cuda.synchronize()
     dec_avg_ms = d_start.elapsed_time(d_end) / args.steps
@@ -449,8 +465,10 @@ def run_ours(args, rank, world, local):
     # ---- end to end: host (pinned) inputs copied in and the output copied out every step
     e2e = None
     if not args.no_e2e:
-        h = {name: t.cpu().pin_memory() for name, t in
-             (("q", q), ("k_new", k_new), ("v_new", v_new), ("tables", tables), ("ctx", ctx))}
+        inputs = [("q", q), ("k", stp["k"]), ("v", stp["v"]), ("tables", tables), ("ctx", ctx)]
+        if stp["seq"] is not None:
+            inputs += [("seq", stp["seq"]), ("pos", stp["pos"])]
+        h = {name: t.cpu().pin_memory() for name, t in inputs}
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         d = {name: torch.empty_like(t, device=device) for name, t in h.items()}
         bi = sum(t.numel() * t.element_size() for t in h.values())
@@ -459,10 +477,8 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for name in d:
                 d[name].copy_(h[name], non_blocking=True)
-            kp.paged_kv_append(pool, d["k_new"], d["v_new"], d["tables"], d["ctx"], stream=stream)
-            kp.paged_decode_attention(pool, d["q"], d["tables"], d["ctx"], w.scale,
-                                      kv_split_tokens=split_req, workspace=workspace, out=out,
-                                      lse=lse, stream=stream)
+            append(d["k"], d["v"], d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
+            attend(d["q"], d["tables"], d["ctx"])
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(max(3, args.warmup)):
@@ -482,7 +498,7 @@ def run_ours(args, rank, world, local):
                "ms_per_step": round(e2e_ms / args.steps, 5)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and s.q_len == 1:
         cpu = cpu_baseline(w, args.cpu_seconds, gpu_out=out)
 
     if rank == 0:

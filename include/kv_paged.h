@@ -217,6 +217,37 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
                                  void* out, float* lse_out, void* stream);
 
 /*
+ * paged_attention_multi_query -- attention of q_len new tokens per sequence
+ * over the paged cache: the verify pass of speculative decoding (the target
+ * model scores the draft's guesses in one pass) and the chunks of a chunked
+ * prefill.  The q_len new tokens must already be appended; query token i of
+ * sequence b sits at position context_lens[b] - q_len + i and attends to keys
+ * 0 .. that position -- the shifted causal mask of cached attention
+ * (xuewyang.github.io/posts/kv, "A KV cache in PyTorch"; 4yush.com "The KV
+ * cache and the systems around it", section "Why the keys and values never
+ * change").
+ *   q: bf16 [batch, q_heads, q_len, head_dim]; out: bf16 [batch, q_heads,
+ *   q_len, head_dim]; lse_out: optional float32 [batch, q_heads, q_len].
+ *   The g = q_heads / kv_heads heads of a group and the q_len query tokens
+ *   (g * q_len rows, at most 4096) share each read of a K/V block.
+ *   context_lens[b] < q_len (but > 0) is a device-side error
+ *   (KV_DEVERR_CONTEXT); queries whose position would be negative attend to
+ *   nothing.  Everything else (tables, split, workspace, errors) as in
+ *   paged_decode_attention, which is this call with q_len == 1.
+ */
+kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_heads, int q_len,
+                                      const int32_t* block_tables, int max_blocks,
+                                      const int32_t* context_lens, int batch, float scale,
+                                      int kv_split_tokens, void* workspace,
+                                      size_t workspace_bytes, void* out, float* lse_out,
+                                      void* stream);
+
+/* Workspace bytes of paged_attention_multi_query for these sizes. */
+kv_status paged_multi_query_workspace_size(const kv_pool* pool, int batch, int q_heads,
+                                           int q_len, int max_blocks, int kv_split_tokens,
+                                           size_t* bytes);
+
+/*
  * Allocation-free decode attention.  The paper has no counterpart to this call;
  * it exists for users of this library who cannot allocate device memory at the
  * call site: plug-in hosts that give a kernel only its input and output

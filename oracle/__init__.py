@@ -238,8 +238,10 @@ def pool_image(w, after_step: bool) -> tuple[np.ndarray, np.ndarray]:
                      token_pos=w.prefill_pos, k_scale=w.k_scale, v_scale=w.v_scale)
         assert bad == 0
     if after_step:
-        bad = append(kp, vp, s.cache_dtype, s.block_size, w.k_new, w.v_new, w.block_tables,
-                     w.context_lens, k_scale=w.k_scale, v_scale=w.v_scale)
+        rows = w.step_rows
+        bad = append(kp, vp, s.cache_dtype, s.block_size, w.k[rows], w.v[rows], w.block_tables,
+                     w.context_lens, token_seq=w.step_seq, token_pos=w.step_pos,
+                     k_scale=w.k_scale, v_scale=w.v_scale)
         assert bad == 0
     return kp, vp
 

@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
-    "paged_decode_workspace_size", "paged_decode_attention", "library_path", "load_library",
+    "paged_decode_workspace_size", "paged_decode_attention", "paged_attention_multi_query",
+    "paged_multi_query_workspace_size", "library_path", "load_library",
     "DEVERR_BLOCK_ID", "DEVERR_CONTEXT", "DEVERR_SEQ", "DEVERR_POSITION", "DEVERR_TIMEOUT",
 ]
 
@@ -77,6 +78,9 @@ def load_library():
             "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
+            "paged_attention_multi_query": ([P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
+                                             P], I),
+            "paged_multi_query_workspace_size": ([P, I, I, I, I, I, ctypes.POINTER(S)], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -262,4 +266,48 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
                                       float(scale), int(kv_split_tokens), _ptr(workspace),
                                       int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
            "paged_decode_attention")
+    return out
+
+
+def paged_multi_query_workspace_size(pool: Pool, batch: int, q_heads: int, q_len: int,
+                                     max_blocks: int, kv_split_tokens: int = 0) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t()
+    _check(lib.paged_multi_query_workspace_size(pool.handle, int(batch), int(q_heads), int(q_len),
+                                                int(max_blocks), int(kv_split_tokens),
+                                                ctypes.byref(n)),
+           "paged_multi_query_workspace_size")
+    return n.value
+
+
+def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale: float | None = None,
+                                kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
+                                stream=None):
+    """Attention of q_len new tokens per sequence; q bf16 [B, Hq, q_len, d].  Returns out."""
+    lib = load_library()
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, q_heads, q_len, head_dim]")
+    batch, q_heads, q_len, d = q.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = paged_multi_query_workspace_size(pool, batch, q_heads, q_len, max_blocks,
+                                                kv_split_tokens)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_attention_multi_query(pool.handle, _ptr(q), int(q_heads), int(q_len),
+                                           _ptr(block_tables), int(max_blocks), _ptr(context_lens),
+                                           int(batch), float(scale), int(kv_split_tokens),
+                                           _ptr(workspace), int(ws_bytes), _ptr(out), _ptr(lse),
+                                           _stream(stream)),
+           "paged_attention_multi_query")
     return out

@@ -105,7 +105,7 @@ kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map)
 }
 
 struct Plan {
-    int group, head_tile, head_groups, split_blocks, max_splits;
+    int group, rows, head_tile, head_groups, split_blocks, max_splits;
 };
 
 // Split-KV plan.  Automatic chunk size: about eight chunks per SM over the
@@ -114,19 +114,22 @@ struct Plan {
 // short enough that the last CTAs to start (the remainder chunks, launched
 // last) end soon.  Measured on GB300 for the Llama-3-8B-shaped, ragged and
 // long-context batches, the best chunks lie between 96 and 256 blocks.
-kv_status make_plan(const kv_pool* pl, int batch, int q_heads, int max_blocks, int split_tokens,
-                    Plan* out)
+kv_status make_plan(const kv_pool* pl, int batch, int q_heads, int q_len, int max_blocks,
+                    int split_tokens, Plan* out)
 {
-    if (pl == nullptr || batch < 0 || q_heads <= 0 || max_blocks <= 0 || split_tokens < 0)
+    if (pl == nullptr || batch < 0 || q_heads <= 0 || q_len <= 0 || max_blocks <= 0 ||
+        split_tokens < 0)
         return KV_ERR_INVALID_ARG;
     if (q_heads % pl->kv_heads != 0) return KV_ERR_INVALID_ARG;
     if (split_tokens % pl->block_size != 0) return KV_ERR_INVALID_ARG;
     if (static_cast<long long>(max_blocks) * pl->block_size > std::numeric_limits<int>::max())
         return KV_ERR_INVALID_ARG;
+    if (static_cast<long long>(q_heads / pl->kv_heads) * q_len > 4096) return KV_ERR_UNSUPPORTED;
     Plan p;
     p.group = q_heads / pl->kv_heads;
-    p.head_tile = kvp::head_tile_for_group(p.group);
-    p.head_groups = (p.group + p.head_tile - 1) / p.head_tile;
+    p.rows = p.group * q_len;
+    p.head_tile = kvp::head_tile_for_group(p.rows);
+    p.head_groups = (p.rows + p.head_tile - 1) / p.head_tile;
     if (split_tokens > 0) {
         p.split_blocks = split_tokens / pl->block_size;
     } else {
@@ -153,11 +156,11 @@ struct WorkspaceLayout {
     size_t part_o, part_ml, tickets, ticket_bytes, total;
 };
 
-WorkspaceLayout workspace_layout(const kv_pool* pl, int batch, int q_heads, const Plan& p)
+WorkspaceLayout workspace_layout(const kv_pool* pl, int batch, const Plan& p)
 {
     WorkspaceLayout w{0, 0, 0, 0, 0};
     if (p.max_splits <= 1) return w;
-    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
+    const size_t n = static_cast<size_t>(batch) * pl->kv_heads * p.rows * p.max_splits;
     w.part_ml = round_up(n * pl->head_dim * sizeof(float), kAlign);
     w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
     w.ticket_bytes = static_cast<size_t>(batch) * pl->kv_heads * p.head_groups * sizeof(int);
@@ -165,9 +168,9 @@ WorkspaceLayout workspace_layout(const kv_pool* pl, int batch, int q_heads, cons
     return w;
 }
 
-size_t workspace_bytes_for(const kv_pool* pl, int batch, int q_heads, const Plan& p)
+size_t workspace_bytes_for(const kv_pool* pl, int batch, const Plan& p)
 {
-    return workspace_layout(pl, batch, q_heads, p).total;
+    return workspace_layout(pl, batch, p).total;
 }
 
 kv_status check_device(const kv_pool* pl)
@@ -392,32 +395,41 @@ kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max
                             int kv_split_tokens, int* split_tokens, int* max_splits)
 {
     Plan p;
-    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    kv_status st = make_plan(pool, batch, q_heads, 1, max_blocks, kv_split_tokens, &p);
     if (st != KV_OK) return st;
     if (split_tokens) *split_tokens = p.split_blocks * pool->block_size;
     if (max_splits) *max_splits = p.max_splits;
     return KV_OK;
 }
 
-kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_heads,
-                                      int max_blocks, int kv_split_tokens, size_t* bytes)
+kv_status paged_multi_query_workspace_size(const kv_pool* pool, int batch, int q_heads,
+                                           int q_len, int max_blocks, int kv_split_tokens,
+                                           size_t* bytes)
 {
     if (bytes == nullptr) return KV_ERR_INVALID_ARG;
     Plan p;
-    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    kv_status st = make_plan(pool, batch, q_heads, q_len, max_blocks, kv_split_tokens, &p);
     if (st != KV_OK) return st;
-    *bytes = workspace_bytes_for(pool, batch, q_heads, p);
+    *bytes = workspace_bytes_for(pool, batch, p);
     return KV_OK;
 }
 
-kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads,
-                                 const int32_t* block_tables, int max_blocks,
-                                 const int32_t* context_lens, int batch, float scale,
-                                 int kv_split_tokens, void* workspace, size_t workspace_bytes,
-                                 void* out, float* lse_out, void* stream)
+kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_heads,
+                                      int max_blocks, int kv_split_tokens, size_t* bytes)
+{
+    return paged_multi_query_workspace_size(pool, batch, q_heads, 1, max_blocks, kv_split_tokens,
+                                            bytes);
+}
+
+kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_heads, int q_len,
+                                      const int32_t* block_tables, int max_blocks,
+                                      const int32_t* context_lens, int batch, float scale,
+                                      int kv_split_tokens, void* workspace,
+                                      size_t workspace_bytes, void* out, float* lse_out,
+                                      void* stream)
 {
     Plan plan;
-    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
+    kv_status st = make_plan(pool, batch, q_heads, q_len, max_blocks, kv_split_tokens, &plan);
     if (st != KV_OK) return st;
     if (batch == 0) return KV_OK;
     if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
@@ -428,12 +440,12 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
         return KV_ERR_INVALID_ARG;
     if (batch > 65535 || static_cast<long long>(pool->kv_heads) * plan.head_groups > 65535)
         return KV_ERR_UNSUPPORTED;                  // grid x / y limits
-    const size_t need = workspace_bytes_for(pool, batch, q_heads, plan);
+    const size_t need = workspace_bytes_for(pool, batch, plan);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KV_ERR_INVALID_ARG;
     st = check_device(pool);
     if (st != KV_OK) return st;
 
-    const WorkspaceLayout wl = workspace_layout(pool, batch, q_heads, plan);
+    const WorkspaceLayout wl = workspace_layout(pool, batch, plan);
     kvp::DecodeParams p;
     p.q = static_cast<const uint16_t*>(q);
     p.tables = block_tables;
@@ -452,6 +464,8 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     p.kv_heads = pool->kv_heads;
     p.group = plan.group;
     p.head_groups = plan.head_groups;
+    p.q_len = q_len;
+    p.rows = plan.rows;
     p.max_blocks = max_blocks;
     p.num_blocks = pool->num_blocks;
     p.split_blocks = plan.split_blocks;
@@ -459,7 +473,7 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     p.scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // chunk-major grid: x = (kv head, head tile), y = sequence, z = chunk
+    // chunk-major grid: x = (kv head, row tile), y = sequence, z = chunk
     const dim3 grid(static_cast<unsigned>(pool->kv_heads * plan.head_groups),
                     static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));
     cudaError_t e = pool->dtype == KV_DTYPE_BF16
@@ -467,8 +481,18 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
                                                   grid, pool->tmk, pool->tmv, p, s)
                         : kvp::launch_decode_fp8(pool->head_dim, pool->block_size, plan.head_tile,
                                                  grid, pool->tmk, pool->tmv, p, s);
-    if (e != cudaSuccess) return KV_ERR_CUDA;
-    return KV_OK;
+    return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                 const int32_t* block_tables, int max_blocks,
+                                 const int32_t* context_lens, int batch, float scale,
+                                 int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                 void* out, float* lse_out, void* stream)
+{
+    return paged_attention_multi_query(pool, q, q_heads, 1, block_tables, max_blocks,
+                                       context_lens, batch, scale, kv_split_tokens, workspace,
+                                       workspace_bytes, out, lse_out, stream);
 }
 
 }  // extern "C"
@@ -519,10 +543,10 @@ extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const v
                                                     float* lse_out, void* stream)
 {
     Plan plan;
-    kv_status st = make_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
+    kv_status st = make_plan(pool, batch, q_heads, 1, max_blocks, kv_split_tokens, &plan);
     if (st != KV_OK) return st;
     if (batch == 0) return KV_OK;
-    const size_t need = workspace_bytes_for(pool, batch, q_heads, plan);
+    const size_t need = workspace_bytes_for(pool, batch, plan);
     if (need > KV_NO_ALLOC_SCRATCH_BYTES) return KV_ERR_UNSUPPORTED;
     st = check_device(pool);
     if (st != KV_OK) return st;
@@ -532,7 +556,7 @@ extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const v
         if (st != KV_OK) return st;
         // The per-unit chunk counts in the scratch must start at zero, whatever
         // an earlier (possibly failed) call left there.
-        const WorkspaceLayout wl = workspace_layout(pool, batch, q_heads, plan);
+        const WorkspaceLayout wl = workspace_layout(pool, batch, plan);
         if (wl.ticket_bytes > 0 &&
             cudaMemsetAsync(static_cast<uint8_t*>(scratch) + wl.tickets, 0, wl.ticket_bytes,
                             static_cast<cudaStream_t>(stream)) != cudaSuccess) {

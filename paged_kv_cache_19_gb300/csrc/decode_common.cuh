@@ -32,7 +32,10 @@ struct DecodeCfg {
     static constexpr int DCH = ROWB / 128;          // 128-byte swizzle rows per token
     static constexpr int TILE = BS * ROWB;          // bytes of one K (or V) block tile
     static constexpr int STAGE = 2 * TILE;          // K tile then V tile
-    static constexpr int NSTAGE = STAGE >= 16384 ? 4 : (STAGE >= 8192 ? 8 : 16);
+    // About 64 KB of stages for 8-row tiles (3 CTAs per SM) and 96 KB for 16-row
+    // tiles, whose registers allow only 2 CTAs per SM: ~192 KB in flight per SM.
+    static constexpr int RING = NT == 8 ? 64 * 1024 : 96 * 1024;
+    static constexpr int NSTAGE = (RING / STAGE) / 4 * 4 >= 4 ? (RING / STAGE) / 4 * 4 : 4;
     static constexpr int NCW = 4;                   // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
     static constexpr int MT = BS / 16;              // 16-token tiles per block
@@ -148,16 +151,34 @@ __device__ __forceinline__ float load_q_frags(uint32_t (&qf)[D / 16][NT / 8][2],
     }
 }
 
+// Causal offsets of the rows this thread's accumulator columns belong to: row
+// r (query token i = r % q_len) sees one token fewer than the sequence's last
+// query for every later query token: dt = q_len - 1 - i.  Zero for decode.
+template <int NTT>
+__device__ __forceinline__ void row_offsets(int (&dt)[NTT][2], int row0, int q_len, int lane)
+{
+    const int c = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) dt[nt][j] = q_len - 1 - (row0 + nt * 8 + 2 * c + j) % q_len;
+}
+
 // One cache block (BS tokens of one kv head, K tile at tk, V tile at tv in
-// shared memory) folded into the warp's online-softmax state.
+// shared memory) folded into the warp's online-softmax state.  lim = ctx minus
+// the block's first token position (may exceed BS): token k of the block is a
+// key for a row with causal offset dt when k < lim - dt; tokens at or past
+// lim are not in the cache at all and their values are never used.
 template <bool FP8, int D, int BS, int NT>
-__device__ __forceinline__ void process_block(uint32_t tk, uint32_t tv, int nvalid,
+__device__ __forceinline__ void process_block(uint32_t tk, uint32_t tv, int lim,
+                                              const int (&dt)[NT / 8][2],
                                               const uint32_t (&qf)[D / 16][NT / 8][2], float sl2,
                                               WarpState<DecodeCfg<FP8, D, BS, NT>>& st, int lane)
 {
     using C = DecodeCfg<FP8, D, BS, NT>;
     const int r = lane >> 2;
     const int c = lane & 3;
+    const int nvalid = min(BS, lim);
 
     // ---- scores S^T[tokens x heads] = K . Q^T
     float s[C::MT][C::NTT][4];
@@ -213,7 +234,7 @@ __device__ __forceinline__ void process_block(uint32_t tk, uint32_t tv, int nval
 #pragma unroll
                 for (int hi = 0; hi < 2; ++hi) {
                     const int tok = mt * 16 + r + 8 * hi;
-                    const float x = tok < nvalid ? s[mt][nt][2 * hi + j] * sl2 : -INFINITY;
+                    const float x = tok < lim - dt[nt][j] ? s[mt][nt][2 * hi + j] * sl2 : -INFINITY;
                     s[mt][nt][2 * hi + j] = x;
                     mx = fmaxf(mx, x);
                 }

@@ -55,8 +55,9 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int blk0 = split * p.split_blocks;
-    const int hq0 = kvh * p.group + hg * NT;           // query head of local head 0
-    const int nh = min(NT, p.group - hg * NT);         // real heads in this tile
+    const int nh = min(NT, p.rows - hg * NT);          // real rows in this tile
+    // global query row of local row 0 (rows = heads of the group x query tokens)
+    const size_t row0 = (static_cast<size_t>(b) * p.kv_heads + kvh) * p.rows + hg * NT;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NSTAGE; ++i) {
@@ -74,14 +75,19 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (warp == C::NCW && blk0 + lane < p.max_blocks) id_first = __ldg(trow + lane);
     uint32_t qf[C::KS][C::NTT][2];
     float sl2 = 0.f;
-    if (warp < C::NCW)
-        sl2 = load_q_frags<FP8, D, BS, NT>(qf, p.q + (static_cast<size_t>(b) * p.q_heads + hq0) * D,
-                                           nh, lane, p.scale_log2, p.k_scale, kvh);
+    int dt[C::NTT][2];
+    if (warp < C::NCW) {
+        sl2 = load_q_frags<FP8, D, BS, NT>(qf, p.q + row0 * D, nh, lane, p.scale_log2, p.k_scale,
+                                           kvh);
+        row_offsets<C::NTT>(dt, hg * NT, p.q_len, lane);
+    }
     int ctx = __ldg(p.ctx + b);
     const int cap = p.max_blocks * BS;
-    if (ctx < 0 || ctx > cap) {
+    if (ctx < 0 || ctx > cap || (ctx > 0 && ctx < p.q_len)) {
+        // out of range (clamped), or fewer cached tokens than new queries (kept:
+        // the queries at negative positions attend to nothing)
         if (threadIdx.x == 0 && split == 0 && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
-        ctx = ctx < 0 ? 0 : cap;
+        ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     }
     const int nblk = (ctx + BS - 1) / BS;
     const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
@@ -171,9 +177,9 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         const int blk = stage_blk[s];
         if (blk >= 0) {
-            const int nvalid = min(BS, ctx - (blk0 + it) * BS);
             const uint32_t tk = smem_u32(smem + s * C::STAGE);
-            process_block<FP8, D, BS, NT>(tk, tk + C::TILE, nvalid, qf, sl2, st, lane);
+            process_block<FP8, D, BS, NT>(tk, tk + C::TILE, ctx - (blk0 + it) * BS, dt, qf, sl2,
+                                          st, lane);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
@@ -190,7 +196,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int t = threadIdx.x;
     const int head = (t * C::E) / D;
     const int d0 = (t * C::E) % D;
-    const size_t bh = static_cast<size_t>(b) * p.q_heads + hq0 + head;
+    const size_t bh = row0 + head;                   // global query row
     if (head < nh) {
         float acc[C::E], M, L;
         combine_warps<C>(red, head, d0, FP8 ? __ldg(p.v_scale + kvh) : 1.f, acc, M, L);

@@ -12,19 +12,24 @@ namespace kvp {
 
 // One CTA of the main decode kernel covers (sequence, kv head, head group,
 // split).  All pointers are device pointers.
+// Query rows: q and out are [batch, q_heads, q_len, head_dim], i.e. rows
+// (b * kv_heads + kvh) * rows + r with rows = group * q_len per kv head and
+// r = (head in the group) * q_len + (query token).  Query token i of a
+// sequence sits at position ctx - q_len + i and sees keys 0 .. that position.
 struct DecodeParams {
-    const uint16_t* q;        // bf16 [batch, q_heads, head_dim]
+    const uint16_t* q;        // bf16 [batch, q_heads, q_len, head_dim]
     const int32_t* tables;    // [batch, max_blocks]
     const int32_t* ctx;       // [batch]
     const float* k_scale;     // [kv_heads] (fp8 cache)
     const float* v_scale;     // [kv_heads] (fp8 cache)
-    uint16_t* out;            // bf16 [batch, q_heads, head_dim]
-    float* lse;               // [batch, q_heads] or null
-    float* part_o;            // [batch, q_heads, max_splits, head_dim]
-    float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum) in log2 units
+    uint16_t* out;            // bf16 [batch, q_heads, q_len, head_dim]
+    float* lse;               // [batch, q_heads, q_len] or null
+    float* part_o;            // [batch, q_heads, q_len, max_splits, head_dim]
+    float* part_ml;           // [batch, q_heads, q_len, max_splits, 2]: (max, sum), log2 units
     uint32_t* err;            // device error word
     int* tickets;             // per-unit count of finished chunks; zero between calls
     int batch, q_heads, kv_heads, group, head_groups;
+    int q_len, rows;          // query tokens per sequence; rows per kv head = group * q_len
     int max_blocks, num_blocks;
     int split_blocks, max_splits;
     float scale_log2;         // softmax scale * log2(e)
@@ -73,8 +78,8 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return e;
 }
 
-// Query-head tile of one CTA: 8 or 16 heads of a GQA group (padding unused rows).
-inline int head_tile_for_group(int group) { return group <= 8 ? 8 : 16; }
+// Row tile of one CTA: 8 or 16 query rows of a kv head (padding unused rows).
+inline int head_tile_for_group(int rows) { return rows <= 8 ? 8 : 16; }
 
 // Dynamic shared memory of one main-kernel CTA (stages + barriers + alignment
 // slack); 0 when no variant exists for these sizes.

@@ -49,11 +49,32 @@ class Staged:
                                token_pos=i32(w.prefill_pos[a:a + chunk]))
         self.k_new = bf16_tensor(w.k_new)
         self.v_new = bf16_tensor(w.v_new)
+        if w.q_len > 1:
+            self.q_multi = bf16_tensor(w.q_multi)
+            self.k_step = bf16_tensor(w.k[w.step_rows])
+            self.v_step = bf16_tensor(w.v[w.step_rows])
+            self.step_seq = i32(w.step_seq)
+            self.step_pos = i32(w.step_pos)
         if step_append:
             self.append_step()
 
     def append_step(self, stream=None):
-        kp.paged_kv_append(self.pool, self.k_new, self.v_new, self.tables, self.ctx, stream=stream)
+        if self.w.q_len > 1:
+            kp.paged_kv_append(self.pool, self.k_step, self.v_step, self.tables, self.ctx,
+                               token_seq=self.step_seq, token_pos=self.step_pos, stream=stream)
+        else:
+            kp.paged_kv_append(self.pool, self.k_new, self.v_new, self.tables, self.ctx,
+                               stream=stream)
+
+    def multi(self, split_tokens=None, lse=True, stream=None):
+        s = self.w.spec
+        split = s.split_tokens if split_tokens is None else split_tokens
+        out = torch.empty_like(self.q_multi)
+        l = (torch.empty(self.q_multi.shape[:3], dtype=torch.float32, device="cuda")
+             if lse else None)
+        kp.paged_attention_multi_query(self.pool, self.q_multi, self.tables, self.ctx, self.w.scale,
+                                       kv_split_tokens=split, out=out, lse=l, stream=stream)
+        return out, l
 
     def decode(self, split_tokens=None, lse=True, stream=None):
         s = self.w.spec

@@ -48,6 +48,7 @@ class Spec:
     prefix_tokens: int = 0          # tokens of the shared prefix
     pool_blocks: int = 0            # fixed pool size; 0 -> ceil(1.1 * blocks in use)
     split_tokens: int = 0           # split-KV chunk (0 = library's automatic choice)
+    q_len: int = 1                  # new tokens per sequence in the step (1: decode)
     note: str = ""
 
 
@@ -67,6 +68,11 @@ CONFIGS = {
                           block_size=16, seed=1004, ctx_lognormal=(1024, 0.8, 16, 8192),
                           prefix_group=8, prefix_tokens=512,
                           note="ragged lognormal batch, groups of 8 share a 512-token prefix"),
+    "llama3_8b_verify4": Spec("llama3_8b_verify4", batch=64, q_heads=32, kv_heads=8,
+                              head_dim=128, block_size=16, seed=1012, ctx_uniform=(512, 4096),
+                              q_len=4,
+                              note="speculative verify pass: 4 new tokens per sequence on the "
+                                   "Llama-3-8B-shaped layer"),
     "mha_fp8": Spec("mha_fp8", batch=128, q_heads=32, kv_heads=32, head_dim=128,
                     block_size=32, cache_dtype="fp8_e4m3", seed=1005, ctx_fixed=(2048,) * 128,
                     note="MHA 7B-shaped decode with an fp8 e4m3 cache"),
@@ -75,14 +81,14 @@ CONFIGS = {
 
 def custom(name="custom", *, batch, q_heads, kv_heads, head_dim, block_size,
            cache_dtype="bf16", seed=7, ctx=None, ctx_uniform=(), prefix_group=0,
-           prefix_tokens=0, pool_blocks=0, split_tokens=0) -> Spec:
+           prefix_tokens=0, pool_blocks=0, split_tokens=0, q_len=1) -> Spec:
     """A small workload for tests: explicit lengths or a uniform range."""
     return Spec(name, batch=batch, q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
                 block_size=block_size, cache_dtype=cache_dtype, seed=seed,
                 ctx_fixed=tuple(int(c) for c in ctx) if ctx is not None else (),
                 ctx_uniform=tuple(ctx_uniform), prefix_group=prefix_group,
                 prefix_tokens=prefix_tokens, pool_blocks=pool_blocks,
-                split_tokens=split_tokens)
+                split_tokens=split_tokens, q_len=q_len)
 
 
 def _rng(*key) -> np.random.Generator:
@@ -138,6 +144,26 @@ class Workload:
     prefill_seq: np.ndarray = field(default=None)   # int32 [N]: tokens written before the step
     prefill_pos: np.ndarray = field(default=None)   # int32 [N]
     prefill_row: np.ndarray = field(default=None)   # int64 [N]: row in k / v
+    q_multi: np.ndarray | None = None               # uint16 bf16 [B, Hq, q_len, d] when q_len > 1
+
+    @property
+    def q_len(self) -> int:
+        return self.spec.q_len
+
+    @property
+    def step_seq(self) -> np.ndarray:
+        """Sequence of each token appended in the step (q_len per sequence)."""
+        return np.repeat(np.arange(self.batch, dtype=np.int32), self.q_len)
+
+    @property
+    def step_pos(self) -> np.ndarray:
+        ctx = self.context_lens.astype(np.int32)
+        t = self.q_len
+        return (np.repeat(ctx - t, t) + np.tile(np.arange(t, dtype=np.int32), self.batch)).astype(np.int32)
+
+    @property
+    def step_rows(self) -> np.ndarray:
+        return np.repeat(self.seq_start, self.q_len) + self.step_pos.astype(np.int64)
 
     @property
     def batch(self):
@@ -203,7 +229,8 @@ def _assign_blocks(spec: Spec, ctx: np.ndarray):
         row = []
         for j in range(int(nb[b])):
             is_shared = False
-            if spec.prefix_group and j < spec.prefix_tokens // bs and j < (int(ctx[b]) - 1) // bs:
+            if (spec.prefix_group and j < spec.prefix_tokens // bs
+                    and j < (int(ctx[b]) - spec.q_len) // bs):
                 is_shared = True
             if is_shared:
                 key = (b // spec.prefix_group, j)
@@ -232,8 +259,8 @@ def _assign_blocks(spec: Spec, ctx: np.ndarray):
 def make(spec: Spec, threads: int | None = None) -> Workload:
     """Draw the whole workload (all K/V values, tables, queries)."""
     ctx = context_lengths(spec)
-    if (ctx < 1).any():
-        raise ValueError("every context must hold at least the appended token")
+    if (ctx < spec.q_len).any():
+        raise ValueError("every context must hold at least the tokens appended in the step")
     tables, shared, num_blocks = _assign_blocks(spec, ctx)
     B, Hq, Hkv, d = spec.batch, spec.q_heads, spec.kv_heads, spec.head_dim
     seq_start = np.zeros(B, dtype=np.int64)
@@ -263,6 +290,7 @@ def make(spec: Spec, threads: int | None = None) -> Workload:
         list(ex.map(fill, [(b, which) for b in range(B) for which in (0, 1)]))
 
     q = _normal_bf16((B, Hq, d), spec.seed, 4)
+    q_multi = _normal_bf16((B, Hq, spec.q_len, d), spec.seed, 5) if spec.q_len > 1 else None
 
     k_scale = v_scale = None
     if spec.cache_dtype == "fp8_e4m3":
@@ -274,12 +302,12 @@ def make(spec: Spec, threads: int | None = None) -> Workload:
     elif spec.cache_dtype != "bf16":
         raise ValueError(f"unknown cache dtype {spec.cache_dtype}")
 
-    # tokens written before this step: positions 0 .. ctx-2; a shared block is written once
+    # tokens written before this step: positions 0 .. ctx-q_len-1; a shared block is written once
     seqs, poss, rows = [], [], []
     written = set()
     bs = spec.block_size
     for b in range(B):
-        n = int(ctx[b]) - 1
+        n = int(ctx[b]) - spec.q_len
         if n <= 0:
             continue
         p = np.arange(n, dtype=np.int64)
@@ -300,4 +328,4 @@ def make(spec: Spec, threads: int | None = None) -> Workload:
                     q=q, k=k, v=v, seq_start=seq_start, shared_block=shared,
                     k_scale=k_scale, v_scale=v_scale,
                     prefill_seq=cat(seqs, np.int32), prefill_pos=cat(poss, np.int32),
-                    prefill_row=cat(rows, np.int64))
+                    prefill_row=cat(rows, np.int64), q_multi=q_multi)

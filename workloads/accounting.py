@@ -44,12 +44,16 @@ def decode_bytes(w, split_tokens: int) -> dict:
     row = 2 * s.kv_heads * s.head_dim * e                      # K and V of one token
     kv_logical = int(ctx.sum()) * row
     kv_unique = unique_kv_tokens(w) * row
-    qo = 2 * w.batch * s.q_heads * s.head_dim * 2               # q read + out written (bf16)
-    meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * w.batch * s.q_heads   # tables, ctx, lse
+    rows = s.q_heads * s.q_len                                  # query rows per sequence
+    tiles = -(-(s.q_heads // s.kv_heads * s.q_len) // 16) if s.q_heads // s.kv_heads * s.q_len > 8 else 1
+    kv_logical *= tiles                                         # each row tile reads the K/V once
+    kv_unique *= tiles
+    qo = 2 * w.batch * rows * s.head_dim * 2                    # q read + out written (bf16)
+    meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * w.batch * rows  # tables, ctx, lse
     sb = max(1, split_tokens // s.block_size)
     nsplit = np.maximum(1, (nb + sb - 1) // sb)
     multi = nsplit > 1
-    partial = int((nsplit[multi] * s.q_heads).sum()) * (s.head_dim + 2) * 4 * 2
+    partial = int((nsplit[multi] * rows).sum()) * (s.head_dim + 2) * 4 * 2
     scales = 2 * 4 * s.kv_heads if s.cache_dtype == "fp8_e4m3" else 0
     other = qo + meta + partial + scales
     return {"kv_logical": kv_logical, "kv_unique": kv_unique, "other": other,
@@ -60,10 +64,10 @@ def decode_bytes(w, split_tokens: int) -> dict:
 def append_bytes(w) -> int:
     """Algorithmic bytes of one paged_kv_append of the step's new tokens."""
     s = w.spec
-    n = w.batch * s.kv_heads * s.head_dim
-    return 2 * n * 2 + 2 * n * w.elem_bytes + 8 * w.batch
+    n = w.batch * s.q_len * s.kv_heads * s.head_dim
+    return 2 * n * 2 + 2 * n * w.elem_bytes + 8 * w.batch * s.q_len
 
 
 def decode_flops(w) -> int:
     s = w.spec
-    return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads)
+    return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads * s.q_len)
