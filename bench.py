@@ -66,8 +66,12 @@ def parse_args():
 
 # --------------------------------------------------------------------------- helpers
 def kernel_source_sha() -> str:
+    """Hash of the sources the decode launch is built from (kernel, shared device
+    code, launch parameters and the host entry that plans the grid)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_19_gb300", "csrc", "*")))
+    csrc = os.path.join(ROOT, "paged_kv_cache_19_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "decode*")) +
+                   [os.path.join(csrc, f) for f in ("device_common.cuh", "kernels.h", "api.cu")])
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode() + fh.read())

@@ -1,6 +1,7 @@
 """Paged KV cache for the decode step on GB300: Python binding of libkvpaged.so.
 
-The functions mirror the C ABI in include/kv_paged.h one to one and only
+The functions mirror the C ABI in include/kv_paged.h and
+include/kv_block_manager.h one to one and only
 marshal arguments (torch tensors -> device pointers, the current stream).
 Every step of the computation runs in the library's CUDA kernels; there is no
 CPU path, and importing a function without the built library raises.
@@ -17,7 +18,8 @@ import torch
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_attention_multi_query",
-    "paged_multi_query_workspace_size", "library_path", "load_library",
+    "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
+    "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING",
     "DEVERR_BLOCK_ID", "DEVERR_CONTEXT", "DEVERR_SEQ", "DEVERR_POSITION", "DEVERR_TIMEOUT",
 ]
 
@@ -37,9 +39,16 @@ DEVERR_SEQ = 0x4
 DEVERR_POSITION = 0x8
 DEVERR_TIMEOUT = 0x10
 _DTYPES = {"bf16": 0, "fp8_e4m3": 1}
+BM_FIFO = 0x0
+BM_LIFO = 0x1
+BM_PREFIX_CACHING = 0x2
 
 _lock = threading.Lock()
 _lib = None
+
+
+class _BlockCopy(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_int32), ("dst", ctypes.c_int32)]
 
 
 class KVError(RuntimeError):
@@ -63,7 +72,7 @@ def load_library():
             raise RuntimeError(
                 f"{_LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
         lib = ctypes.CDLL(_LIB_PATH)
-        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        P, I, S, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int64
         sig = {
             "kv_abi_version": ([], I),
             "kv_status_string": ([I], ctypes.c_char_p),
@@ -81,6 +90,18 @@ def load_library():
             "paged_attention_multi_query": ([P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
                                              P], I),
             "paged_multi_query_workspace_size": ([P, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "kv_bm_create": ([I, I, I, ctypes.POINTER(P)], I),
+            "kv_bm_destroy": ([P], I),
+            "kv_bm_add_sequence": ([P, L, ctypes.c_uint64], I),
+            "kv_bm_fork": ([P, L, L], I),
+            "kv_bm_append_slots": ([P, L, I, P, ctypes.POINTER(_BlockCopy), ctypes.POINTER(I)], I),
+            "kv_bm_match_prefix": ([P, L, P, I, ctypes.POINTER(I)], I),
+            "kv_bm_free_sequence": ([P, L], I),
+            "kv_bm_num_free_blocks": ([P, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "kv_bm_sequence_info": ([P, L, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "kv_bm_block_refcount": ([P, ctypes.c_int32, ctypes.POINTER(I)], I),
+            "kv_bm_build_tables": ([P, P, I, I, P, P], I),
+            "kv_copy_blocks": ([P, P, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -311,3 +332,113 @@ def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale
                                            _stream(stream)),
            "paged_attention_multi_query")
     return out
+
+
+def kv_copy_blocks(pool: Pool, copies, stream=None):
+    """Copy whole pool blocks (K and V) on the device: copies is an int32 CUDA tensor [n, 2]
+    of (src, dst) pairs, as BlockManager.append_slots reports them for copy-on-write."""
+    lib = load_library()
+    _need(copies, torch.int32, "copies")
+    if copies.dim() != 2 or copies.shape[1] != 2:
+        raise ValueError("copies must have shape [n, 2]")
+    _check(lib.kv_copy_blocks(pool.handle, _ptr(copies), int(copies.shape[0]), _stream(stream)),
+           "kv_copy_blocks")
+
+
+class BlockManager:
+    """Host allocator of a pool's blocks (free list, copy-on-write, prefix caching).
+
+    A thin wrapper of the kv_bm_* calls; all bookkeeping runs in the library."""
+
+    def __init__(self, num_blocks: int, block_size: int, lifo: bool = False,
+                 prefix_caching: bool = False):
+        self._lib = load_library()
+        flags = (BM_LIFO if lifo else BM_FIFO) | (BM_PREFIX_CACHING if prefix_caching else 0)
+        h = ctypes.c_void_p()
+        _check(self._lib.kv_bm_create(int(num_blocks), int(block_size), flags, ctypes.byref(h)),
+               "kv_bm_create")
+        self._h = h.value
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    @staticmethod
+    def _ids(token_ids):
+        if token_ids is None:
+            return None, None
+        arr = (ctypes.c_int32 * len(token_ids))(*[int(t) for t in token_ids])
+        return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+    def add_sequence(self, seq: int, salt: int = 0):
+        _check(self._lib.kv_bm_add_sequence(self._h, int(seq), int(salt) & (2**64 - 1)),
+               "kv_bm_add_sequence")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.kv_bm_fork(self._h, int(parent), int(child)), "kv_bm_fork")
+
+    def append_slots(self, seq: int, n_tokens: int, token_ids=None):
+        """Returns the copy-on-write copy to make first, as (src, dst), or None."""
+        if token_ids is not None and len(token_ids) != n_tokens:
+            raise ValueError("token_ids must hold n_tokens ids")
+        keep, ids = self._ids(token_ids)
+        cp, n = _BlockCopy(), ctypes.c_int()
+        _check(self._lib.kv_bm_append_slots(self._h, int(seq), int(n_tokens), ids,
+                                            ctypes.byref(cp), ctypes.byref(n)),
+               "kv_bm_append_slots")
+        return (cp.src, cp.dst) if n.value else None
+
+    def match_prefix(self, seq: int, token_ids) -> int:
+        keep, ids = self._ids(token_ids)
+        c = ctypes.c_int()
+        _check(self._lib.kv_bm_match_prefix(self._h, int(seq), ids, len(token_ids),
+                                            ctypes.byref(c)), "kv_bm_match_prefix")
+        return c.value
+
+    def free_sequence(self, seq: int):
+        _check(self._lib.kv_bm_free_sequence(self._h, int(seq)), "kv_bm_free_sequence")
+
+    def num_free_blocks(self):
+        """(free, cached-and-evictable)."""
+        a, b = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.kv_bm_num_free_blocks(self._h, ctypes.byref(a), ctypes.byref(b)),
+               "kv_bm_num_free_blocks")
+        return a.value, b.value
+
+    def sequence_info(self, seq: int):
+        """(tokens, blocks) of a sequence."""
+        a, b = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.kv_bm_sequence_info(self._h, int(seq), ctypes.byref(a), ctypes.byref(b)),
+               "kv_bm_sequence_info")
+        return a.value, b.value
+
+    def refcount(self, block: int) -> int:
+        r = ctypes.c_int()
+        _check(self._lib.kv_bm_block_refcount(self._h, int(block), ctypes.byref(r)),
+               "kv_bm_block_refcount")
+        return r.value
+
+    def build_tables(self, seqs, max_blocks: int):
+        """Host int32 tensors (block_tables [batch, max_blocks], context_lens [batch])."""
+        batch = len(seqs)
+        ids = (ctypes.c_int64 * max(batch, 1))(*[int(s) for s in seqs])
+        tables = torch.empty(batch, int(max_blocks), dtype=torch.int32)
+        lens = torch.empty(batch, dtype=torch.int32)
+        _check(self._lib.kv_bm_build_tables(self._h, ctypes.cast(ids, ctypes.c_void_p), batch,
+                                            int(max_blocks), tables.data_ptr(), lens.data_ptr()),
+               "kv_bm_build_tables")
+        return tables, lens
+
+    def block_table(self, seq: int):
+        """The sequence's block ids, in order."""
+        n = self.sequence_info(seq)[1]
+        return self.build_tables([seq], max(n, 1))[0][0, :n].tolist()
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.kv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

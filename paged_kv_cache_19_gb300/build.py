@@ -33,7 +33,7 @@ def _nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> list[str]:
@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]

@@ -12,6 +12,7 @@
 #include <new>
 
 #include "kernels.h"
+#include "kv_block_manager.h"
 #include "kv_paged.h"
 
 struct kv_pool {
@@ -389,6 +390,22 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
     p.fp8 = pool->dtype == KV_DTYPE_FP8_E4M3;
     return kvp::launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
                                                                                    : KV_ERR_CUDA;
+}
+
+kv_status kv_copy_blocks(kv_pool* pool, const kv_block_copy* copies, int n, void* stream)
+{
+    if (pool == nullptr || n < 0) return KV_ERR_INVALID_ARG;
+    if (n == 0) return KV_OK;
+    if (copies == nullptr || !aligned(copies, 4)) return KV_ERR_INVALID_ARG;
+    if (n > (1 << 30)) return KV_ERR_UNSUPPORTED;
+    kv_status st = check_device(pool);
+    if (st != KV_OK) return st;
+    const size_t block_bytes = static_cast<size_t>(pool->block_size) * pool->kv_heads *
+                               pool->head_dim * pool->elem;
+    return kvp::launch_copy_blocks(copies, n, pool->k, pool->v, block_bytes, pool->num_blocks,
+                                   pool->err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KV_OK
+               : KV_ERR_CUDA;
 }
 
 kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,

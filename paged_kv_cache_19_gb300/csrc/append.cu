@@ -1,6 +1,7 @@
 // append.cu -- the paged KV append.
 #include "device_common.cuh"
 #include "kernels.h"
+#include "kv_block_manager.h"
 
 namespace kvp {
 
@@ -79,6 +80,39 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s)
 {
     return launch_dependent(paged_kv_append_kernel, dim3(static_cast<unsigned>(p.num_tokens)),
                             dim3(128), 0, s, p);
+}
+
+// ---------------------------------------------------------------------------
+// Whole-block copies for copy-on-write: block src -> dst of the K and the V
+// pool, 16 bytes per thread.  One CTA per (copy, pool half) slice.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_copy_blocks_kernel(const kv_block_copy* copies, int n,
+                                                             uint8_t* k_pool, uint8_t* v_pool,
+                                                             size_t block_bytes, int num_blocks,
+                                                             uint32_t* err)
+{
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int i = blockIdx.x >> 1;
+    if (i >= n) return;
+    uint8_t* pool = (blockIdx.x & 1) ? v_pool : k_pool;
+    const int src = copies[i].src;
+    const int dst = copies[i].dst;
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && (blockIdx.x & 1) == 0) atomicOr(err, KV_DEVERR_BLOCK_ID);
+        return;
+    }
+    const uint4* from = reinterpret_cast<const uint4*>(pool + static_cast<size_t>(src) * block_bytes);
+    uint4* to = reinterpret_cast<uint4*>(pool + static_cast<size_t>(dst) * block_bytes);
+    const size_t nvec = block_bytes / 16;
+    for (size_t v = threadIdx.x; v < nvec; v += blockDim.x) to[v] = from[v];
+}
+
+cudaError_t launch_copy_blocks(const kv_block_copy* copies, int n, uint8_t* k_pool, uint8_t* v_pool,
+                               size_t block_bytes, int num_blocks, uint32_t* err, cudaStream_t s)
+{
+    return launch_dependent(kv_copy_blocks_kernel, dim3(static_cast<unsigned>(2 * n)), dim3(256), 0,
+                            s, copies, n, k_pool, v_pool, block_bytes, num_blocks, err);
 }
 
 }  // namespace kvp

@@ -8,6 +8,8 @@
 
 #include <utility>
 
+struct kv_block_copy;
+
 namespace kvp {
 
 // One CTA of the main decode kernel covers (sequence, kv head, head group,
@@ -95,5 +97,8 @@ cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
+                               uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
+                               cudaStream_t s);
 
 }  // namespace kvp

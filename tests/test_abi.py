@@ -1,6 +1,7 @@
 """CPU checks of the C ABI: the library loads without a GPU, exports every
-function include/kv_paged.h declares, and rejects bad arguments on the host."""
+function the headers under include/ declare, and rejects bad arguments on the host."""
 import ctypes
+import glob
 import os
 import re
 
@@ -18,17 +19,24 @@ def lib():
     return kp.load_library()
 
 
-def declared_functions():
-    text = open(os.path.join(ROOT, "include", "kv_paged.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+def declared_functions(header=None):
+    paths = ([os.path.join(ROOT, "include", header)] if header
+             else sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
+    names = set()
+    for path in paths:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_expected_calls():
-    names = declared_functions()
+    names = declared_functions("kv_paged.h")
     for must in ("kv_pool_create", "paged_kv_append", "paged_decode_attention"):
         assert must in names
     assert len(names) >= 12
+    bm = declared_functions("kv_block_manager.h")
+    for must in ("kv_bm_create", "kv_bm_append_slots", "kv_bm_match_prefix", "kv_copy_blocks"):
+        assert must in bm
 
 
 def test_every_declared_symbol_is_exported(lib):
