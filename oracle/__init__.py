@@ -68,6 +68,10 @@ def _load():
             lib.kvo_decode_multi.argtypes = [P, I, I, I, I, I, P, P, P, P, I, P, P, ctypes.c_double,
                                              P, I, P, P]
             lib.kvo_decode_multi.restype = I
+            lib.kvo_mla_attend.argtypes = [P, I, I, I, P, I, ctypes.c_double, P, P]
+            lib.kvo_mla_attend.restype = None
+            lib.kvo_mla_decode.argtypes = [P, I, I, I, I, P, P, P, ctypes.c_double, P, I, P, P]
+            lib.kvo_mla_decode.restype = I
             _lib = lib
     return _lib
 
@@ -281,3 +285,41 @@ def decode_multi_workload(w, q_multi, q_len: int, seqs=None, cache_dtype: str | 
                         q_len=q_len, kv_heads=s.kv_heads, head_dim=s.head_dim, scale=w.scale,
                         cache_dtype=cache_dtype or s.cache_dtype, k_scale=w.k_scale,
                         v_scale=w.v_scale, seqs=seqs)
+
+
+def mla_attend(q, cache, latent_dim: int, scale: float):
+    """Absorbed multi-head latent attention for one sequence, float64.
+
+    q [Hq, dl + dr] (queries already folded through W_UK, rotary part last), cache
+    [ctx, dl + dr] (latent then rotary key).  Returns (out [Hq, dl], lse [Hq])."""
+    lib = _load()
+    q = _c(q, np.float64)
+    cache = _c(cache, np.float64)
+    hq, dk = q.shape
+    ctx = cache.shape[0]
+    assert cache.shape[1] == dk and 0 < latent_dim <= dk
+    out = np.zeros((hq, latent_dim), dtype=np.float64)
+    lse = np.zeros(hq, dtype=np.float64)
+    lib.kvo_mla_attend(_ptr(q), hq, latent_dim, dk - latent_dim, _ptr(cache), ctx, float(scale),
+                       _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def mla_decode(q, cache, seq_start, context_lens, *, latent_dim: int, scale: float, seqs=None):
+    """Absorbed MLA decode of a batch: q uint16 bf16 [B, Hq, dl + dr], cache uint16 bf16
+    [T_total, dl + dr] contiguous per sequence.  Returns (out [n, Hq, dl], lse [n, Hq])."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    cache = _c(cache, np.uint16)
+    ss = _c(seq_start, np.int64)
+    cl = _c(context_lens, np.int32)
+    batch, hq, dk = q.shape
+    sl = None if seqs is None else _c(seqs, np.int32)
+    n = batch if sl is None else sl.shape[0]
+    out = np.zeros((n, hq, latent_dim), dtype=np.float64)
+    lse = np.zeros((n, hq), dtype=np.float64)
+    rc = lib.kvo_mla_decode(_ptr(q), batch, hq, latent_dim, dk - latent_dim, _ptr(cache), _ptr(ss),
+                            _ptr(cl), float(scale), _ptr(sl), n, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("bad MLA arguments")
+    return out, lse

@@ -24,6 +24,9 @@
  *       r sits at position start + r and sees keys 0 .. start + r.
  *  [P5] kongchang.com "Core Mechanics of LLM Inference Serving" -- GQA: 32 query
  *       heads in 8 groups of 4 sharing one KV head.
+ *  [P1] again, "MLA: how does decode get full-size keys and values back?" -- the
+ *       absorbed form of multi-head latent attention: every head scores one shared
+ *       cached vector (latent + rotary key) and averages its latent part.
  *
  * Readings where the pages are silent (each is listed with its reason in the
  * design notes): query head h uses KV head h / g (contiguous groups); the
@@ -470,5 +473,78 @@ int kvo_decode_multi(const uint16_t* q, int batch, int q_heads, int q_len, int k
         free(kd); free(vd);
     }
     free(qi); free(oi); free(li);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Multi-head latent attention, absorbed form ([P1] "MLA: how does decode get */
+/* full-size keys and values back?"; [P3] section "Smaller caches").  Each    */
+/* token caches one vector c_t of dl latent numbers followed by dr numbers of */
+/* the rotary key, shared by all heads.  With W_UK folded into the query and  */
+/* W_UV applied after the attention, head h scores every cached vector with   */
+/* its whole query and averages only the latent part:                        */
+/*   s_t = scale * sum_{c < dl + dr} q[h,c] c_t[c]                            */
+/*   out[h, :] = sum_t exp(s_t - m) c_t[0 .. dl-1] / sum_t exp(s_t - m)        */
+/*   lse[h] = m + log sum_t exp(s_t - m),  m = max_t s_t                      */
+/* ------------------------------------------------------------------------- */
+void kvo_mla_attend(const double* q, int q_heads, int dl, int dr, const double* cache, int ctx,
+                    double scale, double* out, double* lse)
+{
+    int dk = dl + dr;
+    double* s = (double*)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+    for (int h = 0; h < q_heads; ++h) {
+        const double* qh = q + (size_t)h * dk;
+        double* oh = out + (size_t)h * dl;
+        for (int c = 0; c < dl; ++c) oh[c] = 0.0;
+        if (ctx <= 0) { if (lse) lse[h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int t = 0; t < ctx; ++t) {
+            const double* ct = cache + (size_t)t * dk;
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c) dot += qh[c] * ct[c];
+            s[t] = scale * dot;
+            if (s[t] > m) m = s[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < ctx; ++t) {
+            double w = exp(s[t] - m);
+            const double* ct = cache + (size_t)t * dk;
+            for (int c = 0; c < dl; ++c) oh[c] += w * ct[c];
+            l += w;
+        }
+        for (int c = 0; c < dl; ++c) oh[c] /= l;
+        if (lse) lse[h] = m + log(l);
+    }
+    free(s);
+}
+
+/*
+ * Batch of MLA decodes: q bf16 [batch, q_heads, dl + dr] (the absorbed queries),
+ * cache bf16 [total_tokens, dl + dr] with sequence b's tokens at rows
+ * seq_start[b] .. seq_start[b] + ctx[b] - 1.  Results for the listed sequences
+ * (all when seq_list is NULL) in list order: out [n, q_heads, dl], lse [n, q_heads].
+ */
+int kvo_mla_decode(const uint16_t* q, int batch, int q_heads, int dl, int dr,
+                   const uint16_t* cache, const int64_t* seq_start, const int32_t* context_lens,
+                   double scale, const int32_t* seq_list, int n_list, double* out, double* lse)
+{
+    if (q_heads <= 0 || dl <= 0 || dr < 0) return -1;
+    int dk = dl + dr;
+    int n = seq_list ? n_list : batch;
+    double* qd = (double*)malloc(sizeof(double) * (size_t)q_heads * dk);
+    for (int idx = 0; idx < n; ++idx) {
+        int b = seq_list ? seq_list[idx] : idx;
+        int ctx = context_lens[b];
+        size_t cnt = (size_t)(ctx > 0 ? ctx : 1) * dk;
+        double* cd = (double*)malloc(sizeof(double) * cnt);
+        for (size_t i = 0; ctx > 0 && i < (size_t)ctx * dk; ++i)
+            cd[i] = kvo_bf16_value(cache[(size_t)seq_start[b] * dk + i]);
+        for (int i = 0; i < q_heads * dk; ++i)
+            qd[i] = kvo_bf16_value(q[(size_t)b * q_heads * dk + i]);
+        kvo_mla_attend(qd, q_heads, dl, dr, cd, ctx, scale, out + (size_t)idx * q_heads * dl,
+                       lse ? lse + (size_t)idx * q_heads : NULL);
+        free(cd);
+    }
+    free(qd);
     return 0;
 }

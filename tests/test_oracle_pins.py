@@ -395,3 +395,76 @@ def test_multi_query_of_one_token_is_the_decode():
     a, la = oracle.decode_workload(w)
     b, lb = oracle.decode_multi_workload(w, w.q[:, :, None, :], 1)
     assert np.array_equal(a, b[:, :, 0]) and np.array_equal(la, lb[:, :, 0])
+
+
+# --------------------------------------------------------------------------- MLA (absorbed)
+# xuewyang.github.io/posts/kv, "MLA: how does decode get full-size keys and values back?":
+# folding W_UK into the query and W_UV into the output gives the same result as rebuilding
+# every head's keys and values from the cached latents (the page's float32 check prints a
+# difference of 4.5e-07); DeepSeek-V2 caches 512 latent + 64 rotary-key numbers per token.
+@pytest.mark.parametrize("heads,dh,dl,dr,ctx", [(4, 16, 32, 8, 23), (3, 8, 24, 0, 5),
+                                                (2, 32, 64, 16, 1)])
+def test_mla_absorbed_equals_expanded_attention(heads, dh, dl, dr, ctx):
+    r = np.random.default_rng(heads * 100 + ctx)
+    w_uk = r.standard_normal((heads, dh, dl)) / math.sqrt(dl)
+    w_uv = r.standard_normal((heads, dh, dl)) / math.sqrt(dl)
+    lat = r.standard_normal((ctx, dl))
+    rope_k = r.standard_normal((ctx, dr))
+    q_nope = r.standard_normal((heads, dh))
+    q_rope = r.standard_normal((heads, dr))
+    scale = 1.0 / math.sqrt(dh + dr)
+    # (a) expand: per head, full keys [W_UK c ; k_rope] and values W_UV c, normal attention
+    out_a, lse_a = np.zeros((heads, dh)), np.zeros(heads)
+    for h in range(heads):
+        k_h = np.concatenate([lat @ w_uk[h].T, rope_k], axis=1)[:, None, :]
+        v_h = np.concatenate([lat @ w_uv[h].T, np.zeros((ctx, dr))], axis=1)[:, None, :]
+        q_h = np.concatenate([q_nope[h], q_rope[h]])[None, :]
+        o, l = oracle.attend(q_h, k_h, v_h, scale)
+        out_a[h], lse_a[h] = o[0, :dh], l[0]
+    # (b) absorb: q into latent space, attend over the cached vectors, project up once
+    q_lat = np.concatenate([np.einsum("hkc,hk->hc", w_uk, q_nope), q_rope], axis=1)
+    o_lat, lse_b = oracle.mla_attend(q_lat, np.concatenate([lat, rope_k], axis=1), dl, scale)
+    out_b = np.einsum("hkc,hc->hk", w_uv, o_lat)
+    assert np.max(np.abs(out_a - out_b)) < 1e-12
+    assert np.max(np.abs(lse_a - lse_b)) < 1e-12
+
+
+def test_mla_matches_torch_sdpa_with_a_narrower_value():
+    r = np.random.default_rng(77)
+    heads, dl, dr, ctx = 5, 48, 16, 37
+    q = r.standard_normal((heads, dl + dr))
+    cache = r.standard_normal((ctx, dl + dr))
+    scale = 0.11
+    out, lse = oracle.mla_attend(q, cache, dl, scale)
+    qt = torch.from_numpy(q)[:, None, :]                       # [H, 1, dk]
+    kt = torch.from_numpy(cache)[None].expand(heads, ctx, dl + dr)
+    vt = torch.from_numpy(cache[:, :dl])[None].expand(heads, ctx, dl)
+    ref = F.scaled_dot_product_attention(qt, kt, vt, scale=scale)[:, 0]
+    assert np.max(np.abs(out - ref.numpy())) < 1e-12
+    s = scale * (q @ cache.T)
+    assert np.max(np.abs(lse - logsumexp(s, axis=1))) < 1e-12
+
+
+def test_mla_decode_batch_is_single_kv_head_decode_with_key_equal_value():
+    # bf16 batch form against the (pinned) GQA decode with one kv head whose key and
+    # value are both the cached vector; the MLA output is its first dl numbers
+    heads, dl, dr = 8, 64, 16
+    ctx = np.array([1, 17, 40, 0], dtype=np.int32)
+    starts = np.concatenate([[0], np.cumsum(ctx)[:-1]]).astype(np.int64)
+    cache = _bf16((int(ctx.sum()), dl + dr), 5)
+    q = _bf16((ctx.size, heads, dl + dr), 6)
+    scale = 1.0 / math.sqrt(dl + dr)
+    out, lse = oracle.mla_decode(q, cache, starts, ctx, latent_dim=dl, scale=scale)
+    ref, ref_lse = oracle.decode(q, cache[:, None, :], cache[:, None, :], starts, ctx,
+                                 q_heads=heads, kv_heads=1, head_dim=dl + dr, scale=scale)
+    assert np.array_equal(out, ref[:, :, :dl])
+    assert np.array_equal(lse, ref_lse)
+    assert np.all(out[3] == 0) and np.all(np.isneginf(lse[3]))
+
+
+def test_mla_cache_numbers_per_token():
+    # 512 + 64 = 576 numbers per token and layer against 2 x 128 heads x 128 for MHA
+    from workloads import accounting
+    assert accounting.mla_numbers_per_token(512, 64) == 576
+    assert 2 * 128 * 128 == 32768
+    assert accounting.mla_bytes_per_token(512, 64, 2) == 1152

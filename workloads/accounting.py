@@ -19,6 +19,15 @@ def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, bytes_per_valu
     return 2 * layers * kv_heads * head_dim * bytes_per_value
 
 
+def mla_numbers_per_token(latent_dim: int, rope_dim: int) -> int:
+    """Numbers an MLA cache keeps per token and layer: the latent plus the rotary key."""
+    return latent_dim + rope_dim
+
+
+def mla_bytes_per_token(latent_dim: int, rope_dim: int, bytes_per_value: int) -> int:
+    return mla_numbers_per_token(latent_dim, rope_dim) * bytes_per_value
+
+
 def _nb(w):
     bs = w.spec.block_size
     return (w.context_lens.astype(np.int64) + bs - 1) // bs
