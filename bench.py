@@ -104,6 +104,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 tensor throughput (TFLOP/s, burst) and where it comes from."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons, with host timestamps."""
 
@@ -213,9 +222,14 @@ def rank_spec(config: str, rank: int):
     return spec if rank == 0 else replace(spec, seed=spec.seed + 100_000 * rank)
 
 
+def decode_bytes(w, split_tokens):
+    return (accounting.mla_decode_bytes(w, split_tokens) if w.spec.mla
+            else accounting.decode_bytes(w, split_tokens))
+
+
 def workload_config(w, split_tokens, max_splits, world):
     s = w.spec
-    kv = accounting.decode_bytes(w, split_tokens)
+    kv = decode_bytes(w, split_tokens)
     return {
         "workload": s.name, "batch": s.batch, "q_heads": s.q_heads, "kv_heads": s.kv_heads,
         "head_dim": s.head_dim, "block_size": s.block_size, "cache_dtype": s.cache_dtype,
@@ -229,6 +243,9 @@ def workload_config(w, split_tokens, max_splits, world):
                "working set smaller than L2: numbers include L2 hits"),
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         "seed": s.seed,
+        **({"attention": "MLA absorbed (one cached vector per token: latent + rotary key)",
+            "latent_dim": s.latent_dim, "rope_dim": s.head_dim - s.latent_dim,
+            "softmax_scale": f"1/sqrt({s.qk_head_dim})"} if s.mla else {}),
     }
 
 
@@ -238,6 +255,7 @@ def oracle_step_sample(w, seqs, threads):
     import oracle
     s = w.spec
     # append: the sampled sequences' target blocks, remapped into a small pool image
+    # (a latent pool has one cached vector per token: the V image is scratch)
     pos = w.context_lens[seqs] - 1
     blocks = w.block_tables[seqs, pos // s.block_size]
     uniq, inv = np.unique(blocks, return_inverse=True)
@@ -248,11 +266,17 @@ def oracle_step_sample(w, seqs, threads):
     vp_img = np.full(shape, 0xFF, dtype=np.uint8)
     oracle.append(kp_img, vp_img, s.cache_dtype, s.block_size, w.k_new[seqs], w.v_new[seqs], table,
                   w.context_lens[seqs], k_scale=w.k_scale, v_scale=w.v_scale)
+    if s.mla:
+        return oracle.mla_decode_workload(w, seqs=seqs)
     return oracle.decode_workload(w, seqs=seqs, threads=threads)
 
 
 def sample_bytes(w, seqs):
     s = w.spec
+    if s.mla:
+        ntok = int(w.context_lens[seqs].astype(np.int64).sum())
+        qo = len(seqs) * s.q_heads * (s.head_dim + s.latent_dim) * 2
+        return ntok * s.head_dim * 2 + qo + len(seqs) * s.head_dim * 4, ntok
     row = 2 * s.kv_heads * s.head_dim * w.elem_bytes
     kv = int(w.context_lens[seqs].astype(np.int64).sum()) * row
     qo = 2 * len(seqs) * s.q_heads * s.head_dim * 2
@@ -335,6 +359,23 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def mla_roofline(w, dec_bytes, dec_ms, hbm_peak):
+    """Extra roofline figures of the MLA decode: its arithmetic is dense enough (every head
+    of a sequence scores each cached vector) that the tensor-core time is reported too."""
+    flops = accounting.mla_decode_flops(w)
+    tpeak, tkind = measured_tensor_peak()
+    t_hbm = dec_bytes["total"] / (hbm_peak * 1e9)
+    t_mma = flops / (tpeak * 1e12)
+    return {"flops_per_launch": flops,
+            "intensity_flop_per_byte": round(flops / dec_bytes["total"], 1),
+            "ridge_flop_per_byte": round(tpeak * 1e12 / (hbm_peak * 1e9), 1),
+            "tensor_achieved_tflops": round(flops / (dec_ms / 1e3) / 1e12, 1),
+            "tensor_peak_tflops": tpeak, "tensor_peak_kind": f"{tkind} cuBLAS bf16 (burst)",
+            "tensor_frac": round(flops / (dec_ms / 1e3) / 1e12 / tpeak, 4),
+            "bound_by_arithmetic": "tensor" if t_mma > t_hbm else "hbm",
+            "l2_vector_reads_per_launch": dec_bytes["l2_reads"]}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def stage(w, device):
     import torch
@@ -347,22 +388,26 @@ def stage(w, device):
     def i32(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
-    pool = kp.kv_pool_create(w.num_blocks, s.block_size, s.kv_heads, s.head_dim, s.cache_dtype,
-                             device=device.index)
-    kr, vr = pool.raw_bytes()
-    kr.fill_(workloads.POISON_BYTE)
-    vr.fill_(workloads.POISON_BYTE)
+    if s.mla:
+        pool = kp.kv_mla_pool_create(w.num_blocks, s.block_size, s.latent_dim,
+                                     s.head_dim - s.latent_dim, device=device.index)
+    else:
+        pool = kp.kv_pool_create(w.num_blocks, s.block_size, s.kv_heads, s.head_dim,
+                                 s.cache_dtype, device=device.index)
+    for t in pool.raw_bytes():
+        if t is not None:
+            t.fill_(workloads.POISON_BYTE)
     if s.cache_dtype == "fp8_e4m3":
         pool.set_scales(w.k_scale, w.v_scale)
     tables, ctx = i32(w.block_tables), i32(w.context_lens)
     chunk = 1 << 16
     for a in range(0, w.prefill_seq.size, chunk):
         rows = w.prefill_row[a:a + chunk]
-        kp.paged_kv_append(pool, bf16(w.k[rows]), bf16(w.v[rows]), tables, ctx,
+        kp.paged_kv_append(pool, bf16(w.k[rows]), None if s.mla else bf16(w.v[rows]), tables, ctx,
                            token_seq=i32(w.prefill_seq[a:a + chunk]),
                            token_pos=i32(w.prefill_pos[a:a + chunk]))
     step = {"q": bf16(w.q if w.q_len == 1 else w.q_multi), "k": bf16(w.k[w.step_rows]),
-            "v": bf16(w.v[w.step_rows]),
+            "v": None if s.mla else bf16(w.v[w.step_rows]),
             "seq": None if w.q_len == 1 else i32(w.step_seq),
             "pos": None if w.q_len == 1 else i32(w.step_pos)}
     return pool, tables, ctx, step
@@ -381,16 +426,27 @@ def run_ours(args, rank, world, local):
     split_req = s.split_tokens if args.split_tokens is None else args.split_tokens
     pool, tables, ctx, stp = stage(w, device)
     q = stp["q"]
-    split_tokens, max_splits = kp.paged_decode_plan(pool, s.batch, s.q_heads, w.max_blocks, split_req)
-    ws_bytes = kp.paged_multi_query_workspace_size(pool, s.batch, s.q_heads, s.q_len, w.max_blocks,
-                                                   split_req)
+    if s.mla:
+        split_tokens, max_splits = kp.paged_mla_decode_plan(pool, s.batch, s.q_heads, w.max_blocks,
+                                                            split_req)
+        ws_bytes = kp.paged_mla_workspace_size(pool, s.batch, s.q_heads, w.max_blocks, split_req)
+        out = torch.empty(s.batch, s.q_heads, s.latent_dim, dtype=torch.bfloat16, device=device)
+    else:
+        split_tokens, max_splits = kp.paged_decode_plan(pool, s.batch, s.q_heads, w.max_blocks,
+                                                        split_req)
+        ws_bytes = kp.paged_multi_query_workspace_size(pool, s.batch, s.q_heads, s.q_len,
+                                                       w.max_blocks, split_req)
+        out = torch.empty_like(q)
     workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    out = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
 
     def attend(qq, tt, cc):
-        if s.q_len == 1:
+        if s.mla:
+            kp.paged_mla_decode_attention(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
+                                          workspace=workspace, out=out, lse=lse, stream=stream,
+                                          latent_dim=s.latent_dim)
+        elif s.q_len == 1:
             kp.paged_decode_attention(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
                                       workspace=workspace, out=out, lse=lse, stream=stream)
         else:
@@ -404,8 +460,8 @@ def run_ours(args, rank, world, local):
         append(stp["k"], stp["v"], tables, ctx, stp["seq"], stp["pos"])
         attend(q, tables, ctx)
 
-    dec_bytes = accounting.decode_bytes(w, split_tokens)
-    app_bytes = accounting.append_bytes(w)
+    dec_bytes = decode_bytes(w, split_tokens)
+    app_bytes = accounting.mla_append_bytes(w) if s.mla else accounting.append_bytes(w)
     step_bytes = dec_bytes["total"] + app_bytes
     launches_per_step = 2                     # append + decode (the merge runs inside the decode)
     # (the decode-only roofline loop after the timed region launches K more decode kernels)
@@ -469,7 +525,9 @@ def run_ours(args, rank, world, local):
     # ---- end to end: host (pinned) inputs copied in and the output copied out every step
     e2e = None
     if not args.no_e2e:
-        inputs = [("q", q), ("k", stp["k"]), ("v", stp["v"]), ("tables", tables), ("ctx", ctx)]
+        inputs = [("q", q), ("k", stp["k"]), ("tables", tables), ("ctx", ctx)]
+        if stp["v"] is not None:
+            inputs.append(("v", stp["v"]))
         if stp["seq"] is not None:
             inputs += [("seq", stp["seq"]), ("pos", stp["pos"])]
         h = {name: t.cpu().pin_memory() for name, t in inputs}
@@ -481,7 +539,7 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for name in d:
                 d[name].copy_(h[name], non_blocking=True)
-            append(d["k"], d["v"], d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
+            append(d["k"], d.get("v"), d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
             attend(d["q"], d["tables"], d["ctx"])
             h_out.copy_(out, non_blocking=True)
 
@@ -517,7 +575,8 @@ def run_ours(args, rank, world, local):
             "pct_of_peak": round(100 * value / peak, 2),
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
-            "roofline": {"kernel": "paged_decode_main (one launch per decode call, in-kernel "
+            "roofline": {"kernel": ("paged_mla_decode_main" if s.mla else "paged_decode_main")
+                                   + " (one launch per decode call, in-kernel "
                                    "split-KV merge; K launches timed back to back after the "
                                    "timed steps)",
                          "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
@@ -525,7 +584,8 @@ def run_ours(args, rank, world, local):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "traffic_source": traffic_src,
                          "algorithmic_bytes_per_launch": dec_bytes["total"],
-                         "algorithmic_bytes_unique_per_launch": dec_bytes["total_unique"]},
+                         "algorithmic_bytes_unique_per_launch": dec_bytes["total_unique"],
+                         **(mla_roofline(w, dec_bytes, dec_avg_ms, peak) if s.mla else {})},
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,

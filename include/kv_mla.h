@@ -1,0 +1,88 @@
+/*
+ * kv_mla.h -- decode over a paged cache of multi-head latent attention (MLA).
+ *
+ * xuewyang.github.io/posts/kv, "How big is the cache?" and "MLA: how does decode
+ * get full-size keys and values back?": a model with MLA caches one small vector
+ * per token and layer instead of per-head keys and values -- 512 latent numbers
+ * c_t plus a 64-number rotary key shared by all heads (576 in all, DeepSeek-V2),
+ * against 2 x 128 heads x 128 = 32,768 for multi-head attention.  In decode the
+ * up-projections are absorbed: the query of head h is folded through W_UK,h
+ * (q_lat,h = [W_UK,h^T q_nope,h ; q_rope,h], 576 numbers), every head scores the
+ * cached vectors directly, and the attention-weighted sum of latents is
+ * projected up by W_UV,h once afterwards.  Every head thus attends over one
+ * shared key = value vector per token, multi-query attention with a wide head:
+ *   s_t = scale * q_lat,h . c_t[0 .. 575]
+ *   out_h = sum_t softmax(s)_t c_t[0 .. 511],   lse_h = log sum_t exp(s_t)
+ * learn.mohebi.ai lesson 12, "Smaller caches", gives the same 512 + 64 numbers.
+ *
+ * This header adds the latent pool and the absorbed decode over it.  The folding
+ * of W_UK into the query and of W_UV into the output are dense per-token matrix
+ * products done by the caller before and after this call.
+ *
+ * The pool is a kv_pool (include/kv_paged.h) with one cached vector per token:
+ * device memory [num_blocks, block_size, 576] bf16 (latent then rotary key), no
+ * V half (kv_pool_tensors returns v_pool = NULL).  Appends go through
+ * paged_kv_append with v_new = NULL and k_new = the new tokens' vectors
+ * [num_tokens, 576] bf16; block copies through kv_copy_blocks.  Errors are the
+ * kv_status codes and device error bits of kv_paged.h; nothing here aborts.
+ */
+#ifndef KV_MLA_H
+#define KV_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kv_paged.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * A latent pool of num_blocks blocks of block_size tokens on `device`.
+ * latent_dim must be 512 and rope_dim 64 (the kernels are laid out for them,
+ * else KV_ERR_UNSUPPORTED); block_size 16, 32 or 64.  Contents start zeroed.
+ */
+kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int rope_dim,
+                             int device, kv_pool** out);
+
+/* Split-KV plan (see paged_decode_plan): chunk size in tokens, a multiple of
+ * block_size (0 = automatic: 512 .. 2048 tokens from the batch, heads and SM
+ * count), and the most chunks a sequence can have. */
+kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                                int kv_split_tokens, int* split_tokens, int* max_splits);
+
+/* Bytes of device workspace for these sizes (fp32 partials, (max, sum) pairs,
+ * one 32-bit chunk counter per (sequence, tile of 16 heads)); 0 when every
+ * sequence fits one chunk.  The workspace must be zero-filled before its first
+ * use; every call leaves the counters at zero again. */
+kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                                   int kv_split_tokens, size_t* bytes);
+
+/*
+ * Absorbed MLA decode for every sequence of a ragged batch, reading the latent
+ * cache in place through the block tables (one query per sequence).
+ *   q: bf16 [batch, q_heads, 576] absorbed queries (latent part then rotary part).
+ *   block_tables: int32 [batch, max_blocks]; context_lens: int32 [batch]; token t
+ *     of sequence b is at block block_tables[b][t / block_size], slot
+ *     t % block_size; slots at or past context_lens[b] are never used.
+ *   scale: softmax scale (the model's, e.g. 1/sqrt(128 + 64)).
+ *   out: bf16 [batch, q_heads, 512]; lse: fp32 [batch, q_heads] natural-log
+ *     log-sum-exp of the scaled scores, or NULL.  context_lens[b] == 0 gives
+ *     out = 0 and lse = -inf.
+ *   Bad block ids are skipped and flagged (KV_DEVERR_BLOCK_ID); out-of-range
+ *   context lengths are clamped and flagged (KV_DEVERR_CONTEXT).
+ *   Asynchronous on `stream` (NULL = legacy default stream); no allocation.
+ *   KV_ERR_INVALID_ARG for a pool that is not a latent pool.
+ */
+kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                     const int32_t* block_tables, int max_blocks,
+                                     const int32_t* context_lens, int batch, float scale,
+                                     int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                     void* out, float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV_MLA_H */

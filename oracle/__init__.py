@@ -323,3 +323,10 @@ def mla_decode(q, cache, seq_start, context_lens, *, latent_dim: int, scale: flo
     if rc != 0:
         raise ValueError("bad MLA arguments")
     return out, lse
+
+
+def mla_decode_workload(w, seqs=None):
+    """Oracle absorbed-MLA decode of a workload whose cache holds one vector per token."""
+    s = w.spec
+    return mla_decode(w.q, w.k[:, 0, :], w.seq_start, w.context_lens, latent_dim=s.latent_dim,
+                      scale=w.scale, seqs=seqs)

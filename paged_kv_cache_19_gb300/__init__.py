@@ -1,6 +1,6 @@
 """Paged KV cache for the decode step on GB300: Python binding of libkvpaged.so.
 
-The functions mirror the C ABI in include/kv_paged.h and
+The functions mirror the C ABI in include/kv_paged.h, include/kv_mla.h and
 include/kv_block_manager.h one to one and only
 marshal arguments (torch tensors -> device pointers, the current stream).
 Every step of the computation runs in the library's CUDA kernels; there is no
@@ -19,7 +19,8 @@ __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_attention_multi_query",
     "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
-    "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING",
+    "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING", "kv_mla_pool_create",
+    "paged_mla_decode_plan", "paged_mla_workspace_size", "paged_mla_decode_attention",
     "DEVERR_BLOCK_ID", "DEVERR_CONTEXT", "DEVERR_SEQ", "DEVERR_POSITION", "DEVERR_TIMEOUT",
 ]
 
@@ -102,6 +103,11 @@ def load_library():
             "kv_bm_block_refcount": ([P, ctypes.c_int32, ctypes.POINTER(I)], I),
             "kv_bm_build_tables": ([P, P, I, I, P, P], I),
             "kv_copy_blocks": ([P, P, I, P], I),
+            "kv_mla_pool_create": ([I, I, I, I, I, ctypes.POINTER(P)], I),
+            "paged_mla_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "paged_mla_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
+            "paged_mla_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
+                                            P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -146,12 +152,14 @@ class _CudaBytes:
 class Pool:
     """One layer's paged K/V pool (owned by the library)."""
 
-    def __init__(self, handle: int, num_blocks, block_size, kv_heads, head_dim, dtype, device):
+    def __init__(self, handle: int, num_blocks, block_size, kv_heads, head_dim, dtype, device,
+                 latent: bool = False):
         self._h = ctypes.c_void_p(handle)
         self.num_blocks, self.block_size = num_blocks, block_size
         self.kv_heads, self.head_dim = kv_heads, head_dim
         self.dtype, self.device = dtype, device
         self.elem_bytes = 1 if dtype == "fp8_e4m3" else 2
+        self.latent = latent            # MLA latent pool: one cached vector per token, no V
 
     @property
     def handle(self):
@@ -161,7 +169,8 @@ class Pool:
 
     def tensors(self):
         """Torch views (no copy) of the pool: K, V as raw bytes [num_blocks, bs, Hkv, d*elem]
-        viewed as bf16 or float8_e4m3fn, and the float32 scales [Hkv]."""
+        viewed as bf16 or float8_e4m3fn (V is None for a latent pool), and the float32
+        scales [Hkv]."""
         lib = load_library()
         k, v, ks, vs = (ctypes.c_void_p() for _ in range(4))
         _check(lib.kv_pool_tensors(self.handle, ctypes.byref(k), ctypes.byref(v), ctypes.byref(ks),
@@ -169,16 +178,16 @@ class Pool:
         dev = torch.device("cuda", self.device)
         shape = (self.num_blocks, self.block_size, self.kv_heads, self.head_dim * self.elem_bytes)
         kt = torch.as_tensor(_CudaBytes(k.value, shape), device=dev)
-        vt = torch.as_tensor(_CudaBytes(v.value, shape), device=dev)
+        vt = torch.as_tensor(_CudaBytes(v.value, shape), device=dev) if v.value else None
         st = torch.as_tensor(_CudaBytes(ks.value, (self.kv_heads * 4,)), device=dev).view(torch.float32)
         sv = torch.as_tensor(_CudaBytes(vs.value, (self.kv_heads * 4,)), device=dev).view(torch.float32)
         cache = torch.float8_e4m3fn if self.dtype == "fp8_e4m3" else torch.bfloat16
-        return kt.view(cache), vt.view(cache), st, sv
+        return kt.view(cache), None if vt is None else vt.view(cache), st, sv
 
     def raw_bytes(self):
-        """K and V pools as uint8 views [num_blocks, bs, Hkv, d*elem]."""
+        """K and V pools as uint8 views [num_blocks, bs, Hkv, d*elem] (V None if latent)."""
         k, v, _, _ = self.tensors()
-        return k.view(torch.uint8), v.view(torch.uint8)
+        return k.view(torch.uint8), None if v is None else v.view(torch.uint8)
 
     def set_scales(self, k_scale=None, v_scale=None):
         lib = load_library()
@@ -227,7 +236,7 @@ def paged_kv_append(pool: Pool, k_new, v_new, block_tables, context_lens=None, t
     """Write the key/value rows [T, Hkv, d] (bf16) of T tokens into the pool."""
     lib = load_library()
     _need(k_new, torch.bfloat16, "k_new")
-    _need(v_new, torch.bfloat16, "v_new")
+    _need(v_new, torch.bfloat16, "v_new")          # None for a latent pool
     _need(block_tables, torch.int32, "block_tables")
     _need(context_lens, torch.int32, "context_lens")
     _need(token_seq, torch.int32, "token_seq")
@@ -442,3 +451,65 @@ class BlockManager:
             self.close()
         except Exception:
             pass
+
+
+# --------------------------------------------------------------------------- MLA
+def kv_mla_pool_create(num_blocks: int, block_size: int, latent_dim: int = 512,
+                       rope_dim: int = 64, device: int | None = None) -> Pool:
+    """Latent pool [num_blocks, block_size, latent_dim + rope_dim] bf16 (no V half)."""
+    lib = load_library()
+    if device is None:
+        device = torch.cuda.current_device()
+    h = ctypes.c_void_p()
+    _check(lib.kv_mla_pool_create(int(num_blocks), int(block_size), int(latent_dim),
+                                  int(rope_dim), int(device), ctypes.byref(h)),
+           "kv_mla_pool_create")
+    return Pool(h.value, num_blocks, block_size, 1, latent_dim + rope_dim, "bf16", device,
+                latent=True)
+
+
+def paged_mla_decode_plan(pool: Pool, batch: int, q_heads: int, max_blocks: int,
+                          kv_split_tokens: int = 0):
+    lib = load_library()
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(lib.paged_mla_decode_plan(pool.handle, int(batch), int(q_heads), int(max_blocks),
+                                     int(kv_split_tokens), ctypes.byref(a), ctypes.byref(b)),
+           "paged_mla_decode_plan")
+    return a.value, b.value
+
+
+def paged_mla_workspace_size(pool: Pool, batch: int, q_heads: int, max_blocks: int,
+                             kv_split_tokens: int = 0) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t()
+    _check(lib.paged_mla_workspace_size(pool.handle, int(batch), int(q_heads), int(max_blocks),
+                                        int(kv_split_tokens), ctypes.byref(n)),
+           "paged_mla_workspace_size")
+    return n.value
+
+
+def paged_mla_decode_attention(pool: Pool, q, block_tables, context_lens, scale: float,
+                               kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
+                               stream=None, latent_dim: int = 512):
+    """Absorbed MLA decode: q bf16 [B, Hq, latent + rope] -> out bf16 [B, Hq, latent]."""
+    lib = load_library()
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    batch, q_heads = q.shape[0], q.shape[1]
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty(batch, q_heads, latent_dim, dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if workspace is None:
+        need = paged_mla_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_mla_decode_attention(pool.handle, _ptr(q), int(q_heads), _ptr(block_tables),
+                                          int(max_blocks), _ptr(context_lens), int(batch),
+                                          float(scale), int(kv_split_tokens), _ptr(workspace),
+                                          int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
+           "paged_mla_decode_attention")
+    return out

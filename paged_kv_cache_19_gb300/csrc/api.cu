@@ -13,6 +13,7 @@
 
 #include "kernels.h"
 #include "kv_block_manager.h"
+#include "kv_mla.h"
 #include "kv_paged.h"
 
 struct kv_pool {
@@ -28,6 +29,7 @@ struct kv_pool {
     uint32_t* err;
     CUtensorMap tmk, tmv;   // 5-D tile maps of the K and V pools
     int num_sms;
+    int mla;                // 1: latent pool (one cached vector per token, no V half)
 };
 
 namespace {
@@ -83,7 +85,7 @@ bool variant_supported(kv_dtype dtype, int head_dim, int block_size)
 // Tile map of one pool half: dims (innermost first) = 128-byte row piece,
 // pieces per token row, kv head, slot, block; a box is one block of one kv
 // head, written to shared memory with the 128-byte swizzle.
-kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map)
+kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map, int slots_per_box = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return KV_ERR_CUDA;
@@ -95,7 +97,8 @@ kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map)
     const cuuint64_t strides[4] = {128, row, row * p->kv_heads, row * p->kv_heads * p->block_size};
     const cuuint32_t box[5] = {static_cast<cuuint32_t>(per_piece),
                                static_cast<cuuint32_t>(row / 128), 1,
-                               static_cast<cuuint32_t>(p->block_size), 1};
+                               static_cast<cuuint32_t>(slots_per_box > 0 ? slots_per_box
+                                                                         : p->block_size), 1};
     const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
     const CUtensorMapDataType dt = p->dtype == KV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -359,8 +362,8 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
     if (pool == nullptr || num_tokens < 0 || batch < 0 || max_blocks <= 0)
         return KV_ERR_INVALID_ARG;
     if (num_tokens == 0) return KV_OK;
-    if (k_new == nullptr || v_new == nullptr || block_tables == nullptr || batch == 0)
-        return KV_ERR_INVALID_ARG;
+    if (k_new == nullptr || block_tables == nullptr || batch == 0) return KV_ERR_INVALID_ARG;
+    if ((v_new == nullptr) != (pool->mla != 0)) return KV_ERR_INVALID_ARG;   // latent pools: no V
     if (token_pos == nullptr && context_lens == nullptr) return KV_ERR_INVALID_ARG;
     if (token_seq == nullptr && num_tokens > batch) return KV_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(block_tables, 4) ||
@@ -448,6 +451,7 @@ kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_
     Plan plan;
     kv_status st = make_plan(pool, batch, q_heads, q_len, max_blocks, kv_split_tokens, &plan);
     if (st != KV_OK) return st;
+    if (pool->mla) return KV_ERR_INVALID_ARG;        // latent pools: paged_mla_decode_attention
     if (batch == 0) return KV_OK;
     if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
         return KV_ERR_INVALID_ARG;
@@ -510,6 +514,201 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     return paged_attention_multi_query(pool, q, q_heads, 1, block_tables, max_blocks,
                                        context_lens, batch, scale, kv_split_tokens, workspace,
                                        workspace_bytes, out, lse_out, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Multi-head latent attention (absorbed form) over a latent pool.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMlaHeadTile = 16;
+
+struct MlaPlan {
+    int head_tiles, split_blocks, max_splits;
+};
+
+// Automatic chunk: about eight chunks per SM over the worst case, kept between
+// 512 and 2048 tokens (a cached token is 1152 bytes here, 2.25x a kv head's
+// K and V row at head_dim 128, so chunks are a little shorter in tokens).
+kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_blocks,
+                        int split_tokens, MlaPlan* out)
+{
+    if (pl == nullptr || !pl->mla || batch < 0 || q_heads <= 0 || max_blocks <= 0 ||
+        split_tokens < 0)
+        return KV_ERR_INVALID_ARG;
+    if (split_tokens % pl->block_size != 0) return KV_ERR_INVALID_ARG;
+    if (static_cast<long long>(max_blocks) * pl->block_size > std::numeric_limits<int>::max())
+        return KV_ERR_INVALID_ARG;
+    MlaPlan p;
+    p.head_tiles = (q_heads + kMlaHeadTile - 1) / kMlaHeadTile;
+    if (split_tokens > 0) {
+        p.split_blocks = split_tokens / pl->block_size;
+    } else {
+        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles;
+        const long long work = units * max_blocks * pl->block_size;
+        const long long target = static_cast<long long>(pl->num_sms > 0 ? pl->num_sms : 148) * 8;
+        long long tok = (work + target - 1) / target;
+        if (tok < 512) tok = 512;
+        if (tok > 2048) tok = 2048;
+        p.split_blocks = static_cast<int>((tok + pl->block_size - 1) / pl->block_size);
+    }
+    if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
+    p.max_splits = (max_blocks + p.split_blocks - 1) / p.split_blocks;
+    if (p.max_splits > 65535 || p.head_tiles > 65535 || batch > 65535) return KV_ERR_UNSUPPORTED;
+    *out = p;
+    return KV_OK;
+}
+
+// partial outputs [batch, q_heads, max_splits, 512], (max, sum) pairs, then one
+// ticket per (sequence, head tile).
+WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
+{
+    WorkspaceLayout w{0, 0, 0, 0, 0};
+    if (p.max_splits <= 1) return w;
+    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
+    w.part_ml = round_up(n * kvp::MLA_DV * sizeof(float), kAlign);
+    w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
+    w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * sizeof(int);
+    w.total = w.tickets + w.ticket_bytes;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int rope_dim,
+                             int device, kv_pool** out)
+{
+    if (out == nullptr) return KV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_blocks <= 0 || block_size <= 0 || latent_dim <= 0 || rope_dim < 0 || device < 0)
+        return KV_ERR_INVALID_ARG;
+    if (latent_dim != kvp::MLA_DV || rope_dim != kvp::MLA_DR) return KV_ERR_UNSUPPORTED;
+    if (kvp::mla_stage_tokens(block_size) == 0) return KV_ERR_UNSUPPORTED;
+    const long double bytes = static_cast<long double>(num_blocks) * block_size * kvp::MLA_DK * 2;
+    if (bytes >= static_cast<long double>(1ull << 40)) return KV_ERR_UNSUPPORTED;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) return KV_ERR_CUDA;
+    DeviceGuard guard(device);
+    if (!guard.ok) return KV_ERR_CUDA;
+
+    kv_pool* p = new (std::nothrow) kv_pool();
+    if (p == nullptr) return KV_ERR_OUT_OF_MEMORY;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->kv_heads = 1;
+    p->head_dim = kvp::MLA_DK;
+    p->device = device;
+    p->dtype = KV_DTYPE_BF16;
+    p->elem = 2;
+    p->mla = 1;
+    p->pool_bytes = static_cast<size_t>(bytes);
+    const size_t half = round_up(p->pool_bytes, kAlign);
+    const size_t scales = round_up(sizeof(float), kAlign);
+    const size_t total = half + 2 * scales + kAlign;
+    if (cudaMalloc(&p->base, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return KV_ERR_OUT_OF_MEMORY;
+    }
+    uint8_t* b = static_cast<uint8_t*>(p->base);
+    p->k = b;
+    p->v = nullptr;
+    p->k_scale = reinterpret_cast<float*>(b + half);
+    p->v_scale = reinterpret_cast<float*>(b + half + scales);
+    p->err = reinterpret_cast<uint32_t*>(b + half + 2 * scales);
+    kv_status st = KV_OK;
+    if (cudaMemset(p->base, 0, total) != cudaSuccess) st = KV_ERR_CUDA;
+    if (st == KV_OK && cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device) !=
+                           cudaSuccess)
+        st = KV_ERR_CUDA;
+    if (st == KV_OK) st = encode_pool_map(p, p->k, &p->tmk, kvp::mla_stage_tokens(block_size));
+    if (st == KV_OK && kvp::prepare_mla_decode(block_size) != cudaSuccess) st = KV_ERR_CUDA;
+    if (st == KV_OK && cudaDeviceSynchronize() != cudaSuccess) st = KV_ERR_CUDA;
+    if (st != KV_OK) {
+        cudaGetLastError();
+        cudaFree(p->base);
+        delete p;
+        return st;
+    }
+    *out = p;
+    return KV_OK;
+}
+
+kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                                int kv_split_tokens, int* split_tokens, int* max_splits)
+{
+    MlaPlan p;
+    kv_status st = make_mla_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    if (st != KV_OK) return st;
+    if (split_tokens) *split_tokens = p.split_blocks * pool->block_size;
+    if (max_splits) *max_splits = p.max_splits;
+    return KV_OK;
+}
+
+kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, int max_blocks,
+                                   int kv_split_tokens, size_t* bytes)
+{
+    if (bytes == nullptr) return KV_ERR_INVALID_ARG;
+    MlaPlan p;
+    kv_status st = make_mla_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &p);
+    if (st != KV_OK) return st;
+    *bytes = mla_workspace_layout(batch, q_heads, p).total;
+    return KV_OK;
+}
+
+kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                     const int32_t* block_tables, int max_blocks,
+                                     const int32_t* context_lens, int batch, float scale,
+                                     int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                     void* out, float* lse_out, void* stream)
+{
+    MlaPlan plan;
+    kv_status st = make_mla_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
+    if (st != KV_OK) return st;
+    if (batch == 0) return KV_OK;
+    if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
+        return KV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return KV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4) || !aligned(lse_out, 4) || !aligned(workspace, 16))
+        return KV_ERR_INVALID_ARG;
+    const WorkspaceLayout wl = mla_workspace_layout(batch, q_heads, plan);
+    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total))
+        return KV_ERR_INVALID_ARG;
+    st = check_device(pool);
+    if (st != KV_OK) return st;
+
+    kvp::MlaParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.tables = block_tables;
+    p.ctx = context_lens;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse_out;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part_o = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
+    p.part_ml = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
+    p.tickets = wl.total > 0 ? reinterpret_cast<int*>(ws + wl.tickets) : nullptr;
+    p.err = pool->err;
+    p.batch = batch;
+    p.q_heads = q_heads;
+    p.head_tiles = plan.head_tiles;
+    p.max_blocks = max_blocks;
+    p.num_blocks = pool->num_blocks;
+    p.split_blocks = plan.split_blocks;
+    p.max_splits = plan.max_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    // chunk-major grid: x = head tile, y = sequence, z = chunk
+    const dim3 grid(static_cast<unsigned>(plan.head_tiles), static_cast<unsigned>(batch),
+                    static_cast<unsigned>(plan.max_splits));
+    return kvp::launch_mla_decode(pool->block_size, grid, pool->tmk, p,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KV_OK
+               : KV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -40,6 +40,11 @@ __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams
     const uint4* ks = reinterpret_cast<const uint4*>(p.k_new + static_cast<size_t>(i) * row);
     const uint4* vs = reinterpret_cast<const uint4*>(p.v_new + static_cast<size_t>(i) * row);
     const int nvec = row / 8;
+    if (p.v_pool == nullptr) {                      // latent pool: one cached vector per token
+        uint4* kd = reinterpret_cast<uint4*>(p.k_pool + dst * 2);
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) kd[v] = __ldg(ks + v);
+        return;
+    }
     if (!p.fp8) {
         uint4* kd = reinterpret_cast<uint4*>(p.k_pool + dst * 2);
         uint4* vd = reinterpret_cast<uint4*>(p.v_pool + dst * 2);
@@ -96,6 +101,7 @@ __global__ void __launch_bounds__(256) kv_copy_blocks_kernel(const kv_block_copy
     const int i = blockIdx.x >> 1;
     if (i >= n) return;
     uint8_t* pool = (blockIdx.x & 1) ? v_pool : k_pool;
+    if (pool == nullptr) return;                    // latent pools have no V half
     const int src = copies[i].src;
     const int dst = copies[i].dst;
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {

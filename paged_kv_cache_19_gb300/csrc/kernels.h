@@ -53,6 +53,28 @@ struct AppendParams {
     int fp8;
 };
 
+// Absorbed multi-head latent attention over a latent pool [num_blocks,
+// block_size, MLA_DK] (latent numbers then the rotary key).  One CTA per
+// (sequence, tile of 16 query heads, split chunk).
+constexpr int MLA_DV = 512;                 // latent numbers: the value
+constexpr int MLA_DR = 64;                  // rotary-key numbers
+constexpr int MLA_DK = MLA_DV + MLA_DR;     // numbers a query scores against
+struct MlaParams {
+    const uint16_t* q;        // bf16 [batch, q_heads, MLA_DK] (absorbed queries)
+    const int32_t* tables;    // [batch, max_blocks]
+    const int32_t* ctx;       // [batch]
+    uint16_t* out;            // bf16 [batch, q_heads, MLA_DV]
+    float* lse;               // [batch, q_heads] or null
+    float* part_o;            // [batch, q_heads, max_splits, MLA_DV]
+    float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum), log2 units
+    uint32_t* err;
+    int* tickets;             // [batch, head_tiles]; zero between calls
+    int batch, q_heads, head_tiles;
+    int max_blocks, num_blocks;
+    int split_blocks, max_splits;
+    float scale_log2;
+};
+
 // Launch with programmatic stream serialisation: the kernel may begin launching
 // while the preceding kernel in the stream finishes (it waits for that kernel
 // with griddepcontrol.wait before touching memory).  Falls back to an ordinary
@@ -97,6 +119,11 @@ cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+// Tokens per pipeline stage of the latent decode (0: block size not supported).
+int mla_stage_tokens(int block_size);
+cudaError_t prepare_mla_decode(int block_size);
+cudaError_t launch_mla_decode(int block_size, dim3 grid, const CUtensorMap& tm, const MlaParams& p,
+                              cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
                                cudaStream_t s);

@@ -31,11 +31,15 @@ class Staged:
     def __init__(self, w: workloads.Workload, step_append: bool = True, chunk: int = 1 << 16):
         s = w.spec
         self.w = w
-        self.pool = kp.kv_pool_create(w.num_blocks, s.block_size, s.kv_heads, s.head_dim,
-                                      s.cache_dtype)
-        kr, vr = self.pool.raw_bytes()
-        kr.fill_(workloads.POISON_BYTE)
-        vr.fill_(workloads.POISON_BYTE)
+        if s.mla:
+            self.pool = kp.kv_mla_pool_create(w.num_blocks, s.block_size, s.latent_dim,
+                                              s.head_dim - s.latent_dim)
+        else:
+            self.pool = kp.kv_pool_create(w.num_blocks, s.block_size, s.kv_heads, s.head_dim,
+                                          s.cache_dtype)
+        for t in self.pool.raw_bytes():
+            if t is not None:
+                t.fill_(workloads.POISON_BYTE)
         if s.cache_dtype == "fp8_e4m3":
             self.pool.set_scales(w.k_scale, w.v_scale)
         self.tables = i32(w.block_tables)
@@ -44,11 +48,12 @@ class Staged:
         n = w.prefill_seq.size
         for a in range(0, n, chunk):
             rows = w.prefill_row[a:a + chunk]
-            kp.paged_kv_append(self.pool, bf16_tensor(w.k[rows]), bf16_tensor(w.v[rows]),
+            kp.paged_kv_append(self.pool, bf16_tensor(w.k[rows]),
+                               None if s.mla else bf16_tensor(w.v[rows]),
                                self.tables, self.ctx, token_seq=i32(w.prefill_seq[a:a + chunk]),
                                token_pos=i32(w.prefill_pos[a:a + chunk]))
         self.k_new = bf16_tensor(w.k_new)
-        self.v_new = bf16_tensor(w.v_new)
+        self.v_new = None if s.mla else bf16_tensor(w.v_new)
         if w.q_len > 1:
             self.q_multi = bf16_tensor(w.q_multi)
             self.k_step = bf16_tensor(w.k[w.step_rows])
@@ -83,6 +88,17 @@ class Staged:
         l = torch.empty(self.q.shape[:2], dtype=torch.float32, device="cuda") if lse else None
         kp.paged_decode_attention(self.pool, self.q, self.tables, self.ctx, self.w.scale,
                                   kv_split_tokens=split, out=out, lse=l, stream=stream)
+        return out, l
+
+    def mla(self, split_tokens=None, lse=True, stream=None):
+        s = self.w.spec
+        split = s.split_tokens if split_tokens is None else split_tokens
+        out = torch.empty(self.q.shape[0], self.q.shape[1], s.latent_dim, dtype=torch.bfloat16,
+                          device="cuda")
+        l = torch.empty(self.q.shape[:2], dtype=torch.float32, device="cuda") if lse else None
+        kp.paged_mla_decode_attention(self.pool, self.q, self.tables, self.ctx, self.w.scale,
+                                      kv_split_tokens=split, out=out, lse=l, stream=stream,
+                                      latent_dim=s.latent_dim)
         return out, l
 
     def destroy(self):

@@ -49,7 +49,14 @@ class Spec:
     pool_blocks: int = 0            # fixed pool size; 0 -> ceil(1.1 * blocks in use)
     split_tokens: int = 0           # split-KV chunk (0 = library's automatic choice)
     q_len: int = 1                  # new tokens per sequence in the step (1: decode)
+    latent_dim: int = 0             # MLA: one cached vector per token, its first latent_dim
+                                    # numbers are the value (kv_heads 1, head_dim = latent + rope)
+    qk_head_dim: int = 0            # softmax scale 1/sqrt(qk_head_dim) (0: head_dim)
     note: str = ""
+
+    @property
+    def mla(self) -> bool:
+        return self.latent_dim > 0
 
 
 # The five workloads.  Seeds are 1000 + index.
@@ -76,19 +83,40 @@ CONFIGS = {
     "mha_fp8": Spec("mha_fp8", batch=128, q_heads=32, kv_heads=32, head_dim=128,
                     block_size=32, cache_dtype="fp8_e4m3", seed=1005, ctx_fixed=(2048,) * 128,
                     note="MHA 7B-shaped decode with an fp8 e4m3 cache"),
+    # Multi-head latent attention, absorbed decode: 512 latent + 64 rotary-key numbers
+    # per token (DeepSeek-V2/V3), softmax scale 1/sqrt(128 + 64), blocks of 64 tokens.
+    "deepseek_mla": Spec("deepseek_mla", batch=64, q_heads=128, kv_heads=1, head_dim=576,
+                         block_size=64, seed=1013, ctx_uniform=(512, 4096), latent_dim=512,
+                         qk_head_dim=192,
+                         note="DeepSeek-V3-shaped MLA decode layer, all 128 heads on one GPU"),
+    "deepseek_mla_tp8": Spec("deepseek_mla_tp8", batch=64, q_heads=16, kv_heads=1, head_dim=576,
+                             block_size=64, seed=1014, ctx_uniform=(512, 4096), latent_dim=512,
+                             qk_head_dim=192,
+                             note="the same layer with its heads split over 8 GPUs (16 per GPU)"),
 }
 
 
 def custom(name="custom", *, batch, q_heads, kv_heads, head_dim, block_size,
            cache_dtype="bf16", seed=7, ctx=None, ctx_uniform=(), prefix_group=0,
-           prefix_tokens=0, pool_blocks=0, split_tokens=0, q_len=1) -> Spec:
+           prefix_tokens=0, pool_blocks=0, split_tokens=0, q_len=1, latent_dim=0,
+           qk_head_dim=0) -> Spec:
     """A small workload for tests: explicit lengths or a uniform range."""
     return Spec(name, batch=batch, q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim,
                 block_size=block_size, cache_dtype=cache_dtype, seed=seed,
                 ctx_fixed=tuple(int(c) for c in ctx) if ctx is not None else (),
                 ctx_uniform=tuple(ctx_uniform), prefix_group=prefix_group,
                 prefix_tokens=prefix_tokens, pool_blocks=pool_blocks,
-                split_tokens=split_tokens, q_len=q_len)
+                split_tokens=split_tokens, q_len=q_len, latent_dim=latent_dim,
+                qk_head_dim=qk_head_dim)
+
+
+def mla(name="mla", *, batch, q_heads, block_size, seed=7, ctx=None, ctx_uniform=(),
+        split_tokens=0, pool_blocks=0) -> Spec:
+    """A small MLA workload (512 latent + 64 rotary-key numbers per token)."""
+    return custom(name, batch=batch, q_heads=q_heads, kv_heads=1, head_dim=576,
+                  block_size=block_size, seed=seed, ctx=ctx, ctx_uniform=ctx_uniform,
+                  split_tokens=split_tokens, pool_blocks=pool_blocks, latent_dim=512,
+                  qk_head_dim=192)
 
 
 def _rng(*key) -> np.random.Generator:
@@ -175,7 +203,7 @@ class Workload:
 
     @property
     def scale(self) -> float:
-        return 1.0 / math.sqrt(self.spec.head_dim)
+        return 1.0 / math.sqrt(self.spec.qk_head_dim or self.spec.head_dim)
 
     @property
     def new_rows(self) -> np.ndarray:
@@ -266,8 +294,11 @@ def make(spec: Spec, threads: int | None = None) -> Workload:
     seq_start = np.zeros(B, dtype=np.int64)
     seq_start[1:] = np.cumsum(ctx.astype(np.int64))[:-1]
     total = int(ctx.astype(np.int64).sum())
+    if spec.mla and (Hkv != 1 or spec.cache_dtype != "bf16" or spec.q_len != 1
+                     or spec.prefix_group or not 0 < spec.latent_dim < d):
+        raise ValueError("an MLA workload has one bf16 cached vector per token and one query")
     k = np.empty((total, Hkv, d), dtype=np.uint16)
-    v = np.empty((total, Hkv, d), dtype=np.uint16)
+    v = k if spec.mla else np.empty((total, Hkv, d), dtype=np.uint16)   # MLA: value = the vector
 
     # per (sequence, tensor, head) largest |bf16| bit pattern, for the fp8 scales
     amax_bits = np.zeros((B, 2, Hkv), dtype=np.uint16)
@@ -287,7 +318,7 @@ def make(spec: Spec, threads: int | None = None) -> Workload:
 
     nthreads = threads or min(32, os.cpu_count() or 1)
     with ThreadPoolExecutor(nthreads) as ex:
-        list(ex.map(fill, [(b, which) for b in range(B) for which in (0, 1)]))
+        list(ex.map(fill, [(b, which) for b in range(B) for which in ((0,) if spec.mla else (0, 1))]))
 
     q = _normal_bf16((B, Hq, d), spec.seed, 4)
     q_multi = _normal_bf16((B, Hq, spec.q_len, d), spec.seed, 5) if spec.q_len > 1 else None

@@ -80,3 +80,36 @@ def append_bytes(w) -> int:
 def decode_flops(w) -> int:
     s = w.spec
     return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads * s.q_len)
+
+
+def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16) -> dict:
+    """Algorithmic bytes of one paged_mla_decode_attention call: every cached vector once
+    (kv), the absorbed queries, the latent outputs, tables, lengths, LSE and the split
+    partials.  l2_reads: vector bytes read by all head tiles (each tile of 16 heads
+    reads the sequence's vectors; the copies after the first come from L2)."""
+    s = w.spec
+    ctx = w.context_lens.astype(np.int64)
+    nb = _nb(w)
+    kv = int(ctx.sum()) * s.head_dim * 2
+    tiles = -(-s.q_heads // head_tile)
+    rows = w.batch * s.q_heads
+    qo = rows * (s.head_dim + s.latent_dim) * 2
+    meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * rows
+    sb = max(1, split_tokens // s.block_size)
+    nsplit = np.maximum(1, (nb + sb - 1) // sb)
+    multi = nsplit > 1
+    partial = int(nsplit[multi].sum()) * s.q_heads * (s.latent_dim + 2) * 4 * 2
+    other = qo + meta + partial
+    return {"kv_logical": kv, "kv_unique": kv, "other": other, "total": kv + other,
+            "total_unique": kv + other, "partials": partial, "l2_reads": kv * tiles}
+
+
+def mla_append_bytes(w) -> int:
+    n = w.batch * w.spec.head_dim
+    return 2 * n * 2 + 8 * w.batch
+
+
+def mla_decode_flops(w) -> int:
+    """2 flops per multiply-add: scores over head_dim numbers, values over latent_dim."""
+    s = w.spec
+    return int(2 * w.context_lens.astype(np.int64).sum() * (s.head_dim + s.latent_dim) * s.q_heads)
