@@ -65,16 +65,20 @@ def parse_args():
 
 
 # --------------------------------------------------------------------------- helpers
-def kernel_source_sha() -> str:
-    """Hash of the sources the decode launch is built from (kernel, shared device
-    code, launch parameters and the host entry that plans the grid)."""
+KERNEL_SOURCES = {
+    "gqa": ["decode_kernel.cuh", "decode_common.cuh", "decode_bf16.cu", "decode_fp8.cu",
+            "device_common.cuh"],
+    "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
+}
+
+
+def kernel_source_sha(kind: str = "gqa") -> str:
+    """Hash of the device sources the timed decode kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_19_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "decode*")) +
-                   [os.path.join(csrc, f) for f in ("device_common.cuh", "kernels.h", "api.cu")])
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:12]
 
 
@@ -84,7 +88,7 @@ def profiled_traffic(config: str):
     A profile summary under profiles/ states `kernel_source_sha:` and
     `dram_bytes_per_launch:` for a workload; it counts only while the sources
     are unchanged."""
-    sha = kernel_source_sha()
+    sha = kernel_source_sha("mla" if workloads.CONFIGS[config].mla else "gqa")
     for path in glob.glob(os.path.join(PROFILES, "*.md")) + glob.glob(os.path.join(PROFILES, "*.txt")):
         text = open(path).read()
         m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
@@ -300,11 +304,12 @@ def cpu_baseline(w, target_s: float, gpu_out=None):
         out, _ = oracle_step_sample(w, seqs, threads)
         dt = time.perf_counter() - t0
     nbytes, ntok = sample_bytes(w, seqs)
-    res = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+    used = 1 if w.spec.mla else threads           # the MLA oracle runs on one thread
+    res = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": used,
            "kind": "oracle",
            "sample": (f"append + decode of {len(seqs)} of {w.batch} sequences ({ntok} cached "
                       f"tokens, all {w.spec.q_heads} query heads), float64 C oracle, "
-                      f"{threads} threads, {dt:.2f} s"),
+                      f"{used} thread{'s' if used > 1 else ''}, {dt:.2f} s"),
            "kv_tokens_per_s": round(ntok / dt, 1)}
     if gpu_out is not None:
         got = gpu_out[seqs].float().cpu().double().numpy()
@@ -342,8 +347,10 @@ def run_reference(args, rank, world):
         total_tok += tok
     dt = time.perf_counter() - t0
     value = total_bytes / dt / 1e9
+    if w.spec.mla:
+        threads = 1                                # the MLA oracle runs on one thread
     sample = (f"each step: append + decode of {n} of {w.batch} sequences, float64 C oracle, "
-              f"{threads} threads")
+              f"{threads} thread{'s' if threads > 1 else ''}")
     line = {
         "impl": "reference", "metric": METRIC,
         "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,

@@ -47,7 +47,7 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
                              int device, kv_pool** out);
 
 /* Split-KV plan (see paged_decode_plan): chunk size in tokens, a multiple of
- * block_size (0 = automatic: 512 .. 2048 tokens from the batch, heads and SM
+ * block_size (0 = automatic: 768 .. 2048 tokens from the batch, heads and SM
  * count), and the most chunks a sequence can have. */
 kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                 int kv_split_tokens, int* split_tokens, int* max_splits);

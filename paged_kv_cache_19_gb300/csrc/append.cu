@@ -38,13 +38,13 @@ __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams
     const int row = p.kv_heads * p.head_dim;                 // elements per token
     const size_t dst = (static_cast<size_t>(blk) * p.block_size + slot) * row;
     const uint4* ks = reinterpret_cast<const uint4*>(p.k_new + static_cast<size_t>(i) * row);
-    const uint4* vs = reinterpret_cast<const uint4*>(p.v_new + static_cast<size_t>(i) * row);
     const int nvec = row / 8;
     if (p.v_pool == nullptr) {                      // latent pool: one cached vector per token
         uint4* kd = reinterpret_cast<uint4*>(p.k_pool + dst * 2);
         for (int v = threadIdx.x; v < nvec; v += blockDim.x) kd[v] = __ldg(ks + v);
         return;
     }
+    const uint4* vs = reinterpret_cast<const uint4*>(p.v_new + static_cast<size_t>(i) * row);
     if (!p.fp8) {
         uint4* kd = reinterpret_cast<uint4*>(p.k_pool + dst * 2);
         uint4* vd = reinterpret_cast<uint4*>(p.v_pool + dst * 2);

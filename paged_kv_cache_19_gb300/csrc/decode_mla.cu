@@ -51,6 +51,9 @@ struct MlaCfg {
     static constexpr int E = NT * DV / (NCW * 32);  // output numbers per thread: 64
     static constexpr int RING = NSTAGE * STAGE;
     static constexpr int SMEM = 1024 + RING + XBYTES + NSTAGE * (8 + 8 + 4) + 16;
+    // Two CTAs per SM with a short ring, or one CTA with a deep ring (about 180 KB
+    // of stages in flight) for grids that would leave SMs with a single CTA anyway.
+    static constexpr int MINB = RING <= 80 * 1024 ? 2 : 1;
     static_assert(BS % SUB == 0 && SUB % 16 == 0, "stages are whole 16-token slices of a block");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert((16 * DCH) % 8 == 0, "16-token slices keep the swizzle phase");
@@ -74,7 +77,7 @@ __device__ __forceinline__ uint32_t swz_off(int tok, int ch)
 }
 
 template <int BS, int SUB, int NSTAGE>
-__global__ void __launch_bounds__(MlaCfg<BS, SUB, NSTAGE>::THREADS, 2)
+__global__ void __launch_bounds__(MlaCfg<BS, SUB, NSTAGE>::THREADS, MlaCfg<BS, SUB, NSTAGE>::MINB)
 paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p)
 {
     using C = MlaCfg<BS, SUB, NSTAGE>;
@@ -308,9 +311,25 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                 }
         }
 
-        // ---- online softmax (log2 domain); tokens at or past lim are not cached
+        // ---- online softmax (log2 domain); tokens at or past lim are not cached.
+        // The max is taken on the raw scores (the scale is positive) and the scale
+        // is applied inside the exponent: p = 2^(s * sl2 - m).
         const int lim = ctx - (blk0 * BS + it * SUB);
         const int nvalid = min(SUB, lim);
+        const bool partial = nvalid < SUB;
+        if (partial) {
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi)
+                    if (mt * 16 + r + 8 * hi >= nvalid) {
+#pragma unroll
+                        for (int nt = 0; nt < C::NTT; ++nt) {
+                            sc[mt][nt][2 * hi] = -INFINITY;
+                            sc[mt][nt][2 * hi + 1] = -INFINITY;
+                        }
+                    }
+        }
         bool rescale = false;
         float alpha[C::NTT][2];
 #pragma unroll
@@ -321,16 +340,11 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
-                    for (int hi = 0; hi < 2; ++hi) {
-                        const int tok = mt * 16 + r + 8 * hi;
-                        const float x = tok < nvalid ? sc[mt][nt][2 * hi + j] * sl2 : -INFINITY;
-                        sc[mt][nt][2 * hi + j] = x;
-                        mx = fmaxf(mx, x);
-                    }
+                    for (int hi = 0; hi < 2; ++hi) mx = fmaxf(mx, sc[mt][nt][2 * hi + j]);
                 mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
-                const float m_new = fmaxf(st.m[nt][j], mx);
+                const float m_new = fmaxf(st.m[nt][j], mx * sl2);
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
                 const float a_ = fast_exp2(st.m[nt][j] - m_use);
                 st.m[nt][j] = m_new;
@@ -339,7 +353,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                 for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
                     for (int hi = 0; hi < 2; ++hi) {
-                        const float pr = fast_exp2(sc[mt][nt][2 * hi + j] - m_use);
+                        const float pr = fast_exp2(fmaf(sc[mt][nt][2 * hi + j], sl2, -m_use));
                         sc[mt][nt][2 * hi + j] = pr;
                         ls += pr;
                     }
@@ -361,7 +375,8 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         }
 
         // ---- O^T[latent slice x heads] += C^T[latent x tokens] . P^T[tokens x heads]
-        const bool partial = nvalid < SUB;
+        // (in a partial stage the values of tokens past the cache are zeroed: they
+        // may hold anything, and 0 * NaN would poison the sums)
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
             uint32_t pb[C::NTT][2];
@@ -370,23 +385,31 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                 pb[nt][0] = movmatrix_trans(pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
                 pb[nt][1] = movmatrix_trans(pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
             }
-            const int t0 = mt * 16 + 2 * c;
-            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-            if (partial) {
-                mlo = (t0 < nvalid ? 0x0000ffffu : 0u) | (t0 + 1 < nvalid ? 0xffff0000u : 0u);
-                mhi = (t0 + 8 < nvalid ? 0x0000ffffu : 0u) | (t0 + 9 < nvalid ? 0xffff0000u : 0u);
-            }
+            if (!partial) {
 #pragma unroll
-            for (int ms = 0; ms < C::MSW; ++ms) {
-                uint32_t a[4];
-                ldsm_x4_trans(tile + mt * C::MT_BYTES + off_v[ms], a);
-                a[0] &= mlo;
-                a[1] &= mlo;
-                a[2] &= mhi;
-                a[3] &= mhi;
+                for (int ms = 0; ms < C::MSW; ++ms) {
+                    uint32_t a[4];
+                    ldsm_x4_trans(tile + mt * C::MT_BYTES + off_v[ms], a);
 #pragma unroll
-                for (int nt = 0; nt < C::NTT; ++nt)
-                    mma_bf16_16816(st.o[ms][nt], a, pb[nt][0], pb[nt][1]);
+                    for (int nt = 0; nt < C::NTT; ++nt)
+                        mma_bf16_16816(st.o[ms][nt], a, pb[nt][0], pb[nt][1]);
+                }
+            } else {
+                const int t0 = mt * 16 + 2 * c;
+                const uint32_t mlo = (t0 < nvalid ? 0x0000ffffu : 0u) | (t0 + 1 < nvalid ? 0xffff0000u : 0u);
+                const uint32_t mhi = (t0 + 8 < nvalid ? 0x0000ffffu : 0u) | (t0 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int ms = 0; ms < C::MSW; ++ms) {
+                    uint32_t a[4];
+                    ldsm_x4_trans(tile + mt * C::MT_BYTES + off_v[ms], a);
+                    a[0] &= mlo;
+                    a[1] &= mlo;
+                    a[2] &= mhi;
+                    a[3] &= mhi;
+#pragma unroll
+                    for (int nt = 0; nt < C::NTT; ++nt)
+                        mma_bf16_16816(st.o[ms][nt], a, pb[nt][0], pb[nt][1]);
+                }
             }
         }
         __syncwarp();
@@ -508,10 +531,10 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 
 namespace {
 
-template <int BS>
+template <int BS, bool DEEP>
 struct MlaVariant {
     static constexpr int SUB = BS < 32 ? BS : 32;
-    static constexpr int NSTAGE = SUB == 16 ? 4 : 2;
+    static constexpr int NSTAGE = (SUB == 16 ? 4 : 2) * (DEEP ? 5 : 2) / 2;
     using C = MlaCfg<BS, SUB, NSTAGE>;
     static cudaError_t prepare()
     {
@@ -525,14 +548,21 @@ struct MlaVariant {
     }
 };
 
+template <int BS>
+cudaError_t prepare_both()
+{
+    cudaError_t e = MlaVariant<BS, false>::prepare();
+    return e != cudaSuccess ? e : MlaVariant<BS, true>::prepare();
+}
+
 }  // namespace
 
 int mla_stage_tokens(int block_size)
 {
     switch (block_size) {
-    case 16: return MlaVariant<16>::SUB;
-    case 32: return MlaVariant<32>::SUB;
-    case 64: return MlaVariant<64>::SUB;
+    case 16: return MlaVariant<16, false>::SUB;
+    case 32: return MlaVariant<32, false>::SUB;
+    case 64: return MlaVariant<64, false>::SUB;
     default: return 0;
     }
 }
@@ -540,20 +570,23 @@ int mla_stage_tokens(int block_size)
 cudaError_t prepare_mla_decode(int block_size)
 {
     switch (block_size) {
-    case 16: return MlaVariant<16>::prepare();
-    case 32: return MlaVariant<32>::prepare();
-    case 64: return MlaVariant<64>::prepare();
+    case 16: return prepare_both<16>();
+    case 32: return prepare_both<32>();
+    case 64: return prepare_both<64>();
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_mla_decode(int block_size, dim3 grid, const CUtensorMap& tm, const MlaParams& p,
-                              cudaStream_t s)
+cudaError_t launch_mla_decode(int block_size, bool deep, dim3 grid, const CUtensorMap& tm,
+                              const MlaParams& p, cudaStream_t s)
 {
     switch (block_size) {
-    case 16: return MlaVariant<16>::launch(grid, tm, p, s);
-    case 32: return MlaVariant<32>::launch(grid, tm, p, s);
-    case 64: return MlaVariant<64>::launch(grid, tm, p, s);
+    case 16: return deep ? MlaVariant<16, true>::launch(grid, tm, p, s)
+                         : MlaVariant<16, false>::launch(grid, tm, p, s);
+    case 32: return deep ? MlaVariant<32, true>::launch(grid, tm, p, s)
+                         : MlaVariant<32, false>::launch(grid, tm, p, s);
+    case 64: return deep ? MlaVariant<64, true>::launch(grid, tm, p, s)
+                         : MlaVariant<64, false>::launch(grid, tm, p, s);
     default: return cudaErrorInvalidValue;
     }
 }

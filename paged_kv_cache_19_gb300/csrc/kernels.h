@@ -122,8 +122,9 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 // Tokens per pipeline stage of the latent decode (0: block size not supported).
 int mla_stage_tokens(int block_size);
 cudaError_t prepare_mla_decode(int block_size);
-cudaError_t launch_mla_decode(int block_size, dim3 grid, const CUtensorMap& tm, const MlaParams& p,
-                              cudaStream_t s);
+// deep: the one-CTA-per-SM variant with a deep ring of stages (small grids).
+cudaError_t launch_mla_decode(int block_size, bool deep, dim3 grid, const CUtensorMap& tm,
+                              const MlaParams& p, cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
                                cudaStream_t s);

@@ -27,6 +27,11 @@ SMALL = {
     "bs64_auto_split_long": M(batch=2, q_heads=16, block_size=64, ctx=[9000, 40], seed=205),
     "bs64_split64_ragged": M(batch=5, q_heads=16, block_size=64, ctx=[1, 63, 64, 129, 1000],
                              seed=206, split_tokens=64),
+    # grids of more than two CTAs per SM run the two-CTAs-per-SM variant
+    "bs16_h128_many_ctas": M(batch=24, q_heads=128, block_size=16, ctx_uniform=(1, 300),
+                             seed=209, split_tokens=64),
+    "bs32_h64_many_ctas": M(batch=24, q_heads=64, block_size=32, ctx_uniform=(1, 400),
+                            seed=210, split_tokens=64),
 }
 
 
