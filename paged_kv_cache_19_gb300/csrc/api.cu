@@ -27,7 +27,9 @@ struct kv_pool {
     float* k_scale;
     float* v_scale;
     uint32_t* err;
-    CUtensorMap tmk, tmv;   // 5-D tile maps of the K and V pools
+    CUtensorMap tmk, tmv;   // 5-D tile maps of the K and V pools; latent pools: the map
+                            // with the stage box of the producer-warp decode (tmk) and of
+                            // the three-CTA decode (tmv)
     int num_sms;
     int mla;                // 1: latent pool (one cached vector per token, no V half)
 };
@@ -588,7 +590,7 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
     if (num_blocks <= 0 || block_size <= 0 || latent_dim <= 0 || rope_dim < 0 || device < 0)
         return KV_ERR_INVALID_ARG;
     if (latent_dim != kvp::MLA_DV || rope_dim != kvp::MLA_DR) return KV_ERR_UNSUPPORTED;
-    if (kvp::mla_stage_tokens(block_size) == 0) return KV_ERR_UNSUPPORTED;
+    if (kvp::mla_stage_tokens(block_size, true) == 0) return KV_ERR_UNSUPPORTED;
     const long double bytes = static_cast<long double>(num_blocks) * block_size * kvp::MLA_DK * 2;
     if (bytes >= static_cast<long double>(1ull << 40)) return KV_ERR_UNSUPPORTED;
 
@@ -627,7 +629,10 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
     if (st == KV_OK && cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, device) !=
                            cudaSuccess)
         st = KV_ERR_CUDA;
-    if (st == KV_OK) st = encode_pool_map(p, p->k, &p->tmk, kvp::mla_stage_tokens(block_size));
+    if (st == KV_OK)
+        st = encode_pool_map(p, p->k, &p->tmk, kvp::mla_stage_tokens(block_size, true));
+    if (st == KV_OK)
+        st = encode_pool_map(p, p->k, &p->tmv, kvp::mla_stage_tokens(block_size, false));
     if (st == KV_OK && kvp::prepare_mla_decode(block_size) != cudaSuccess) st = KV_ERR_CUDA;
     if (st == KV_OK && cudaDeviceSynchronize() != cudaSuccess) st = KV_ERR_CUDA;
     if (st != KV_OK) {
@@ -703,14 +708,14 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    // chunk-major grid: x = head tile, y = sequence, z = chunk.  A grid that fits
-    // one CTA per SM runs with a deep ring of stages (about 180 KB in flight per
-    // SM); larger grids run two CTAs per SM with short rings.
+    // chunk-major grid: x = head tile, y = sequence, z = chunk.  Grids of up to
+    // three CTAs per SM run the producer-warp variant (32-token stages, two CTAs
+    // per SM), larger ones the three-CTAs-per-SM variant (16-token stages).
     const dim3 grid(static_cast<unsigned>(plan.head_tiles), static_cast<unsigned>(batch),
                     static_cast<unsigned>(plan.max_splits));
     const long long ctas = static_cast<long long>(plan.head_tiles) * batch * plan.max_splits;
-    const bool deep = ctas <= (pool->num_sms > 0 ? pool->num_sms : 148);
-    return kvp::launch_mla_decode(pool->block_size, deep, grid, pool->tmk, p,
+    const bool prod = ctas <= 3LL * (pool->num_sms > 0 ? pool->num_sms : 148);
+    return kvp::launch_mla_decode(pool->block_size, prod, grid, prod ? pool->tmk : pool->tmv, p,
                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KV_OK
                : KV_ERR_CUDA;

@@ -6,30 +6,40 @@
 // into the query and W_UV applied after the attention, so full keys and values
 // are never built).
 //
-// One CTA per (sequence, tile of 16 query heads, split-KV chunk); 160 threads:
-//   * warp 4 streams stages of SUB tokens x 1152 bytes with 5-D TMA loads
-//     (128-byte swizzle) into a ring of NSTAGE stages guarded by mbarriers;
-//   * warps 0-3 all work on every stage.  Scores S^T[tokens x 16 heads] =
-//     C[tokens x 576] . Q^T are split over the 576 numbers (warp w sums its 144
-//     on the tensor cores, with the query fragments held in registers), the four
-//     partial sums are exchanged through shared memory and added in the same
-//     order by every warp, so all warps hold the same scores and run the same
-//     online softmax; then warp w accumulates O^T[latent 128w .. 128w+127 x 16
-//     heads] += C^T . P^T.  Splitting the 576-long sums keeps each warp's chain
-//     of dependent MMAs short (9) and its registers low (O^T is 64 of them).
+// One CTA per (sequence, tile of 16 query heads, split-KV chunk).  Four consumer
+// warps all work on every stage of SUB tokens x 1152 bytes:
+//   * scores S^T[tokens x 16 heads] = C[tokens x 576] . Q^T are split over the
+//     576 numbers (warp w sums its 144 on the tensor cores, with the query
+//     fragments held in registers); the four partial sums are exchanged through
+//     shared memory across one barrier per stage and added in the same order by
+//     every warp, so all warps hold the same scores and run the same online
+//     softmax; then warp w accumulates O^T[latent 128w .. 128w+127 x 16 heads]
+//     += C^T . P^T.  Splitting the 576-long sums keeps each warp's chain of
+//     dependent MMAs short (9) and its accumulator at 64 registers.
+//   * stages arrive by 5-D TMA loads (128-byte swizzle) into a ring guarded by
+//     "full" mbarriers, in one of two ways:
+//       PROD: a fifth warp issues the loads and waits for "empty" mbarriers that
+//         the consumers arrive on -- 32-token stages, 2 stages, 2 CTAs per SM;
+//         the load of a stage starts as soon as its slot is released.
+//       otherwise: the exchange barrier already tells that the previous stage is
+//         free, so thread 0 issues the load NSTAGE - 1 stages ahead right there
+//         -- no producer warp and no "empty" barriers, 16-token stages, 3
+//         stages, 3 CTAs per SM (12 consumer warps).
+//     The host takes the producer form for grids of up to three CTAs per SM and
+//     the three-CTA form beyond.
 //   * the swizzled shared-memory offsets each lane reads are fixed per warp and
 //     computed once, before the loop.
 //   * split chunks leave fp32 partials and the last one to finish merges them by
 //     log-sum-exp (ticket in the workspace), as in the GQA decode kernel.
-// Every wait is bounded; a late stage sets KV_DEVERR_TIMEOUT and all consumer
-// warps leave the loop together (the decision is shared across the exchange
-// barrier, so no warp is left waiting on it).
+// Every wait is bounded; a stage that does not arrive sets KV_DEVERR_TIMEOUT and
+// all consumer warps leave the loop together (the decision is shared across the
+// exchange barrier), after the loads in flight have landed (bounded waits).
 #include "decode_common.cuh"
 #include "kernels.h"
 
 namespace kvp {
 
-template <int BS, int SUB, int NSTAGE>
+template <int BS, int SUB, int NSTAGE, bool PROD>
 struct MlaCfg {
     static constexpr int DK = MLA_DK;               // numbers per cached token (key)
     static constexpr int DV = MLA_DV;               // latent numbers (value)
@@ -37,7 +47,7 @@ struct MlaCfg {
     static constexpr int STAGE = SUB * DK * 2;      // bytes of one stage
     static constexpr int SPB = BS / SUB;            // stages per block
     static constexpr int NCW = 4;
-    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int THREADS = (NCW + (PROD ? 1 : 0)) * 32;
     static constexpr int NT = 16;                   // heads per CTA
     static constexpr int NTT = NT / 8;
     static constexpr int MT = SUB / 16;             // 16-token slices per stage
@@ -51,10 +61,10 @@ struct MlaCfg {
     static constexpr int E = NT * DV / (NCW * 32);  // output numbers per thread: 64
     static constexpr int RING = NSTAGE * STAGE;
     static constexpr int SMEM = 1024 + RING + XBYTES + NSTAGE * (8 + 8 + 4) + 16;
-    // Two CTAs per SM with a short ring, or one CTA with a deep ring (about 180 KB
-    // of stages in flight) for grids that would leave SMs with a single CTA anyway.
-    static constexpr int MINB = RING <= 80 * 1024 ? 2 : 1;
+    static constexpr int MINB = PROD ? 2 : 3;      // CTAs per SM (shared memory allows it)
+    static_assert(MINB * (SMEM + 1024) <= 228 * 1024, "CTAs per SM fit the shared memory");
     static_assert(BS % SUB == 0 && SUB % 16 == 0, "stages are whole 16-token slices of a block");
+    static_assert(NSTAGE >= 2, "one stage in use, at least one loading");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert((16 * DCH) % 8 == 0, "16-token slices keep the swizzle phase");
     static_assert(RED_BYTES <= RING, "epilogue buffer reuses the stages");
@@ -76,17 +86,43 @@ __device__ __forceinline__ uint32_t swz_off(int tok, int ch)
     return static_cast<uint32_t>(row * 128 + ((((ch & 7) ^ (row & 7))) << 4));
 }
 
-template <int BS, int SUB, int NSTAGE>
-__global__ void __launch_bounds__(MlaCfg<BS, SUB, NSTAGE>::THREADS, MlaCfg<BS, SUB, NSTAGE>::MINB)
+// Thread 0: issue (or skip) the load of chunk stage `it` into ring slot it % NSTAGE.
+// Returns the block id it used (-1: bad id, flagged; the stage arrives empty).
+template <class C, int SUB, int NSTAGE>
+__device__ __forceinline__ void issue_stage(int it, const int32_t* trow, int num_blocks,
+                                            uint8_t* smem, uint64_t* full, int* stage_blk,
+                                            const CUtensorMap* tmc, uint32_t* err)
+{
+    const int j = it / C::SPB;
+    const int sub = it - j * C::SPB;
+    int blk = __ldg(trow + j);
+    if (blk < 0 || blk >= num_blocks) {
+        atomicOr(err, KV_DEVERR_BLOCK_ID);
+        blk = -1;
+    }
+    const int st = it % NSTAGE;
+    stage_blk[st] = blk;
+    const uint32_t fb = smem_u32(full + st);
+    if (blk >= 0) {
+        mbar_arrive_expect_tx(fb, C::STAGE);
+        tma_load_5d(smem_u32(smem + st * C::STAGE), tmc, 0, 0, 0, sub * SUB, blk, fb);
+    } else {
+        mbar_arrive(fb);
+    }
+}
+
+template <int BS, int SUB, int NSTAGE, bool PROD>
+__global__ void __launch_bounds__(MlaCfg<BS, SUB, NSTAGE, PROD>::THREADS,
+                                  MlaCfg<BS, SUB, NSTAGE, PROD>::MINB)
 paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p)
 {
-    using C = MlaCfg<BS, SUB, NSTAGE>;
+    using C = MlaCfg<BS, SUB, NSTAGE, PROD>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* xbuf = reinterpret_cast<float*>(smem + C::RING);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::RING + C::XBYTES);
-    uint64_t* empty = full + NSTAGE;
+    uint64_t* empty = full + NSTAGE;                // PROD only
     int* stage_blk = reinterpret_cast<int*>(empty + NSTAGE);
     int* flags = stage_blk + NSTAGE;                // [0]: abort, [1]: merge
 
@@ -104,7 +140,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
             mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(empty + i), C::NCW);
+            if (PROD) mbar_init(smem_u32(empty + i), C::NCW);
         }
         flags[0] = 0;
         fence_mbar_init();
@@ -113,22 +149,21 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 
     const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
     int id_first = -1;
-    if (warp == C::NCW && blk0 + lane < p.max_blocks) id_first = __ldg(trow + lane);
+    if (PROD && warp == C::NCW && blk0 + lane < p.max_blocks) id_first = __ldg(trow + lane);
 
     // Q^T fragments of this warp's 144 numbers: k slice kk is slice 9w + kk.
     uint32_t qf[C::KSW][C::NTT][2];
-    if (warp < C::NCW) {
 #pragma unroll
-        for (int nt = 0; nt < C::NTT; ++nt) {
-            const int hl = nt * 8 + r;
-            const bool valid = hl < nh;
-            const uint16_t* qh = p.q + (row0 + (valid ? hl : 0)) * C::DK;
+    for (int nt = 0; nt < C::NTT; ++nt) {
+        if (warp >= C::NCW) break;
+        const int hl = nt * 8 + r;
+        const bool valid = hl < nh;
+        const uint16_t* qh = p.q + (row0 + (valid ? hl : 0)) * C::DK;
 #pragma unroll
-            for (int kk = 0; kk < C::KSW; ++kk) {
-                const int k0 = (warp * C::KSW + kk) * 16;
-                qf[kk][nt][0] = valid ? *reinterpret_cast<const uint32_t*>(qh + k0 + 2 * c) : 0u;
-                qf[kk][nt][1] = valid ? *reinterpret_cast<const uint32_t*>(qh + k0 + 8 + 2 * c) : 0u;
-            }
+        for (int kk = 0; kk < C::KSW; ++kk) {
+            const int k0 = (warp * C::KSW + kk) * 16;
+            qf[kk][nt][0] = valid ? *reinterpret_cast<const uint32_t*>(qh + k0 + 2 * c) : 0u;
+            qf[kk][nt][1] = valid ? *reinterpret_cast<const uint32_t*>(qh + k0 + 8 + 2 * c) : 0u;
         }
     }
     int ctx = __ldg(p.ctx + b);
@@ -141,14 +176,14 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
     const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
     const int nb = max(0, min(nblk - blk0, p.split_blocks));
     const int nstages = nb * C::SPB;
-    __syncthreads();
+    __syncthreads();                                 // barriers initialised
     if (split >= nsplit) {
         grid_dependents_launch();
         return;
     }
 
-    // ------------------------------------------------------------ producer warp
-    if (warp == C::NCW) {
+    // ------------------------------------------------------------ producer warp (PROD)
+    if (PROD && warp == C::NCW) {
         if (lane == 0) prefetch_tensormap(&tmc);
         int issued = 0;
         bool ok = true;
@@ -197,7 +232,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
             }
         }
         grid_dependents_launch();
-        if (lane == 0) {
+        if (lane == 0) {                            // the CTA must not exit with copies in flight
             for (int it = max(0, issued - NSTAGE); it < issued; ++it) {
                 if (!mbar_wait_bounded(smem_u32(full + (it % NSTAGE)),
                                        static_cast<uint32_t>(it / NSTAGE) & 1u)) {
@@ -210,6 +245,14 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
     }
 
     // ------------------------------------------------------------ consumer warps
+    int issued = 0;                                  // thread 0 (not PROD): loads issued
+    if (!PROD && threadIdx.x == 0) {
+        prefetch_tensormap(&tmc);
+        for (; issued < min(NSTAGE, nstages); ++issued)
+            issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
+                                        p.err);
+    }
+
     MlaState st;
 #pragma unroll
     for (int ms = 0; ms < C::MSW; ++ms)
@@ -238,7 +281,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
             off_v[ms] = swz_off<C::DCH>(tok_v, 2 * (warp * C::MSW + ms) + (quad & 1));
     }
     float* xw = xbuf + warp * (C::MT * C::NTT * 32 * 4) + lane * 4;
-    int done = 0;                                   // stages that went through the exchange
+    int waited = 0;                                  // stages this CTA has seen arrive
 
     for (int it = 0; it < nstages; ++it) {
         const int s = it % NSTAGE;
@@ -248,9 +291,10 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
             atomicOr(p.err, KV_DEVERR_TIMEOUT);
             flags[0] = 1;
         }
+        if (arrived) waited = it + 1;
         const int blk = arrived ? stage_blk[s] : -1;
         const uint32_t tile = smem_u32(smem + s * C::STAGE);
-        const int xo = (done & 1) * C::XFLOATS;
+        const int xo = (it & 1) * C::XFLOATS;
 
         // ---- partial scores over this warp's 144 numbers
         float sc[C::MT][C::NTT][4];
@@ -272,7 +316,8 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                         mma_bf16_16816(sc[mt][nt], a, qf[kk][nt][0], qf[kk][nt][1]);
                 }
         }
-        // ---- exchange: every warp publishes its partial sums, then adds all four
+        // ---- exchange: every warp publishes its partial sums, then adds all four.
+        // Past this barrier every warp is also done with stage it - 1.
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt)
 #pragma unroll
@@ -280,11 +325,17 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                 *reinterpret_cast<float4*>(xw + xo + (mt * C::NTT + nt) * 128) =
                     make_float4(sc[mt][nt][0], sc[mt][nt][1], sc[mt][nt][2], sc[mt][nt][3]);
         named_barrier_sync(1, C::NCW * 32);
-        ++done;
         if (flags[0]) break;                        // a stage never arrived: all warps leave
+        if (!PROD && threadIdx.x == 0 && it >= 1 && issued < nstages) {
+            issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
+                                        p.err);   // into the slot of stage it - 1
+            ++issued;
+        }
         if (blk < 0) {                              // skipped (bad id): nothing to fold in
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(empty + s));
+            if (PROD) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(empty + s));
+            }
             continue;
         }
         {
@@ -310,7 +361,6 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                     sc[mt][nt][3] = acc.w;
                 }
         }
-
         // ---- online softmax (log2 domain); tokens at or past lim are not cached.
         // The max is taken on the raw scores (the scale is positive) and the scale
         // is applied inside the exponent: p = 2^(s * sl2 - m).
@@ -412,8 +462,18 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        if (PROD) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        }
+    }
+    if (!PROD && threadIdx.x == 0) {
+        // loads issued but never waited for (only after a timeout) must land first
+        for (int it = waited; it < issued; ++it) {
+            if (!mbar_wait_bounded(smem_u32(full + (it % NSTAGE)),
+                                   static_cast<uint32_t>(it / NSTAGE) & 1u))
+                break;
+        }
     }
 
     // ------------------------------------------------------------ epilogue
@@ -531,20 +591,20 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 
 namespace {
 
-template <int BS, bool DEEP>
+template <int BS, bool PROD>
 struct MlaVariant {
-    static constexpr int SUB = BS < 32 ? BS : 32;
-    static constexpr int NSTAGE = (SUB == 16 ? 4 : 2) * (DEEP ? 5 : 2) / 2;
-    using C = MlaCfg<BS, SUB, NSTAGE>;
+    static constexpr int SUB = PROD ? (BS < 32 ? BS : 32) : 16;
+    static constexpr int NSTAGE = PROD ? (SUB == 16 ? 4 : 2) : 3;
+    using C = MlaCfg<BS, SUB, NSTAGE, PROD>;
     static cudaError_t prepare()
     {
-        return cudaFuncSetAttribute(paged_mla_decode_main<BS, SUB, NSTAGE>,
+        return cudaFuncSetAttribute(paged_mla_decode_main<BS, SUB, NSTAGE, PROD>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     }
     static cudaError_t launch(dim3 grid, const CUtensorMap& tm, const MlaParams& p, cudaStream_t s)
     {
-        return launch_dependent(paged_mla_decode_main<BS, SUB, NSTAGE>, grid, dim3(C::THREADS),
-                                C::SMEM, s, tm, p);
+        return launch_dependent(paged_mla_decode_main<BS, SUB, NSTAGE, PROD>, grid,
+                                dim3(C::THREADS), C::SMEM, s, tm, p);
     }
 };
 
@@ -557,12 +617,12 @@ cudaError_t prepare_both()
 
 }  // namespace
 
-int mla_stage_tokens(int block_size)
+int mla_stage_tokens(int block_size, bool prod)
 {
     switch (block_size) {
-    case 16: return MlaVariant<16, false>::SUB;
-    case 32: return MlaVariant<32, false>::SUB;
-    case 64: return MlaVariant<64, false>::SUB;
+    case 16: return prod ? MlaVariant<16, true>::SUB : MlaVariant<16, false>::SUB;
+    case 32: return prod ? MlaVariant<32, true>::SUB : MlaVariant<32, false>::SUB;
+    case 64: return prod ? MlaVariant<64, true>::SUB : MlaVariant<64, false>::SUB;
     default: return 0;
     }
 }
@@ -577,15 +637,15 @@ cudaError_t prepare_mla_decode(int block_size)
     }
 }
 
-cudaError_t launch_mla_decode(int block_size, bool deep, dim3 grid, const CUtensorMap& tm,
+cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtensorMap& tm,
                               const MlaParams& p, cudaStream_t s)
 {
     switch (block_size) {
-    case 16: return deep ? MlaVariant<16, true>::launch(grid, tm, p, s)
+    case 16: return prod ? MlaVariant<16, true>::launch(grid, tm, p, s)
                          : MlaVariant<16, false>::launch(grid, tm, p, s);
-    case 32: return deep ? MlaVariant<32, true>::launch(grid, tm, p, s)
+    case 32: return prod ? MlaVariant<32, true>::launch(grid, tm, p, s)
                          : MlaVariant<32, false>::launch(grid, tm, p, s);
-    case 64: return deep ? MlaVariant<64, true>::launch(grid, tm, p, s)
+    case 64: return prod ? MlaVariant<64, true>::launch(grid, tm, p, s)
                          : MlaVariant<64, false>::launch(grid, tm, p, s);
     default: return cudaErrorInvalidValue;
     }

@@ -119,11 +119,11 @@ cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
-// Tokens per pipeline stage of the latent decode (0: block size not supported).
-int mla_stage_tokens(int block_size);
+// Tokens per pipeline stage of the latent decode (0: block size not supported);
+// prod: the variant with a producer warp (small grids), else the three-CTA one.
+int mla_stage_tokens(int block_size, bool prod);
 cudaError_t prepare_mla_decode(int block_size);
-// deep: the one-CTA-per-SM variant with a deep ring of stages (small grids).
-cudaError_t launch_mla_decode(int block_size, bool deep, dim3 grid, const CUtensorMap& tm,
+cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtensorMap& tm,
                               const MlaParams& p, cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
