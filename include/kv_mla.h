@@ -47,8 +47,15 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
                              int device, kv_pool** out);
 
 /* Split-KV plan (see paged_decode_plan): chunk size in tokens, a multiple of
- * block_size (0 = automatic: 768 .. 2048 tokens from the batch, heads and SM
- * count), and the most chunks a sequence can have. */
+ * block_size (0 = automatic, from the batch, heads and SM count: 768 .. 2048
+ * tokens, or 2048 .. 4096 for the tensor-core form), and the most chunks a
+ * sequence can have.
+ *
+ * Two kernels serve this call.  Latent pools with blocks of 64 tokens and at
+ * least 64 query heads run the tcgen05 form: tiles of 128 heads on the MMA's M
+ * dimension, queries and accumulators in tensor memory, four CTAs per sequence
+ * chunk each producing a quarter of the latent output.  Other shapes run the
+ * mma.sync form with tiles of 16 heads. */
 kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                 int kv_split_tokens, int* split_tokens, int* max_splits);
 

@@ -30,6 +30,9 @@ struct kv_pool {
     CUtensorMap tmk, tmv;   // 5-D tile maps of the K and V pools; latent pools: the map
                             // with the stage box of the producer-warp decode (tmk) and of
                             // the three-CTA decode (tmv)
+    CUtensorMap tmt;        // latent pools with blocks of 64: one 128-byte piece of a block
+                            // per box (the tcgen05 decode)
+    int has_tc;
     int num_sms;
     int mla;                // 1: latent pool (one cached vector per token, no V half)
 };
@@ -87,7 +90,8 @@ bool variant_supported(kv_dtype dtype, int head_dim, int block_size)
 // Tile map of one pool half: dims (innermost first) = 128-byte row piece,
 // pieces per token row, kv head, slot, block; a box is one block of one kv
 // head, written to shared memory with the 128-byte swizzle.
-kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map, int slots_per_box = 0)
+kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map, int slots_per_box = 0,
+                          int pieces_per_box = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return KV_ERR_CUDA;
@@ -98,7 +102,8 @@ kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map, int
                                 static_cast<cuuint64_t>(p->num_blocks)};
     const cuuint64_t strides[4] = {128, row, row * p->kv_heads, row * p->kv_heads * p->block_size};
     const cuuint32_t box[5] = {static_cast<cuuint32_t>(per_piece),
-                               static_cast<cuuint32_t>(row / 128), 1,
+                               static_cast<cuuint32_t>(pieces_per_box > 0 ? pieces_per_box
+                                                                          : row / 128), 1,
                                static_cast<cuuint32_t>(slots_per_box > 0 ? slots_per_box
                                                                          : p->block_size), 1};
     const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
@@ -529,7 +534,14 @@ constexpr int kMlaHeadTile = 16;
 
 struct MlaPlan {
     int head_tiles, split_blocks, max_splits;
+    int tc;                 // tcgen05 form: head tiles of 128, four latent quarters each
 };
+
+// The tcgen05 form takes wide head tiles (at least 64 real heads of 128 rows).
+bool use_tc(const kv_pool* pl, int q_heads)
+{
+    return pl->has_tc && q_heads >= 64;
+}
 
 // Automatic chunk: about eight chunks per SM over the worst case, kept between
 // 768 and 2048 tokens.  Measured on GB300 (DeepSeek-shaped layer, contexts
@@ -545,9 +557,22 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
     if (static_cast<long long>(max_blocks) * pl->block_size > std::numeric_limits<int>::max())
         return KV_ERR_INVALID_ARG;
     MlaPlan p;
-    p.head_tiles = (q_heads + kMlaHeadTile - 1) / kMlaHeadTile;
+    p.tc = use_tc(pl, q_heads) ? 1 : 0;
+    const int tile = p.tc ? kvp::MLA_TC_HEADS : kMlaHeadTile;
+    p.head_tiles = (q_heads + tile - 1) / tile;
     if (split_tokens > 0) {
         p.split_blocks = split_tokens / pl->block_size;
+    } else if (p.tc) {
+        // one CTA per SM: about two chunks per SM over the worst case, 2048..4096 tokens
+        // (measured on GB300, 128 heads, contexts in [512, 4096]: 3072-token chunks
+        // 215 us, 2048 234 us, 1024 274 us -- each chunk pays a query load and a merge)
+        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles * 4;
+        const long long work = units * max_blocks * pl->block_size;
+        const long long target = static_cast<long long>(pl->num_sms > 0 ? pl->num_sms : 148) * 2;
+        long long tok = (work + target - 1) / target;
+        if (tok < 2048) tok = 2048;
+        if (tok > 4096) tok = 4096;
+        p.split_blocks = static_cast<int>((tok + pl->block_size - 1) / pl->block_size);
     } else {
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles;
         const long long work = units * max_blocks * pl->block_size;
@@ -559,7 +584,8 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
     }
     if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
     p.max_splits = (max_blocks + p.split_blocks - 1) / p.split_blocks;
-    if (p.max_splits > 65535 || p.head_tiles > 65535 || batch > 65535) return KV_ERR_UNSUPPORTED;
+    if (p.max_splits > 65535 || p.head_tiles * (p.tc ? 4LL : 1LL) > 65535 || batch > 65535)
+        return KV_ERR_UNSUPPORTED;
     *out = p;
     return KV_OK;
 }
@@ -573,7 +599,7 @@ WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
     const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
     w.part_ml = round_up(n * kvp::MLA_DV * sizeof(float), kAlign);
     w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
-    w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * sizeof(int);
+    w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * (p.tc ? 4 : 1) * sizeof(int);
     w.total = w.tickets + w.ticket_bytes;
     return w;
 }
@@ -633,6 +659,11 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
         st = encode_pool_map(p, p->k, &p->tmk, kvp::mla_stage_tokens(block_size, true));
     if (st == KV_OK)
         st = encode_pool_map(p, p->k, &p->tmv, kvp::mla_stage_tokens(block_size, false));
+    if (st == KV_OK && block_size == kvp::MLA_TC_BLOCK) {
+        st = encode_pool_map(p, p->k, &p->tmt, block_size, 1);
+        if (st == KV_OK && kvp::prepare_mla_decode_tc() != cudaSuccess) st = KV_ERR_CUDA;
+        p->has_tc = 1;
+    }
     if (st == KV_OK && kvp::prepare_mla_decode(block_size) != cudaSuccess) st = KV_ERR_CUDA;
     if (st == KV_OK && cudaDeviceSynchronize() != cudaSuccess) st = KV_ERR_CUDA;
     if (st != KV_OK) {
@@ -708,6 +739,15 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
+    if (plan.tc) {
+        // x = head tile * 4 + latent quarter, y = sequence, z = chunk
+        const dim3 grid(static_cast<unsigned>(plan.head_tiles * 4), static_cast<unsigned>(batch),
+                        static_cast<unsigned>(plan.max_splits));
+        return kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? KV_OK
+                   : KV_ERR_CUDA;
+    }
     // chunk-major grid: x = head tile, y = sequence, z = chunk.  Grids of up to
     // three CTAs per SM run the producer-warp variant (32-token stages, two CTAs
     // per SM), larger ones the three-CTAs-per-SM variant (16-token stages).

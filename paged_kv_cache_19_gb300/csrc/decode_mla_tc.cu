@@ -1,0 +1,480 @@
+// decode_mla_tc.cu -- absorbed multi-head latent attention on the 5th-generation
+// tensor cores (tcgen05), for wide head tiles: all 128 query heads of a sequence
+// on the MMA's M dimension (xuewyang.github.io/posts/kv, "MLA: how does decode
+// get full-size keys and values back?": every head scores the shared cached
+// vector -- 512 latent + 64 rotary-key numbers -- and averages its latent part).
+//
+// One CTA per (sequence, tile of 128 heads, quarter of the latent output, split
+// chunk); 192 threads:
+//   * warp 4 streams one 64-token block per stage with nine TMA loads (one per
+//     128-byte piece of the 576 numbers, 128-byte swizzle), so a stage is nine
+//     [64 tokens x 64 numbers] K-major tiles: 72 KB, 3 stages;
+//   * warp 5 (one thread) issues the MMAs.  Scores S[128 heads x 64 tokens] =
+//     Q . C^T: A = the absorbed queries, kept in tensor memory for the whole
+//     chunk (128 lanes x 288 columns), B = the stage (K-major), 36 MMAs of K = 16.
+//     Then O[128 heads x 128 latent] += P . C[:, quarter]: A = the probabilities
+//     in tensor memory, B = the same stage read MN-major (the latent numbers of a
+//     token are contiguous), 4 MMAs.  Completion is signalled by tcgen05.commit on
+//     mbarriers.  The scores of stage i+1 are computed while the softmax of stage
+//     i runs, and the output update of stage i while the softmax of stage i+1 runs.
+//   * warps 0-3: thread h owns head h (tensor-memory lane h): it reads its 64
+//     scores, keeps the running max and sum, writes its 64 probabilities (bf16)
+//     back to tensor memory and, at the end, reads its 128 outputs, normalises
+//     and stores them.  The output is rescaled only when the running max grows by
+//     more than 2^8 (log2 units); until then the older maximum stays the
+//     reference, which is exact because the final division uses the sum taken
+//     against the same reference.
+//   * the four quarter-CTAs of a sequence chunk compute the same scores (the
+//     tensor memory of an SM holds the fp32 output of 128 heads x 128 latent
+//     numbers beside the queries and one score tile, not more) and read the same
+//     stages, which the L2 serves after the first.
+//   * tensor memory: queries [0, 288), scores [288, 352), probabilities
+//     [352, 384), output [384, 512).
+// Every wait is bounded; a late barrier sets KV_DEVERR_TIMEOUT and every role
+// leaves its loop, waits (bounded) for its copies and MMAs in flight, and the CTA
+// frees its tensor memory before it exits.
+#include "decode_common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace kvp {
+
+namespace {
+
+constexpr int TC_TOK = 64;                      // tokens per stage (one block)
+constexpr int TC_NSTAGE = 3;
+constexpr int TC_PIECE = TC_TOK * 128;          // one 64-number piece of 64 tokens
+constexpr int TC_NPIECE = MLA_DK / 64;          // 9
+constexpr int TC_STAGE = TC_NPIECE * TC_PIECE;  // 73,728 bytes
+constexpr int TC_DQ = 128;                      // latent numbers per CTA
+constexpr int TC_M = 128;                       // heads per CTA
+constexpr int TC_THREADS = 192;
+constexpr uint32_t TM_Q = 0, TM_S = 288, TM_P = 352, TM_O = 384, TM_COLS = 512;
+constexpr uint32_t IDESC_S = tc_idesc_bf16(TC_M, TC_TOK, 0, 0);
+constexpr uint32_t IDESC_O = tc_idesc_bf16(TC_M, TC_DQ, 0, 1);
+constexpr float RESCALE_LOG2 = 8.f;
+constexpr int TC_CTL = 256;
+constexpr int TC_SMEM = 1024 + TC_NSTAGE * TC_STAGE + TC_CTL;
+static_assert(TC_SMEM <= 227 * 1024, "one CTA per SM");
+static_assert(TM_O + TC_DQ <= TM_COLS && TM_P + TC_TOK / 2 <= TM_O && TM_S + TC_TOK <= TM_P &&
+                  TM_Q + MLA_DK / 2 <= TM_S,
+              "tensor-memory columns");
+
+struct TcCtl {
+    uint64_t kv_full[TC_NSTAGE];
+    uint64_t kv_empty[TC_NSTAGE];
+    uint64_t s_full, s_free, p_full, p_free, q_ready, mma_done;
+    uint32_t tmem_base;
+    int stage_blk[TC_NSTAGE];
+    int abort_flag;
+    int merge_flag;
+};
+static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
+
+__device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
+
+// The output update of stage k: O += P . C[:, quarter] over its 64 tokens.
+__device__ __forceinline__ void issue_output_mma(uint32_t tbase, uint32_t stage_addr, int dq, bool first)
+{
+#pragma unroll
+    for (int kk = 0; kk < TC_TOK / 16; ++kk) {
+        const uint64_t b = tc_smem_desc(stage_addr + 2 * dq * TC_PIECE + kk * 2048, TC_PIECE, 1024);
+        tc_mma_ts(tbase + TM_O, tbase + TM_P + kk * 8, b, IDESC_O, !(first && kk == 0));
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    TcCtl* ctl = reinterpret_cast<TcCtl*>(smem + TC_NSTAGE * TC_STAGE);
+
+    const int dq = blockIdx.x & 3;
+    const int ht = blockIdx.x >> 2;
+    const int b = blockIdx.y;
+    const int split = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int blk0 = split * p.split_blocks;
+    const int nh = min(TC_M, p.q_heads - ht * TC_M);
+    const size_t row0 = static_cast<size_t>(b) * p.q_heads + ht * TC_M;
+
+    if (tid == 0) {
+        for (int i = 0; i < TC_NSTAGE; ++i) {
+            mbar_init(smem_u32(&ctl->kv_full[i]), 1);
+            mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&ctl->s_full), 1);
+        mbar_init(smem_u32(&ctl->s_free), 4);
+        mbar_init(smem_u32(&ctl->p_full), 4);
+        mbar_init(smem_u32(&ctl->p_free), 1);
+        mbar_init(smem_u32(&ctl->q_ready), 4);
+        mbar_init(smem_u32(&ctl->mma_done), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    grid_dependency_wait();
+
+    int ctx = __ldg(p.ctx + b);
+    const int cap = p.max_blocks * TC_TOK;
+    if (ctx < 0 || ctx > cap) {
+        if (tid == 0 && split == 0 && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int nblk = (ctx + TC_TOK - 1) / TC_TOK;
+    const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
+    const int nstages = max(0, min(nblk - blk0, p.split_blocks));   // one block per stage
+    const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+    __syncthreads();
+    if (split >= nsplit) {                          // uniform: before any tensor memory
+        grid_dependents_launch();
+        return;
+    }
+    if (warp == 5) tc_alloc(smem_u32(&ctl->tmem_base), TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = ctl->tmem_base;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ loads
+        if (lane == 0) {
+            prefetch_tensormap(&tmp);
+            int issued = 0;
+            for (int it = 0; it < nstages; ++it) {
+                const int st = it % TC_NSTAGE;
+                const uint32_t ph = static_cast<uint32_t>(it / TC_NSTAGE) & 1u;
+                if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty[st]), ph ^ 1u)) {
+                    atomicOr(p.err, KV_DEVERR_TIMEOUT);
+                    ctl->abort_flag = 1;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
+                int blk = __ldg(trow + it);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    atomicOr(p.err, KV_DEVERR_BLOCK_ID);
+                    blk = -1;
+                }
+                ctl->stage_blk[st] = blk;
+                const uint32_t fb = smem_u32(&ctl->kv_full[st]);
+                if (blk >= 0) {
+                    mbar_arrive_expect_tx(fb, TC_STAGE);
+                    const uint32_t dst = smem_u32(smem + st * TC_STAGE);
+                    for (int pc = 0; pc < TC_NPIECE; ++pc)
+                        tma_load_5d(dst + pc * TC_PIECE, &tmp, 0, pc, 0, 0, blk, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
+                issued = it + 1;
+            }
+            // copies still in flight must land before the CTA moves on
+            for (int it = max(0, issued - TC_NSTAGE); it < issued; ++it)
+                if (!mbar_wait_bounded(smem_u32(&ctl->kv_full[it % TC_NSTAGE]),
+                                       static_cast<uint32_t>(it / TC_NSTAGE) & 1u))
+                    break;
+        }
+        grid_dependents_launch();
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(smem_u32(&ctl->q_ready), 0);
+            int out_issued = 0;                     // stages whose output update is issued
+            for (int it = 0; ok && it < nstages; ++it) {
+                const int st = it % TC_NSTAGE;
+                ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]),
+                                       static_cast<uint32_t>(it / TC_NSTAGE) & 1u);
+                if (ok && it >= 1)
+                    ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(it - 1) & 1u);
+                if (!ok || *reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + st * TC_STAGE);
+#pragma unroll 4
+                for (int ks = 0; ks < MLA_DK / 16; ++ks) {
+                    const uint64_t bdesc =
+                        tc_smem_desc(sa + (ks >> 2) * TC_PIECE + (ks & 3) * 32, 16, 1024);
+                    tc_mma_ts(tbase + TM_S, tbase + TM_Q + ks * 8, bdesc, IDESC_S, ks > 0);
+                }
+                tc_commit(smem_u32(&ctl->s_full));
+                if (it >= 1) {
+                    ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(it - 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int k = it - 1;
+                    issue_output_mma(tbase, smem_u32(smem + (k % TC_NSTAGE) * TC_STAGE), dq, k == 0);
+                    tc_commit(smem_u32(&ctl->p_free));
+                    tc_commit(smem_u32(&ctl->kv_empty[k % TC_NSTAGE]));
+                    out_issued = it;
+                }
+            }
+            if (ok && nstages >= 1 && out_issued == nstages - 1) {
+                const int k = nstages - 1;
+                ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(k) & 1u);
+                if (ok) {
+                    tc_fence_after();
+                    issue_output_mma(tbase, smem_u32(smem + (k % TC_NSTAGE) * TC_STAGE), dq, k == 0);
+                    tc_commit(smem_u32(&ctl->p_free));
+                    tc_commit(smem_u32(&ctl->kv_empty[k % TC_NSTAGE]));
+                }
+            }
+            if (!ok) {
+                atomicOr(p.err, KV_DEVERR_TIMEOUT);
+                ctl->abort_flag = 1;
+            }
+            // every MMA issued must be complete before the tensor memory is freed
+            tc_commit(smem_u32(&ctl->mma_done));
+            mbar_wait_bounded(smem_u32(&ctl->mma_done), 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int h = tid;                          // head of the tile = tensor-memory lane
+        const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        {
+            const uint4* qg = reinterpret_cast<const uint4*>(p.q + (row0 + (h < nh ? h : 0)) * MLA_DK);
+#pragma unroll 1
+            for (int c9 = 0; c9 < TC_NPIECE; ++c9) {
+                uint32_t r[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 x = h < nh ? __ldg(qg + c9 * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+                    r[4 * v] = x.x;
+                    r[4 * v + 1] = x.y;
+                    r[4 * v + 2] = x.z;
+                    r[4 * v + 3] = x.w;
+                }
+                tc_st32(lrow + TM_Q + c9 * 32, r);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->q_ready));
+        }
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int it = 0; it < nstages; ++it) {
+            const int st = it % TC_NSTAGE;
+            ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(it / TC_NSTAGE) & 1u);
+            if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->s_full), static_cast<uint32_t>(it) & 1u);
+            ok = all_ok(ok);
+            if (!ok || __any_sync(FULL_MASK, *reinterpret_cast<volatile int*>(&ctl->abort_flag) != 0)) break;
+            tc_fence_after();
+            const int blk = ctl->stage_blk[st];
+            const int nvalid = blk < 0 ? 0 : min(TC_TOK, ctx - (blk0 + it) * TC_TOK);
+            float s[TC_TOK];
+            {
+                uint32_t r[32];
+                tc_ld32(lrow + TM_S, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
+                tc_ld32(lrow + TM_S + 32, r);
+                tc_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free));
+
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < TC_TOK; ++j) {
+                if (j >= nvalid) s[j] = -INFINITY;   // not cached (may be NaN)
+                mx = fmaxf(mx, s[j]);
+            }
+            const float m_new = fmaxf(m_ref, mx * sl2);
+            float f = 1.f;
+            if (m_ref == -INFINITY) {
+                m_ref = m_new;                      // nothing accumulated yet
+            } else if (m_new > m_ref + RESCALE_LOG2) {
+                f = fast_exp2(m_ref - m_new);
+                l *= f;
+                m_ref = m_new;
+            }
+            if (__any_sync(FULL_MASK, f != 1.f)) {
+                // O holds stages < it: wait for the last of their updates, then scale
+                ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(it - 1) & 1u));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c4 = 0; c4 < TC_DQ / 32; ++c4) {
+                    uint32_t r[32];
+                    tc_ld32(lrow + TM_O + c4 * 32, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                    tc_st32(lrow + TM_O + c4 * 32, r);
+                }
+                tc_wait_st();
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t pk[32];
+            float ls = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = fast_exp2(fmaf(s[2 * j], sl2, -m_use));
+                const float p1 = fast_exp2(fmaf(s[2 * j + 1], sl2, -m_use));
+                ls += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l += ls;
+            if (nvalid < TC_TOK) {
+                // values of tokens past the cache (or of a skipped block) are zeroed so
+                // that 0 * NaN cannot reach the output sums
+                uint8_t* sp = smem + st * TC_STAGE + 2 * dq * TC_PIECE;
+                for (int i = tid; i < (TC_TOK - nvalid) * 16; i += 128) {
+                    const int row = nvalid + (i >> 4);
+                    const int pc = (i >> 3) & 1;
+                    const int ch = i & 7;
+                    *reinterpret_cast<uint4*>(sp + pc * TC_PIECE + row * 128 + (ch << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            if (it >= 1) {
+                // the previous probabilities must have been consumed
+                ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(it - 1) & 1u));
+                if (!ok) break;
+            }
+            tc_fence_after();
+            tc_st32(lrow + TM_P, pk);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+        }
+        if (!ok && lane == 0) {
+            atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            ctl->abort_flag = 1;
+        }
+        if (ok && nstages >= 1)
+            ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(nstages - 1) & 1u));
+        tc_fence_after();
+
+        // ---- epilogue: this thread's head, latent numbers 128 dq .. 128 dq + 127
+        const size_t bh = row0 + h;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool write = ok && h < nh;
+        const bool whole = nsplit == 1;
+        {
+#pragma unroll 1
+            for (int c4 = 0; c4 < TC_DQ / 32; ++c4) {
+                uint32_t r[32];
+                if (nstages >= 1) {
+                    tc_ld32(lrow + TM_O + c4 * 32, r);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
+                if (!write) continue;
+                const int d0 = dq * TC_DQ + c4 * 32;
+                if (whole) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.part_o + (bh * p.max_splits + split) * MLA_DV + d0);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                }
+            }
+        }
+        if (write) {
+            if (whole) {
+                if (p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(m_ref, l);
+            } else {
+                // every quarter writes the same (max, sum); the merge of a quarter reads
+                // the pairs its own siblings wrote before counting themselves
+                p.part_ml[(bh * p.max_splits + split) * 2 + 0] = m_ref;
+                p.part_ml[(bh * p.max_splits + split) * 2 + 1] = l;
+                __threadfence();
+            }
+        }
+        if (!whole) {
+            named_barrier_sync(1, 128);
+            int* ticket = p.tickets + (static_cast<size_t>(b) * p.head_tiles + ht) * 4 + dq;
+            if (tid == 0) {
+                const int last = atomicAdd(ticket, 1) == nsplit - 1;
+                if (last) __threadfence();
+                ctl->merge_flag = last;
+            }
+            named_barrier_sync(1, 128);
+            if (ctl->merge_flag) {
+                if (h < nh) {
+                    const float* ml = p.part_ml + bh * p.max_splits * 2;
+                    float M = -INFINITY;
+                    for (int j = 0; j < nsplit; ++j)
+                        if (__ldcg(ml + 2 * j + 1) > 0.f) M = fmaxf(M, __ldcg(ml + 2 * j));
+                    float W = 0.f;
+                    for (int j = 0; j < nsplit; ++j) {
+                        const float lj = __ldcg(ml + 2 * j + 1);
+                        if (lj > 0.f) W += lj * fast_exp2(__ldcg(ml + 2 * j) - M);
+                    }
+                    const float winv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll 1
+                    for (int c8 = 0; c8 < TC_DQ / 8; ++c8) {
+                        const int d0 = dq * TC_DQ + c8 * 8;
+                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        for (int j = 0; j < nsplit; ++j) {
+                            const float lj = __ldcg(ml + 2 * j + 1);
+                            if (!(lj > 0.f)) continue;
+                            const float wj = lj * fast_exp2(__ldcg(ml + 2 * j) - M);
+                            const float4* src = reinterpret_cast<const float4*>(
+                                p.part_o + (bh * p.max_splits + j) * MLA_DV + d0);
+                            const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
+                            acc[0] += wj * a0.x;
+                            acc[1] += wj * a0.y;
+                            acc[2] += wj * a0.z;
+                            acc[3] += wj * a0.w;
+                            acc[4] += wj * a1.x;
+                            acc[5] += wj * a1.y;
+                            acc[6] += wj * a1.z;
+                            acc[7] += wj * a1.w;
+                        }
+                        *reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0) =
+                            make_uint4(pack_bf16x2(acc[0] * winv, acc[1] * winv), pack_bf16x2(acc[2] * winv, acc[3] * winv),
+                                       pack_bf16x2(acc[4] * winv, acc[5] * winv), pack_bf16x2(acc[6] * winv, acc[7] * winv));
+                    }
+                    if (p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(M, W);
+                }
+                if (tid == 0) *ticket = 0;
+            }
+        }
+        grid_dependents_launch();
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tc_dealloc(tbase, TM_COLS);
+    }
+}
+
+cudaError_t prepare_mla_decode_tc()
+{
+    return cudaFuncSetAttribute(paged_mla_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TC_SMEM);
+}
+
+cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
+                                 cudaStream_t s)
+{
+    return launch_dependent(paged_mla_decode_tc, grid, dim3(TC_THREADS), TC_SMEM, s, tm, p);
+}
+
+}  // namespace kvp

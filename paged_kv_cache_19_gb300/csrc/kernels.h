@@ -125,6 +125,13 @@ int mla_stage_tokens(int block_size, bool prod);
 cudaError_t prepare_mla_decode(int block_size);
 cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtensorMap& tm,
                               const MlaParams& p, cudaStream_t s);
+// The tcgen05 form: tiles of 128 heads, blocks of 64 tokens, four CTAs (latent
+// quarters) per (sequence, head tile, chunk); grid x = head tile * 4 + quarter.
+constexpr int MLA_TC_HEADS = 128;
+constexpr int MLA_TC_BLOCK = 64;
+cudaError_t prepare_mla_decode_tc();
+cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
+                                 cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
                                cudaStream_t s);

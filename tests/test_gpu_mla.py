@@ -32,6 +32,13 @@ SMALL = {
                              seed=209, split_tokens=64),
     "bs32_h64_many_ctas": M(batch=24, q_heads=64, block_size=32, ctx_uniform=(1, 400),
                             seed=210, split_tokens=64),
+    # blocks of 64 and at least 64 heads run the tcgen05 form (128-head tiles, latent quarters)
+    "tc_h128_split128": M(batch=4, q_heads=128, block_size=64, ctx=[1, 64, 65, 700], seed=211,
+                          split_tokens=128),
+    "tc_h96_padded_tile": M(batch=3, q_heads=96, block_size=64, ctx=[63, 200, 1000], seed=212),
+    "tc_h256_two_tiles": M(batch=2, q_heads=256, block_size=64, ctx=[130, 900], seed=213,
+                           split_tokens=256),
+    "tc_h64_long": M(batch=2, q_heads=64, block_size=64, ctx=[5000, 3], seed=214),
 }
 
 
@@ -87,12 +94,13 @@ def test_repeated_calls_are_identical(staged):
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
-def test_empty_sequence_and_out_of_range_length():
-    w = workloads.make(M(batch=2, q_heads=16, block_size=16, ctx=[40, 20], seed=207))
+@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128)])
+def test_empty_sequence_and_out_of_range_length(bs, heads):
+    w = workloads.make(M(batch=2, q_heads=heads, block_size=bs, ctx=[40, 20], seed=207))
     st = Staged(w)
     ctx = torch.tensor([0, 20], dtype=torch.int32, device="cuda")
-    out = torch.empty(2, 16, 512, dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty(2, 16, dtype=torch.float32, device="cuda")
+    out = torch.empty(2, heads, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(2, heads, dtype=torch.float32, device="cuda")
     kp.paged_mla_decode_attention(st.pool, st.q, st.tables, ctx, w.scale, out=out, lse=lse)
     torch.cuda.synchronize()
     assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
@@ -105,12 +113,13 @@ def test_empty_sequence_and_out_of_range_length():
     st.destroy()
 
 
-def test_bad_block_ids_are_skipped_and_flagged():
-    w = workloads.make(M(batch=2, q_heads=16, block_size=16, ctx=[50, 50], seed=208))
+@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128)])
+def test_bad_block_ids_are_skipped_and_flagged(bs, heads):
+    w = workloads.make(M(batch=2, q_heads=heads, block_size=bs, ctx=[150, 150], seed=208))
     st = Staged(w)
     tables = st.tables.clone()
     tables[0, 1] = w.num_blocks + 5
-    out = torch.empty(2, 16, 512, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(2, heads, 512, dtype=torch.bfloat16, device="cuda")
     kp.paged_mla_decode_attention(st.pool, st.q, tables, st.ctx, w.scale, out=out)
     assert st.pool.device_errors() & kp.DEVERR_BLOCK_ID
     assert torch.isfinite(out.float()).all()
