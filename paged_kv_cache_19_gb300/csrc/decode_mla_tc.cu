@@ -5,11 +5,11 @@
 // vector -- 512 latent + 64 rotary-key numbers -- and averages its latent part).
 //
 // One CTA per (sequence, tile of 128 heads, quarter of the latent output, split
-// chunk); 192 threads:
-//   * warp 4 streams one 64-token block per stage with nine TMA loads (one per
+// chunk); 320 threads:
+//   * warp 8 streams one 64-token block per stage with nine TMA loads (one per
 //     128-byte piece of the 576 numbers, 128-byte swizzle), so a stage is nine
 //     [64 tokens x 64 numbers] K-major tiles: 72 KB, 3 stages;
-//   * warp 5 (one thread) issues the MMAs.  Scores S[128 heads x 64 tokens] =
+//   * warp 9 (one thread) issues the MMAs.  Scores S[128 heads x 64 tokens] =
 //     Q . C^T: A = the absorbed queries, kept in tensor memory for the whole
 //     chunk (128 lanes x 288 columns), B = the stage (K-major), 36 MMAs of K = 16.
 //     Then O[128 heads x 128 latent] += P . C[:, quarter]: A = the probabilities
@@ -17,13 +17,16 @@
 //     token are contiguous), 4 MMAs.  Completion is signalled by tcgen05.commit on
 //     mbarriers.  The scores of stage i+1 are computed while the softmax of stage
 //     i runs, and the output update of stage i while the softmax of stage i+1 runs.
-//   * warps 0-3: thread h owns head h (tensor-memory lane h): it reads its 64
-//     scores, keeps the running max and sum, writes its 64 probabilities (bf16)
-//     back to tensor memory and, at the end, reads its 128 outputs, normalises
-//     and stores them.  The output is rescaled only when the running max grows by
-//     more than 2^8 (log2 units); until then the older maximum stays the
-//     reference, which is exact because the final division uses the sum taken
-//     against the same reference.
+//   * warps 0-7: head h (tensor-memory lane h) belongs to two threads, one in
+//     warp h / 32 (tokens 0-31 of a stage, output columns 0-63) and one in warp
+//     h / 32 + 4 (tokens 32-63, columns 64-127) -- a warp can only reach its own
+//     quarter of the lanes, and two warps per quarter halve the serial work of
+//     each.  Each reads its 32 scores, the pair exchanges its maxima through
+//     shared memory, and each writes its 32 probabilities (bf16) back to tensor
+//     memory; at the end each normalises and stores its 64 outputs.  The output
+//     is rescaled only when the running max grows by more than 2^8 (log2
+//     units); until then the older maximum stays the reference, which is exact
+//     because the final division uses the sum taken against the same reference.
 //   * the four quarter-CTAs of a sequence chunk compute the same scores (the
 //     tensor memory of an SM holds the fp32 output of 128 heads x 128 latent
 //     numbers beside the queries and one score tile, not more) and read the same
@@ -48,12 +51,12 @@ constexpr int TC_NPIECE = MLA_DK / 64;          // 9
 constexpr int TC_STAGE = TC_NPIECE * TC_PIECE;  // 73,728 bytes
 constexpr int TC_DQ = 128;                      // latent numbers per CTA
 constexpr int TC_M = 128;                       // heads per CTA
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;                 // warps 0-7 softmax, 8 loads, 9 MMA
 constexpr uint32_t TM_Q = 0, TM_S = 288, TM_P = 352, TM_O = 384, TM_COLS = 512;
 constexpr uint32_t IDESC_S = tc_idesc_bf16(TC_M, TC_TOK, 0, 0);
 constexpr uint32_t IDESC_O = tc_idesc_bf16(TC_M, TC_DQ, 0, 1);
 constexpr float RESCALE_LOG2 = 8.f;
-constexpr int TC_CTL = 256;
+constexpr int TC_CTL = 4096;
 constexpr int TC_SMEM = 1024 + TC_NSTAGE * TC_STAGE + TC_CTL;
 static_assert(TC_SMEM <= 227 * 1024, "one CTA per SM");
 static_assert(TM_O + TC_DQ <= TM_COLS && TM_P + TC_TOK / 2 <= TM_O && TM_S + TC_TOK <= TM_P &&
@@ -68,19 +71,35 @@ struct TcCtl {
     int stage_blk[TC_NSTAGE];
     int abort_flag;
     int merge_flag;
+    float xmax[2][2][TC_M];                         // [stage parity][token half][head]
+    float xl[2][TC_M];                              // [token half][head]
 };
 static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
 
 __device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
 
+// The scores of a stage: S = Q . C^T, 36 MMAs of K = 16.  The descriptor of slice
+// ks is the stage's base descriptor plus a constant (16-byte units in the low
+// word), so each issue is one add: a single thread issues every MMA of the CTA
+// and its issue rate, not the tensor pipe, bounds small-N MMAs like these.
+__device__ __forceinline__ void issue_score_mma(uint32_t tbase, uint32_t stage_addr)
+{
+    const uint64_t d0 = tc_smem_desc(stage_addr, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < MLA_DK / 16; ++ks)
+        tc_mma_ts(tbase + TM_S + 0u, tbase + TM_Q + ks * 8,
+                  d0 + static_cast<uint64_t>(((ks >> 2) * TC_PIECE + (ks & 3) * 32) >> 4), IDESC_S,
+                  ks > 0);
+}
+
 // The output update of stage k: O += P . C[:, quarter] over its 64 tokens.
 __device__ __forceinline__ void issue_output_mma(uint32_t tbase, uint32_t stage_addr, int dq, bool first)
 {
+    const uint64_t d0 = tc_smem_desc(stage_addr + 2 * dq * TC_PIECE, TC_PIECE, 1024);
 #pragma unroll
-    for (int kk = 0; kk < TC_TOK / 16; ++kk) {
-        const uint64_t b = tc_smem_desc(stage_addr + 2 * dq * TC_PIECE + kk * 2048, TC_PIECE, 1024);
-        tc_mma_ts(tbase + TM_O, tbase + TM_P + kk * 8, b, IDESC_O, !(first && kk == 0));
-    }
+    for (int kk = 0; kk < TC_TOK / 16; ++kk)
+        tc_mma_ts(tbase + TM_O, tbase + TM_P + kk * 8, d0 + static_cast<uint64_t>((kk * 2048) >> 4),
+                  IDESC_O, !(first && kk == 0));
 }
 
 }  // namespace
@@ -110,10 +129,10 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
         }
         mbar_init(smem_u32(&ctl->s_full), 1);
-        mbar_init(smem_u32(&ctl->s_free), 4);
-        mbar_init(smem_u32(&ctl->p_full), 4);
+        mbar_init(smem_u32(&ctl->s_free), 8);
+        mbar_init(smem_u32(&ctl->p_full), 8);
         mbar_init(smem_u32(&ctl->p_free), 1);
-        mbar_init(smem_u32(&ctl->q_ready), 4);
+        mbar_init(smem_u32(&ctl->q_ready), 8);
         mbar_init(smem_u32(&ctl->mma_done), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -135,27 +154,29 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         grid_dependents_launch();
         return;
     }
-    if (warp == 5) tc_alloc(smem_u32(&ctl->tmem_base), TM_COLS);
+    if (warp == 9) tc_alloc(smem_u32(&ctl->tmem_base), TM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = ctl->tmem_base;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ loads
         if (lane == 0) {
             prefetch_tensormap(&tmp);
             int issued = 0;
+            int next_blk = nstages > 0 ? __ldg(trow) : -1;   // block id read one stage ahead
             for (int it = 0; it < nstages; ++it) {
                 const int st = it % TC_NSTAGE;
                 const uint32_t ph = static_cast<uint32_t>(it / TC_NSTAGE) & 1u;
+                int blk = next_blk;
+                if (it + 1 < nstages) next_blk = __ldg(trow + it + 1);
                 if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty[st]), ph ^ 1u)) {
                     atomicOr(p.err, KV_DEVERR_TIMEOUT);
                     ctl->abort_flag = 1;
                     break;
                 }
                 if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
-                int blk = __ldg(trow + it);
                 if (blk < 0 || blk >= p.num_blocks) {
                     atomicOr(p.err, KV_DEVERR_BLOCK_ID);
                     blk = -1;
@@ -179,7 +200,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     break;
         }
         grid_dependents_launch();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             bool ok = mbar_wait_bounded(smem_u32(&ctl->q_ready), 0);
@@ -192,13 +213,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(it - 1) & 1u);
                 if (!ok || *reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + st * TC_STAGE);
-#pragma unroll 4
-                for (int ks = 0; ks < MLA_DK / 16; ++ks) {
-                    const uint64_t bdesc =
-                        tc_smem_desc(sa + (ks >> 2) * TC_PIECE + (ks & 3) * 32, 16, 1024);
-                    tc_mma_ts(tbase + TM_S, tbase + TM_Q + ks * 8, bdesc, IDESC_S, ks > 0);
-                }
+                issue_score_mma(tbase, smem_u32(smem + st * TC_STAGE));
                 tc_commit(smem_u32(&ctl->s_full));
                 if (it >= 1) {
                     ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(it - 1) & 1u);
@@ -231,12 +246,14 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
-        const int h = tid;                          // head of the tile = tensor-memory lane
-        const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        const int half = warp >> 2;                 // token half of a stage, output half
+        const int h = (warp & 3) * 32 + lane;       // head of the tile = tensor-memory lane
+        const int st_id = warp * 32 + lane;         // 0 .. 255 among the softmax threads
+        const uint32_t lrow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         {
             const uint4* qg = reinterpret_cast<const uint4*>(p.q + (row0 + (h < nh ? h : 0)) * MLA_DK);
 #pragma unroll 1
-            for (int c9 = 0; c9 < TC_NPIECE; ++c9) {
+            for (int c9 = half * 5; c9 < (half ? TC_NPIECE : 5); ++c9) {
                 uint32_t r[32];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
@@ -256,37 +273,44 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        bool failed = false;                         // this thread has seen a wait give up
         for (int it = 0; it < nstages; ++it) {
             const int st = it % TC_NSTAGE;
             ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(it / TC_NSTAGE) & 1u);
             if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->s_full), static_cast<uint32_t>(it) & 1u);
             ok = all_ok(ok);
-            if (!ok || __any_sync(FULL_MASK, *reinterpret_cast<volatile int*>(&ctl->abort_flag) != 0)) break;
-            tc_fence_after();
-            const int blk = ctl->stage_blk[st];
-            const int nvalid = blk < 0 ? 0 : min(TC_TOK, ctx - (blk0 + it) * TC_TOK);
-            float s[TC_TOK];
-            {
+            if (!ok) failed = true;
+            const int blk = ok ? ctl->stage_blk[st] : -1;
+            const int nvalid_all = blk < 0 ? 0 : min(TC_TOK, ctx - (blk0 + it) * TC_TOK);
+            const int nvalid = nvalid_all - half * 32;   // of this thread's 32 tokens
+            float s[32];
+            if (ok) {
+                tc_fence_after();
                 uint32_t r[32];
-                tc_ld32(lrow + TM_S, r);
+                tc_ld32(lrow + TM_S + half * 32, r);
                 tc_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
-                tc_ld32(lrow + TM_S + 32, r);
-                tc_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free));
-
-            float mx = -INFINITY;
+            if (nvalid < 32) {
 #pragma unroll
-            for (int j = 0; j < TC_TOK; ++j) {
-                if (j >= nvalid) s[j] = -INFINITY;   // not cached (may be NaN)
-                mx = fmaxf(mx, s[j]);
+                for (int j = 0; j < 32; ++j)
+                    if (j >= nvalid) s[j] = -INFINITY;   // not cached (may be NaN)
             }
+            float mx = s[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, s[j]);
+            ctl->xmax[it & 1][half][h] = mx;
+            // Every softmax thread reaches this barrier each stage and leaves the loop
+            // here together, on any failure seen so far (its own or another role's).
+            if (named_barrier_or(2, 256, failed || *reinterpret_cast<volatile int*>(&ctl->abort_flag) != 0)) {
+                failed = true;
+                break;
+            }
+            mx = fmaxf(mx, ctl->xmax[it & 1][half ^ 1][h]);
             const float m_new = fmaxf(m_ref, mx * sl2);
             float f = 1.f;
             if (m_ref == -INFINITY) {
@@ -296,39 +320,48 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 l *= f;
                 m_ref = m_new;
             }
+            // Past the exchange barrier no warp leaves the loop on its own (its partner
+            // would wait at the next barrier): a failed wait is noted and the loop
+            // ends at the next barrier.
             if (__any_sync(FULL_MASK, f != 1.f)) {
                 // O holds stages < it: wait for the last of their updates, then scale
+                // this thread's half of the output row
                 ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(it - 1) & 1u));
-                if (!ok) break;
+                if (!ok) {
+                    failed = true;
+                    continue;
+                }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c4 = 0; c4 < TC_DQ / 32; ++c4) {
+                for (int c2 = 0; c2 < 2; ++c2) {
                     uint32_t r[32];
-                    tc_ld32(lrow + TM_O + c4 * 32, r);
+                    const uint32_t col = TM_O + half * 64 + c2 * 32;
+                    tc_ld32(lrow + col, r);
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                    tc_st32(lrow + TM_O + c4 * 32, r);
+                    tc_st32(lrow + col, r);
                 }
                 tc_wait_st();
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t pk[32];
+            uint32_t pk[16];
             float ls = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
                 const float p0 = fast_exp2(fmaf(s[2 * j], sl2, -m_use));
                 const float p1 = fast_exp2(fmaf(s[2 * j + 1], sl2, -m_use));
                 ls += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
             }
             l += ls;
-            if (nvalid < TC_TOK) {
+            if (nvalid_all < TC_TOK) {
                 // values of tokens past the cache (or of a skipped block) are zeroed so
                 // that 0 * NaN cannot reach the output sums
                 uint8_t* sp = smem + st * TC_STAGE + 2 * dq * TC_PIECE;
-                for (int i = tid; i < (TC_TOK - nvalid) * 16; i += 128) {
-                    const int row = nvalid + (i >> 4);
+                const int v0 = max(0, nvalid_all);
+                for (int i = st_id; i < (TC_TOK - v0) * 16; i += 256) {
+                    const int row = v0 + (i >> 4);
                     const int pc = (i >> 3) & 1;
                     const int ch = i & 7;
                     *reinterpret_cast<uint4*>(sp + pc * TC_PIECE + row * 128 + (ch << 4)) =
@@ -339,60 +372,65 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             if (it >= 1) {
                 // the previous probabilities must have been consumed
                 ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(it - 1) & 1u));
-                if (!ok) break;
+                if (!ok) {
+                    failed = true;
+                    continue;
+                }
             }
             tc_fence_after();
-            tc_st32(lrow + TM_P, pk);
+            tc_st16(lrow + TM_P + half * 16, pk);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
         }
-        if (!ok && lane == 0) {
+        ok = !failed;
+        if (failed && lane == 0) {
             atomicOr(p.err, KV_DEVERR_TIMEOUT);
             ctl->abort_flag = 1;
         }
         if (ok && nstages >= 1)
             ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free), static_cast<uint32_t>(nstages - 1) & 1u));
         tc_fence_after();
+        ctl->xl[half][h] = l;
+        named_barrier_sync(1, 256);
+        l = ctl->xl[0][h] + ctl->xl[1][h];
 
-        // ---- epilogue: this thread's head, latent numbers 128 dq .. 128 dq + 127
+        // ---- epilogue: this thread's head, latent numbers 128 dq + 64 half .. + 63
         const size_t bh = row0 + h;
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const bool write = ok && h < nh;
         const bool whole = nsplit == 1;
-        {
 #pragma unroll 1
-            for (int c4 = 0; c4 < TC_DQ / 32; ++c4) {
-                uint32_t r[32];
-                if (nstages >= 1) {
-                    tc_ld32(lrow + TM_O + c4 * 32, r);
-                    tc_wait_ld();
-                } else {
+        for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t r[32];
+            if (nstages >= 1) {
+                tc_ld32(lrow + TM_O + half * 64 + c2 * 32, r);
+                tc_wait_ld();
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;
-                }
-                if (!write) continue;
-                const int d0 = dq * TC_DQ + c4 * 32;
-                if (whole) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0);
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+            if (!write) continue;
+            const int d0 = dq * TC_DQ + half * 64 + c2 * 32;
+            if (whole) {
+                uint4* dst = reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.part_o + (bh * p.max_splits + split) * MLA_DV + d0);
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(
+                        pack_bf16x2(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                        pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                        pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                        pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+            } else {
+                float4* dst = reinterpret_cast<float4*>(p.part_o + (bh * p.max_splits + split) * MLA_DV + d0);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-                }
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                         __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
             }
         }
-        if (write) {
+        if (write && half == 0) {
             if (whole) {
                 if (p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(m_ref, l);
             } else {
@@ -400,18 +438,18 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 // the pairs its own siblings wrote before counting themselves
                 p.part_ml[(bh * p.max_splits + split) * 2 + 0] = m_ref;
                 p.part_ml[(bh * p.max_splits + split) * 2 + 1] = l;
-                __threadfence();
             }
         }
         if (!whole) {
-            named_barrier_sync(1, 128);
+            __threadfence();
+            named_barrier_sync(1, 256);
             int* ticket = p.tickets + (static_cast<size_t>(b) * p.head_tiles + ht) * 4 + dq;
-            if (tid == 0) {
+            if (st_id == 0) {
                 const int last = atomicAdd(ticket, 1) == nsplit - 1;
                 if (last) __threadfence();
                 ctl->merge_flag = last;
             }
-            named_barrier_sync(1, 128);
+            named_barrier_sync(1, 256);
             if (ctl->merge_flag) {
                 if (h < nh) {
                     const float* ml = p.part_ml + bh * p.max_splits * 2;
@@ -425,8 +463,8 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     }
                     const float winv = W > 0.f ? 1.f / W : 0.f;
 #pragma unroll 1
-                    for (int c8 = 0; c8 < TC_DQ / 8; ++c8) {
-                        const int d0 = dq * TC_DQ + c8 * 8;
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const int d0 = dq * TC_DQ + half * 64 + c8 * 8;
                         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                         for (int j = 0; j < nsplit; ++j) {
                             const float lj = __ldcg(ml + 2 * j + 1);
@@ -448,9 +486,9 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                             make_uint4(pack_bf16x2(acc[0] * winv, acc[1] * winv), pack_bf16x2(acc[2] * winv, acc[3] * winv),
                                        pack_bf16x2(acc[4] * winv, acc[5] * winv), pack_bf16x2(acc[6] * winv, acc[7] * winv));
                     }
-                    if (p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(M, W);
+                    if (p.lse != nullptr && dq == 0 && half == 0) p.lse[bh] = lse_from(M, W);
                 }
-                if (tid == 0) *ticket = 0;
+                if (st_id == 0) *ticket = 0;
             }
         }
         grid_dependents_launch();
@@ -459,7 +497,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
     // ------------------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tc_dealloc(tbase, TM_COLS);
     }
