@@ -69,7 +69,20 @@ KERNEL_SOURCES = {
     "gqa": ["decode_kernel.cuh", "decode_common.cuh", "decode_bf16.cu", "decode_fp8.cu",
             "device_common.cuh"],
     "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
+    "mla_tc": ["decode_mla_tc.cu", "tcgen05.cuh", "decode_common.cuh", "device_common.cuh"],
 }
+
+
+def kernel_kind(spec) -> str:
+    """Which decode kernel a workload runs: the GQA kernel, or the mma.sync / tcgen05 form of
+    the latent decode (tcgen05 for blocks of 64 and at least 64 query heads)."""
+    if not spec.mla:
+        return "gqa"
+    return "mla_tc" if spec.block_size == 64 and spec.q_heads >= 64 else "mla"
+
+
+KERNEL_NAMES = {"gqa": "paged_decode_main", "mla": "paged_mla_decode_main (mma.sync)",
+                "mla_tc": "paged_mla_decode_tc (tcgen05)"}
 
 
 def kernel_source_sha(kind: str = "gqa") -> str:
@@ -88,7 +101,7 @@ def profiled_traffic(config: str):
     A profile summary under profiles/ states `kernel_source_sha:` and
     `dram_bytes_per_launch:` for a workload; it counts only while the sources
     are unchanged."""
-    sha = kernel_source_sha("mla" if workloads.CONFIGS[config].mla else "gqa")
+    sha = kernel_source_sha(kernel_kind(workloads.CONFIGS[config]))
     for path in glob.glob(os.path.join(PROFILES, "*.md")) + glob.glob(os.path.join(PROFILES, "*.txt")):
         text = open(path).read()
         m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
@@ -582,7 +595,7 @@ def run_ours(args, rank, world, local):
             "pct_of_peak": round(100 * value / peak, 2),
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
-            "roofline": {"kernel": ("paged_mla_decode_main" if s.mla else "paged_decode_main")
+            "roofline": {"kernel": KERNEL_NAMES[kernel_kind(s)]
                                    + " (one launch per decode call, in-kernel "
                                    "split-KV merge; K launches timed back to back after the "
                                    "timed steps)",

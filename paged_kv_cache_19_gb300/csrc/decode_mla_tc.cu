@@ -78,6 +78,19 @@ static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
 
 __device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
 
+// Named barrier that also returns, to every participant, the OR of their `pred`.
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 // The scores of a stage: S = Q . C^T, 36 MMAs of K = 16.  The descriptor of slice
 // ks is the stage's base descriptor plus a constant (16-byte units in the low
 // word), so each issue is one add: a single thread issues every MMA of the CTA

@@ -199,19 +199,6 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Named barrier that also returns, to every participant, the OR of their `pred`.
-__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
 {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
