@@ -60,9 +60,11 @@ kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int
                                 int kv_split_tokens, int* split_tokens, int* max_splits);
 
 /* Bytes of device workspace for these sizes (fp32 partials, (max, sum) pairs,
- * one 32-bit chunk counter per (sequence, tile of 16 heads)); 0 when every
- * sequence fits one chunk.  The workspace must be zero-filled before its first
- * use; every call leaves the counters at zero again. */
+ * one 32-bit chunk counter per (sequence, head tile[, latent quarter]), and for
+ * the tensor-core form two 32-bit work-queue counters); 0 when every sequence
+ * fits one chunk and the mma.sync form runs.  The workspace must be zero-filled
+ * before its first use; every call leaves the counters at zero again.  Calls
+ * sharing a workspace must not overlap in time. */
 kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                    int kv_split_tokens, size_t* bytes);
 

@@ -595,14 +595,22 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
 WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
 {
     WorkspaceLayout w{0, 0, 0, 0, 0};
-    if (p.max_splits <= 1) return w;
-    const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
-    w.part_ml = round_up(n * kvp::MLA_DV * sizeof(float), kAlign);
-    w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
-    w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * (p.tc ? 4 : 1) * sizeof(int);
-    w.total = w.tickets + w.ticket_bytes;
+    if (p.max_splits > 1) {
+        const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
+        w.part_ml = round_up(n * kvp::MLA_DV * sizeof(float), kAlign);
+        w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
+        w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * (p.tc ? 4 : 1) * sizeof(int);
+        w.total = w.tickets + w.ticket_bytes;
+    }
+    if (p.tc) {
+        // the persistent form's work counter (next item, CTAs done) follows the tickets
+        w.ticket_bytes = round_up(w.ticket_bytes, 16) + 2 * sizeof(int);
+        w.total = w.tickets + w.ticket_bytes;
+    }
     return w;
 }
+
+size_t mla_queue_offset(const WorkspaceLayout& w) { return w.total - 2 * sizeof(int); }
 
 }  // namespace
 
@@ -730,6 +738,7 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.part_o = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
     p.part_ml = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
     p.tickets = wl.total > 0 ? reinterpret_cast<int*>(ws + wl.tickets) : nullptr;
+    p.queue = plan.tc ? reinterpret_cast<int*>(ws + mla_queue_offset(wl)) : nullptr;
     p.err = pool->err;
     p.batch = batch;
     p.q_heads = q_heads;
@@ -740,9 +749,12 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
     if (plan.tc) {
-        // x = head tile * 4 + latent quarter, y = sequence, z = chunk
-        const dim3 grid(static_cast<unsigned>(plan.head_tiles * 4), static_cast<unsigned>(batch),
-                        static_cast<unsigned>(plan.max_splits));
+        // persistent: one CTA per SM (at most one per work item) pulling items
+        // (chunk, sequence, head tile, latent quarter) from the workspace counter
+        const long long items = static_cast<long long>(plan.head_tiles) * 4 * batch * plan.max_splits;
+        if (items > std::numeric_limits<int>::max()) return KV_ERR_UNSUPPORTED;
+        const int sms = pool->num_sms > 0 ? pool->num_sms : 148;
+        const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
         return kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream)) ==
                        cudaSuccess
                    ? KV_OK

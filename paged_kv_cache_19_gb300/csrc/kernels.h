@@ -69,6 +69,7 @@ struct MlaParams {
     float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum), log2 units
     uint32_t* err;
     int* tickets;             // [batch, head_tiles]; zero between calls
+    int* queue;               // tcgen05 form: [0] next work item, [1] CTAs done; zero between calls
     int batch, q_heads, head_tiles;
     int max_blocks, num_blocks;
     int split_blocks, max_splits;
