@@ -239,9 +239,19 @@ def rank_spec(config: str, rank: int):
     return spec if rank == 0 else replace(spec, seed=spec.seed + 100_000 * rank)
 
 
-def decode_bytes(w, split_tokens):
-    return (accounting.mla_decode_bytes(w, split_tokens) if w.spec.mla
-            else accounting.decode_bytes(w, split_tokens))
+def tc_grid(w, split_tokens, sms=152):
+    """CTAs of the tensor-core MLA launch (the library's rule: one per SM, no more than
+    ranges of split_blocks units the batch could hold)."""
+    s = w.spec
+    units = -(-s.q_heads // 128) * 2 * w.batch * w.max_blocks
+    return min(sms, max(1, units // max(1, split_tokens // s.block_size)))
+
+
+def decode_bytes(w, split_tokens, sms=152):
+    if w.spec.mla:
+        grid = tc_grid(w, split_tokens, sms) if kernel_kind(w.spec) == "mla_tc" else 0
+        return accounting.mla_decode_bytes(w, split_tokens, tc_grid=grid)
+    return accounting.decode_bytes(w, split_tokens)
 
 
 def workload_config(w, split_tokens, max_splits, world):
@@ -480,10 +490,13 @@ def run_ours(args, rank, world, local):
         append(stp["k"], stp["v"], tables, ctx, stp["seq"], stp["pos"])
         attend(q, tables, ctx)
 
-    dec_bytes = decode_bytes(w, split_tokens)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    dec_bytes = decode_bytes(w, split_tokens, sms)
     app_bytes = accounting.mla_append_bytes(w) if s.mla else accounting.append_bytes(w)
     step_bytes = dec_bytes["total"] + app_bytes
-    launches_per_step = 2                     # append + decode (the merge runs inside the decode)
+    # append + decode; the tensor-core MLA form adds its merge kernel when sequences can be
+    # cut into pieces (the other forms merge inside the decode kernel)
+    launches_per_step = 3 if kernel_kind(s) == "mla_tc" and max_splits > 1 else 2
     # (the decode-only roofline loop after the timed region launches K more decode kernels)
 
     for _ in range(max(3, args.warmup)):

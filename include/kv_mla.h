@@ -48,23 +48,25 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
 
 /* Split-KV plan (see paged_decode_plan): chunk size in tokens, a multiple of
  * block_size (0 = automatic, from the batch, heads and SM count: 768 .. 2048
- * tokens, or 2048 .. 4096 for the tensor-core form), and the most chunks a
- * sequence can have.
+ * tokens), and the most chunks a sequence can have.
  *
  * Two kernels serve this call.  Latent pools with blocks of 64 tokens and at
  * least 64 query heads run the tcgen05 form: tiles of 128 heads on the MMA's M
- * dimension, queries and accumulators in tensor memory, four CTAs per sequence
- * chunk each producing a quarter of the latent output.  Other shapes run the
- * mma.sync form with tiles of 16 heads. */
+ * dimension, accumulators in tensor memory, one CTA per SM.  Its work units
+ * (latent half, head tile, sequence, block) are cut into equal contiguous ranges,
+ * one per CTA; a sequence cut by a range boundary is merged from its pieces by a
+ * second kernel.  For it the chunk argument is the least number of tokens a range
+ * holds (0 = automatic: 256 .. 1024 tokens), and max_splits the most pieces a
+ * sequence can be cut into.  Other shapes run the mma.sync form with tiles of 16
+ * heads. */
 kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                 int kv_split_tokens, int* split_tokens, int* max_splits);
 
-/* Bytes of device workspace for these sizes (fp32 partials, (max, sum) pairs,
- * one 32-bit chunk counter per (sequence, head tile[, latent quarter]), and for
- * the tensor-core form two 32-bit work-queue counters); 0 when every sequence
- * fits one chunk and the mma.sync form runs.  The workspace must be zero-filled
- * before its first use; every call leaves the counters at zero again.  Calls
- * sharing a workspace must not overlap in time. */
+/* Bytes of device workspace for these sizes (fp32 partials, (max, sum) pairs and
+ * one 32-bit counter per (sequence, head tile[, latent half])); 0 when no sequence
+ * can be cut into pieces.  The workspace must be zero-filled before its first use;
+ * every call leaves the counters ready for the next.  Calls sharing a workspace
+ * must not overlap in time. */
 kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                    int kv_split_tokens, size_t* bytes);
 

@@ -534,7 +534,7 @@ constexpr int kMlaHeadTile = 16;
 
 struct MlaPlan {
     int head_tiles, split_blocks, max_splits;
-    int tc;                 // tcgen05 form: head tiles of 128, four latent quarters each
+    int tc;                 // tcgen05 form: head tiles of 128, two latent halves each
 };
 
 // The tcgen05 form takes wide head tiles (at least 64 real heads of 128 rows).
@@ -560,19 +560,31 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
     p.tc = use_tc(pl, q_heads) ? 1 : 0;
     const int tile = p.tc ? kvp::MLA_TC_HEADS : kMlaHeadTile;
     p.head_tiles = (q_heads + tile - 1) / tile;
+    if (p.tc) {
+        // the units (latent half, head tile, sequence, block) are cut into one contiguous
+        // range per CTA; split_blocks is the least a range holds (the chunk argument, or
+        // automatically about half the worst-case share of an SM, 4..16 blocks), so a
+        // sequence of max_blocks blocks is cut into at most ceil((max_blocks - 1) /
+        // split_blocks) + 1 pieces, each merged from its own partial
+        if (split_tokens > 0) {
+            p.split_blocks = split_tokens / pl->block_size;
+        } else {
+            const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles * 2 * max_blocks;
+            const long long share = units / (2LL * (pl->num_sms > 0 ? pl->num_sms : 148));
+            p.split_blocks = static_cast<int>(share < 4 ? 4 : (share > 16 ? 16 : share));
+        }
+        if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
+        p.max_splits = (max_blocks - 1 + p.split_blocks - 1) / p.split_blocks + 1;
+        if (p.max_splits > max_blocks) p.max_splits = max_blocks;
+        // the partition's arithmetic: units x CTAs must stay far inside 64 bits
+        const long long units_max = static_cast<long long>(batch) * p.head_tiles * 2 * max_blocks;
+        if (units_max > (1LL << 40)) return KV_ERR_UNSUPPORTED;
+        if (p.max_splits > 65535 || p.head_tiles > 32767 || batch > 65535) return KV_ERR_UNSUPPORTED;
+        *out = p;
+        return KV_OK;
+    }
     if (split_tokens > 0) {
         p.split_blocks = split_tokens / pl->block_size;
-    } else if (p.tc) {
-        // one CTA per SM: about two chunks per SM over the worst case, 2048..4096 tokens
-        // (measured on GB300, 128 heads, contexts in [512, 4096]: 3072-token chunks
-        // 215 us, 2048 234 us, 1024 274 us -- each chunk pays a query load and a merge)
-        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles * 4;
-        const long long work = units * max_blocks * pl->block_size;
-        const long long target = static_cast<long long>(pl->num_sms > 0 ? pl->num_sms : 148) * 2;
-        long long tok = (work + target - 1) / target;
-        if (tok < 2048) tok = 2048;
-        if (tok > 4096) tok = 4096;
-        p.split_blocks = static_cast<int>((tok + pl->block_size - 1) / pl->block_size);
     } else {
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles;
         const long long work = units * max_blocks * pl->block_size;
@@ -584,33 +596,35 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
     }
     if (p.split_blocks > max_blocks) p.split_blocks = max_blocks;
     p.max_splits = (max_blocks + p.split_blocks - 1) / p.split_blocks;
-    if (p.max_splits > 65535 || p.head_tiles * (p.tc ? 4LL : 1LL) > 65535 || batch > 65535)
-        return KV_ERR_UNSUPPORTED;
+    if (p.max_splits > 65535 || p.head_tiles > 65535 || batch > 65535) return KV_ERR_UNSUPPORTED;
     *out = p;
     return KV_OK;
 }
 
-// partial outputs [batch, q_heads, max_splits, 512], (max, sum) pairs, then one
-// ticket per (sequence, head tile).
+// partial outputs [batch, q_heads, max_splits, 512], (max, sum) pairs, then one ticket
+// per (sequence, head tile); the tensor-core form lays its pieces out per (sequence,
+// head tile, latent half, split) instead.
 WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
 {
     WorkspaceLayout w{0, 0, 0, 0, 0};
-    if (p.max_splits > 1) {
+    if (p.max_splits > 1 && p.tc) {
+        // pieces (sequence, head tile, latent half, split): fp32 partials of 128 heads x
+        // 256 latent numbers, (max, sum) per head, then the piece count of each
+        // (sequence, head tile, half) -- read by the merge kernel
+        const size_t pieces = static_cast<size_t>(batch) * p.head_tiles * 2 * p.max_splits;
+        w.part_ml = round_up(pieces * kvp::MLA_TC_HEADS * (kvp::MLA_DV / 2) * sizeof(float), kAlign);
+        w.tickets = w.part_ml + round_up(pieces * kvp::MLA_TC_HEADS * 2 * sizeof(float), kAlign);
+        w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * 2 * sizeof(int);
+        w.total = w.tickets + w.ticket_bytes;
+    } else if (p.max_splits > 1) {
         const size_t n = static_cast<size_t>(batch) * q_heads * p.max_splits;
         w.part_ml = round_up(n * kvp::MLA_DV * sizeof(float), kAlign);
         w.tickets = w.part_ml + round_up(n * 2 * sizeof(float), kAlign);
-        w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * (p.tc ? 4 : 1) * sizeof(int);
-        w.total = w.tickets + w.ticket_bytes;
-    }
-    if (p.tc) {
-        // the persistent form's work counter (next item, CTAs done) follows the tickets
-        w.ticket_bytes = round_up(w.ticket_bytes, 16) + 2 * sizeof(int);
+        w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * sizeof(int);
         w.total = w.tickets + w.ticket_bytes;
     }
     return w;
 }
-
-size_t mla_queue_offset(const WorkspaceLayout& w) { return w.total - 2 * sizeof(int); }
 
 }  // namespace
 
@@ -738,7 +752,6 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.part_o = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
     p.part_ml = wl.total > 0 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
     p.tickets = wl.total > 0 ? reinterpret_cast<int*>(ws + wl.tickets) : nullptr;
-    p.queue = plan.tc ? reinterpret_cast<int*>(ws + mla_queue_offset(wl)) : nullptr;
     p.err = pool->err;
     p.batch = batch;
     p.q_heads = q_heads;
@@ -749,12 +762,13 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
     if (plan.tc) {
-        // persistent: one CTA per SM (at most one per work item) pulling items
-        // (chunk, sequence, head tile, latent quarter) from the workspace counter
-        const long long items = static_cast<long long>(plan.head_tiles) * 4 * batch * plan.max_splits;
-        if (items > std::numeric_limits<int>::max()) return KV_ERR_UNSUPPORTED;
+        // persistent: one CTA per SM, each taking a contiguous range of the units
+        // (latent half, head tile, sequence, block); no more CTAs than ranges of
+        // split_blocks units the longest batch could have
+        const long long units_max = static_cast<long long>(plan.head_tiles) * 2 * batch * max_blocks;
+        const long long ranges = units_max / plan.split_blocks > 0 ? units_max / plan.split_blocks : 1;
         const int sms = pool->num_sms > 0 ? pool->num_sms : 148;
-        const dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
+        const dim3 grid(static_cast<unsigned>(ranges < sms ? ranges : sms));
         return kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream)) ==
                        cudaSuccess
                    ? KV_OK

@@ -4,41 +4,47 @@
 // get full-size keys and values back?": every head scores the shared cached
 // vector -- 512 latent + 64 rotary-key numbers -- and averages its latent part).
 //
+// Work item = (sequence, tile of 128 heads, half of the latent output, split
+// chunk).  The two halves of a chunk run on two CTAs that each compute the full
+// scores and one 256-wide half of the output: the fp32 output of 128 heads x 512
+// latent numbers alone would fill an SM's tensor memory.
+//
 // Persistent: one CTA per SM holds its tensor memory for the whole launch and
-// works through items (sequence, tile of 128 heads, quarter of the latent output,
-// split chunk) taken from a counter in the workspace, first chunks first; the
-// last CTA to finish resets the counter.  320 threads:
+// takes items from a counter in the workspace, first chunks first; the last CTA
+// to finish resets the counter.  320 threads:
 //   * warp 8 takes the next item, skips empty ones (chunks past a sequence's
 //     end), passes the item to the other roles through a 4-slot ring in shared
 //     memory, and streams the item's 64-token blocks, one per stage, with nine
-//     TMA loads (one per 128-byte piece of the 576 numbers, 128-byte swizzle),
-//     so a stage is nine [64 tokens x 64 numbers] K-major tiles: 72 KB, 3 stages.
-//     The loads of the next item start while the current one is computed.
+//     TMA loads (one per 128-byte piece of the 576 numbers, 128-byte swizzle):
+//     a stage is nine K-major [64 tokens x 64 numbers] tiles, 72 KB, 2 stages.
+//     The five pieces only the scores read (the other half's latent numbers and
+//     the rotary key) and the four pieces of this CTA's output half have
+//     barriers of their own: the first five are reloaded as soon as the scores
+//     of their stage are done, the other four once its output update is.
 //   * warp 9 (one thread) issues the MMAs.  Scores S[128 heads x 64 tokens] =
-//     Q . C^T: A = the absorbed queries, kept in tensor memory for the item
-//     (128 lanes x 288 columns), B = the stage (K-major), 36 MMAs of K = 16.
-//     Then O[128 heads x 128 latent] += P . C[:, quarter]: A = the probabilities
-//     in tensor memory, B = the same stage read MN-major (the latent numbers of a
-//     token are contiguous), 4 MMAs.  Completion is signalled by tcgen05.commit on
-//     mbarriers.  The scores of stage i+1 are computed while the softmax of stage
-//     i runs, and the output update of stage i while the softmax of stage i+1 runs.
+//     Q . C^T in 36 MMAs of K = 16: the 20 over the score-only pieces take A =
+//     the queries' matching 320 numbers held in tensor memory, the 16 over the
+//     output pieces (whose loads land last) take A = the other 256 numbers held
+//     in shared memory.  Then O[128 heads x 256 latent] += P . C[:, half]: A =
+//     the probabilities in tensor memory, B = the four output pieces read
+//     MN-major (the latent numbers of a token are contiguous), 4 MMAs of N =
+//     256.  Completion is signalled by tcgen05.commit on mbarriers.  The scores
+//     of stage i+1 are computed while the softmax of stage i runs, and the
+//     output update of stage i while the softmax of stage i+1 runs.
 //   * warps 0-7: head h (tensor-memory lane h) belongs to two threads, one in
-//     warp h / 32 (tokens 0-31 of a stage, output columns 0-63) and one in warp
-//     h / 32 + 4 (tokens 32-63, columns 64-127) -- a warp can only reach its own
-//     quarter of the lanes, and two warps per quarter halve the serial work of
-//     each.  Each reads its 32 scores, the pair exchanges its maxima through
+//     warp h / 32 (tokens 0-31 of a stage, output columns 0-127) and one in warp
+//     h / 32 + 4 (tokens 32-63, columns 128-255) -- a warp can only reach its
+//     own quarter of the lanes, and two warps per quarter halve the serial work
+//     of each.  Each reads its 32 scores, the pair exchanges its maxima through
 //     shared memory, and each writes its 32 probabilities (bf16) back to tensor
-//     memory; at the end of an item each normalises and stores its 64 outputs,
+//     memory; at the end of an item each normalises and stores its 128 outputs,
 //     then loads the next item's queries.  The output is rescaled only when the
 //     running max grows by more than 2^8 (log2 units); until then the older
 //     maximum stays the reference, which is exact because the final division
 //     uses the sum taken against the same reference.
-//   * the four quarter-items of a sequence chunk compute the same scores (the
-//     tensor memory of an SM holds the fp32 output of 128 heads x 128 latent
-//     numbers beside the queries and one score tile, not more) and read the same
-//     stages, which the L2 serves after the first.
-//   * tensor memory: queries [0, 288), scores [288, 352), probabilities
-//     [352, 384), output [384, 512).
+//   * tensor memory: queries [0, 160), scores [160, 224), probabilities
+//     [224, 256), output [256, 512).  Shared memory: 2 stages (144 KB), the
+//     queries' other 256 numbers (64 KB, K-major, 128-byte swizzle), control.
 // Every wait is bounded; a late barrier sets KV_DEVERR_TIMEOUT and every role
 // leaves its loop, waits (bounded) for its copies and MMAs in flight, and the CTA
 // frees its tensor memory before it exits.
@@ -51,46 +57,89 @@ namespace kvp {
 namespace {
 
 constexpr int TC_TOK = 64;                      // tokens per stage (one block)
-constexpr int TC_NSTAGE = 3;
+constexpr int TC_NSTAGE = 2;
 constexpr int TC_PIECE = TC_TOK * 128;          // one 64-number piece of 64 tokens
 constexpr int TC_NPIECE = MLA_DK / 64;          // 9
+constexpr int TC_NEARLY = 5;                    // pieces only the scores read
+constexpr int TC_NLATE = TC_NPIECE - TC_NEARLY; // 4: this CTA's output half
 constexpr int TC_STAGE = TC_NPIECE * TC_PIECE;  // 73,728 bytes
-constexpr int TC_DQ = 128;                      // latent numbers per CTA
+constexpr int TC_DQ = 256;                      // latent numbers per CTA
 constexpr int TC_M = 128;                       // heads per CTA
+constexpr int TC_QPIECE = TC_M * 128;           // one 64-number piece of 128 heads
+constexpr int TC_QS = TC_NLATE * TC_QPIECE;     // queries kept in shared memory
 constexpr int TC_THREADS = 320;                 // warps 0-7 softmax, 8 loads, 9 MMA
-constexpr uint32_t TM_Q = 0, TM_S = 288, TM_P = 352, TM_O = 384, TM_COLS = 512;
+constexpr uint32_t TM_Q = 0, TM_S = 160, TM_P = 224, TM_O = 256, TM_COLS = 512;
 constexpr uint32_t IDESC_S = tc_idesc_bf16(TC_M, TC_TOK, 0, 0);
 constexpr uint32_t IDESC_O = tc_idesc_bf16(TC_M, TC_DQ, 0, 1);
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int TC_CTL = 4096;
-constexpr int TC_SMEM = 1024 + TC_NSTAGE * TC_STAGE + TC_CTL;
+constexpr int TC_SMEM = 1024 + TC_NSTAGE * TC_STAGE + TC_QS + TC_CTL;
 static_assert(TC_SMEM <= 227 * 1024, "one CTA per SM");
-static_assert(TM_O + TC_DQ <= TM_COLS && TM_P + TC_TOK / 2 <= TM_O && TM_S + TC_TOK <= TM_P &&
-                  TM_Q + MLA_DK / 2 <= TM_S,
+static_assert(TM_Q + TC_NEARLY * 32 <= TM_S && TM_S + TC_TOK <= TM_P && TM_P + TC_TOK / 2 <= TM_O &&
+                  TM_O + TC_DQ <= TM_COLS,
               "tensor-memory columns");
+static_assert(TC_NLATE * 64 == TC_DQ, "the output half is the four late pieces");
 
 constexpr int TC_NITEM = 4;                     // ring of work items in shared memory
 
-// A work item as the producer hands it on: n = stages, at least 1 (-1: no more items).
+// Piece of the 576 numbers held by score-only slot j (0..4) / output slot j (0..3)
+// of a stage, for the CTA computing latent half dq.
+__device__ __forceinline__ int early_piece(int dq, int j) { return j < 4 ? 4 * (1 - dq) + j : 8; }
+__device__ __forceinline__ int late_piece(int dq, int j) { return 4 * dq + j; }
+
+// A work item as the producer hands it on: blocks blk0 .. blk0 + n - 1 of sequence b
+// (n >= 1; -1: no more items), piece `split` of the `nsplit` the sequence's units
+// were cut into by the partition.
 struct TcItem {
-    int b, ht, dq, split, n, ctx;
+    int b, ht, dq, split, nsplit, blk0, n, ctx;
 };
 
 struct TcCtl {
-    uint64_t kv_full[TC_NSTAGE];
-    uint64_t kv_empty[TC_NSTAGE];
+    uint64_t kv_full_e[TC_NSTAGE];                  // score-only pieces landed
+    uint64_t kv_full_l[TC_NSTAGE];                  // output pieces landed
+    uint64_t kv_empty_e[TC_NSTAGE];                 // scores of the stage done
+    uint64_t kv_empty_l[TC_NSTAGE];                 // output update of the stage done
     uint64_t s_full, s_free, p_full, p_free, q_ready, mma_done;
     uint64_t item_full[TC_NITEM];
     uint64_t item_empty[TC_NITEM];
     uint32_t tmem_base;
     int stage_blk[TC_NSTAGE];
     int abort_flag;
-    int merge_flag;
     TcItem items[TC_NITEM];
     float xmax[2][2][TC_M];                         // [stage parity][token half][head]
     float xl[2][TC_M];                              // [token half][head]
 };
 static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
+
+// L2 prefetch of `bytes` (a multiple of 16) contiguous bytes of global memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Non-blocking probe of an mbarrier phase (test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// L2 prefetch of one TMA box (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+                 : "memory");
+}
 
 __device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
 
@@ -107,24 +156,39 @@ __device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
     return r != 0;
 }
 
-// The scores of a stage: S = Q . C^T, 36 MMAs of K = 16.  The descriptor of slice
-// ks is the stage's base descriptor plus a constant (16-byte units in the low
-// word), so each issue is one add: a single thread issues every MMA of the CTA
-// and its issue rate, not the tensor pipe, bounds small-N MMAs like these.
-__device__ __forceinline__ void issue_score_mma(uint32_t tbase, uint32_t stage_addr)
+// Scores over the five score-only pieces: 20 MMAs of K = 16 with A = the queries'
+// matching numbers in tensor memory.  The descriptor of slice ks is the stage's
+// base descriptor plus a constant (16-byte units in the low word), so each issue
+// is one add: a single thread issues every MMA of the CTA, and its issue rate, not
+// the tensor pipe, bounds small-N MMAs like these.
+__device__ __forceinline__ void issue_score_early(uint32_t tbase, uint32_t stage_addr)
 {
     const uint64_t d0 = tc_smem_desc(stage_addr, 16, 1024);
 #pragma unroll
-    for (int ks = 0; ks < MLA_DK / 16; ++ks)
-        tc_mma_ts(tbase + TM_S + 0u, tbase + TM_Q + ks * 8,
+    for (int ks = 0; ks < TC_NEARLY * 4; ++ks)
+        tc_mma_ts(tbase + TM_S, tbase + TM_Q + ks * 8,
                   d0 + static_cast<uint64_t>(((ks >> 2) * TC_PIECE + (ks & 3) * 32) >> 4), IDESC_S,
                   ks > 0);
 }
 
-// The output update of stage k: O += P . C[:, quarter] over its 64 tokens.
-__device__ __forceinline__ void issue_output_mma(uint32_t tbase, uint32_t stage_addr, int dq, bool first)
+// Scores over the four output pieces: 16 MMAs with A = the other query numbers,
+// K-major in shared memory.
+__device__ __forceinline__ void issue_score_late(uint32_t tbase, uint32_t stage_addr, uint32_t q_addr)
 {
-    const uint64_t d0 = tc_smem_desc(stage_addr + 2 * dq * TC_PIECE, TC_PIECE, 1024);
+    const uint64_t b0 = tc_smem_desc(stage_addr + TC_NEARLY * TC_PIECE, 16, 1024);
+    const uint64_t a0 = tc_smem_desc(q_addr, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < TC_NLATE * 4; ++ks)
+        tc_mma_ss(tbase + TM_S, a0 + static_cast<uint64_t>(((ks >> 2) * TC_QPIECE + (ks & 3) * 32) >> 4),
+                  b0 + static_cast<uint64_t>(((ks >> 2) * TC_PIECE + (ks & 3) * 32) >> 4), IDESC_S, true);
+}
+
+// The output update of a stage: O += P . C[:, half] over its 64 tokens; the four
+// output pieces are the N = 256 operand read MN-major (64-number atoms one piece
+// apart, 8-token groups 1 KB apart).
+__device__ __forceinline__ void issue_output_mma(uint32_t tbase, uint32_t stage_addr, bool first)
+{
+    const uint64_t d0 = tc_smem_desc(stage_addr + TC_NEARLY * TC_PIECE, TC_PIECE, 1024);
 #pragma unroll
     for (int kk = 0; kk < TC_TOK / 16; ++kk)
         tc_mma_ts(tbase + TM_O, tbase + TM_P + kk * 8, d0 + static_cast<uint64_t>((kk * 2048) >> 4),
@@ -139,7 +203,8 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    TcCtl* ctl = reinterpret_cast<TcCtl*>(smem + TC_NSTAGE * TC_STAGE);
+    uint8_t* qsm = smem + TC_NSTAGE * TC_STAGE;
+    TcCtl* ctl = reinterpret_cast<TcCtl*>(qsm + TC_QS);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -148,8 +213,10 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 
     if (tid == 0) {
         for (int i = 0; i < TC_NSTAGE; ++i) {
-            mbar_init(smem_u32(&ctl->kv_full[i]), 1);
-            mbar_init(smem_u32(&ctl->kv_empty[i]), 1);
+            mbar_init(smem_u32(&ctl->kv_full_e[i]), 1);
+            mbar_init(smem_u32(&ctl->kv_full_l[i]), 1);
+            mbar_init(smem_u32(&ctl->kv_empty_e[i]), 1);
+            mbar_init(smem_u32(&ctl->kv_empty_l[i]), 1);
         }
         for (int i = 0; i < TC_NITEM; ++i) {
             mbar_init(smem_u32(&ctl->item_full[i]), 1);
@@ -172,51 +239,168 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
     const uint32_t tbase = ctl->tmem_base;
 
     if (warp == 8) {
-        // ------------------------------------------------------------ items and loads
+        // ------------------------------------------------------------ partition, items, loads
+        // Units: (half dq, head tile ht, sequence b, block) in that order, T in all;
+        // CTA c takes the contiguous range [c T / G, (c + 1) T / G) with G active
+        // CTAs chosen so that a range holds at least split_blocks units.  Every CTA
+        // derives the same partition from the context lengths.
+        const int cap = p.max_blocks * TC_TOK;
+        long long S = 0;                            // blocks of the batch
+        for (int b0 = 0; b0 < p.batch; b0 += 256) {
+            int raw[8];                             // eight lengths per lane in flight
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int b = b0 + i * 32 + lane;
+                raw[i] = b < p.batch ? __ldg(p.ctx + b) : 0;
+            }
+            int nbs = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int b = b0 + i * 32 + lane;
+                int ctx = raw[i];
+                if (b < p.batch && (ctx < 0 || ctx > cap)) {
+                    if (blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
+                    ctx = ctx < 0 ? 0 : cap;
+                }
+                const int nb = (ctx + TC_TOK - 1) / TC_TOK;
+                nbs += nb;
+                if (b < p.batch && nb == 0 && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+                    // an empty sequence has no units: its output is 0 and its LSE -inf,
+                    // written by CTA b mod G
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(b) * p.q_heads * MLA_DV);
+                    for (int v = 0; v < p.q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (p.lse != nullptr)
+                        for (int hh = 0; hh < p.q_heads; ++hh) p.lse[static_cast<size_t>(b) * p.q_heads + hh] = -INFINITY;
+                }
+            }
+            long long sum = nbs;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL_MASK, sum, o);
+            S += sum;
+        }
+        const int nouter = p.head_tiles * 2;
+        const long long T = S * nouter;
+        long long gact = T / p.split_blocks;
+        if (gact < 1) gact = 1;
+        if (gact > gridDim.x) gact = gridDim.x;
+        const long long c = blockIdx.x;
+        const long long u0 = c < gact ? c * T / gact : T;
+        const long long u1 = c < gact ? (c + 1) * T / gact : T;
+        // the sequence holding a unit: prefix sums of the block counts, 32 at a time
+        // (all lanes; u < T)
+        auto locate = [&](long long u, int& b_at, long long& pre_at) {
+            const long long v = u % S;
+            long long pre = 0;
+            b_at = 0;
+            pre_at = 0;
+            for (int b0 = 0; b0 < p.batch; b0 += 32) {
+                const int b = b0 + lane;
+                int nb = 0;
+                if (b < p.batch) {
+                    int ctx = __ldg(p.ctx + b);
+                    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+                    nb = (ctx + TC_TOK - 1) / TC_TOK;
+                }
+                int incl = nb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(FULL_MASK, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const unsigned past = __ballot_sync(FULL_MASK, pre + incl > v);
+                if (past != 0u) {
+                    const int fl = __ffs(past) - 1;
+                    b_at = b0 + fl;
+                    pre_at = pre + __shfl_sync(FULL_MASK, incl, fl) - __shfl_sync(FULL_MASK, nb, fl);
+                    return;
+                }
+                pre += __shfl_sync(FULL_MASK, incl, 31);
+            }
+        };
+        int b_first = 0, b_last = 0;
+        long long pre_first = 0, pre_last = 0;
+        if (u0 < u1) {
+            locate(u0, b_first, pre_first);
+            locate(u1 - 1, b_last, pre_last);
+        }
         if (lane == 0) {
             prefetch_tensormap(&tmp);
-            const int per_chunk = p.batch * p.head_tiles * 4;
-            const int total = per_chunk * p.max_splits;
+            // the CTA whose range holds unit x
+            auto cta_of = [&](long long x) { return static_cast<int>(((x + 1) * gact - 1) / T); };
+            // the item for blocks blk .. blk + n - 1 of the sequence whose units start at ub
+            auto make_item = [&](int outer, int b, long long ub, int blk, int n, int ctx, int nb) {
+                TcItem it;
+                const int cf = cta_of(ub);
+                it.b = b;
+                it.dq = outer / p.head_tiles;
+                it.ht = outer - it.dq * p.head_tiles;
+                it.split = static_cast<int>(c) - cf;
+                it.nsplit = cta_of(ub + nb - 1) - cf + 1;
+                it.blk0 = blk;
+                it.n = n;
+                it.ctx = ctx;
+                return it;
+            };
+            auto seq_ctx = [&](int b) {
+                const int ctx = __ldg(p.ctx + b);
+                return ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+            };
             int k = 0;                              // items handed on
             int g = 0;                              // stages issued (all items)
+            int ge = 0, gl = 0;                     // stages with score-only / output loads issued
             bool ok = true;
+            // Order: the range's last segment first, then the rest from the start.  A
+            // sequence cut between CTA c and c + 1 is then worked on first by both, and
+            // its merge (by the second to finish) overlaps their other work.
+            long long ls = u1;                      // start of the last segment
+            int outer_l = 0, ctx_l = 0, nb_l = 0;
+            long long ub_l = 0;
+            if (u0 < u1) {
+                outer_l = static_cast<int>((u1 - 1) / S);
+                ub_l = static_cast<long long>(outer_l) * S + pre_last;
+                ls = ub_l > u0 ? ub_l : u0;
+                ctx_l = seq_ctx(b_last);
+                nb_l = (ctx_l + TC_TOK - 1) / TC_TOK;
+            }
+            bool last_done = !(u0 < u1);
+            long long u = u0;
+            int outer = u0 < u1 ? static_cast<int>(u0 / S) : 0;
+            int b = b_first;
+            long long pre = pre_first;
+            int blk = u0 < u1 ? static_cast<int>(u0 % S - pre_first) : 0;
             for (;;) {
-                const int item = atomicAdd(p.queue, 1);
-                const bool last = item >= total || *abort_flag;
                 TcItem it{};
-                if (!last) {
-                    it.split = item / per_chunk;
-                    const int rem = item - it.split * per_chunk;
-                    it.b = rem / (p.head_tiles * 4);
-                    const int x = rem - it.b * (p.head_tiles * 4);
-                    it.ht = x >> 2;
-                    it.dq = x & 3;
-                    int ctx = __ldg(p.ctx + it.b);
-                    const int cap = p.max_blocks * TC_TOK;
-                    if (ctx < 0 || ctx > cap) {
-                        if (it.split == 0 && x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
-                        ctx = ctx < 0 ? 0 : cap;
-                    }
-                    it.ctx = ctx;
-                    const int nblk = (ctx + TC_TOK - 1) / TC_TOK;
-                    const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
-                    if (it.split >= nsplit) continue;       // past the sequence's end: skip
-                    it.n = max(0, min(nblk - it.split * p.split_blocks, p.split_blocks));
-                    if (it.n == 0) {
-                        // an empty sequence: its output quarter is 0 (and its LSE -inf),
-                        // written here, so every item handed on has stages -- the softmax
-                        // warps then never run more than one item ahead of the MMA thread
-                        const int nh = min(TC_M, p.q_heads - it.ht * TC_M);
-                        const size_t row0 = static_cast<size_t>(it.b) * p.q_heads + it.ht * TC_M;
-                        for (int hh = 0; hh < nh; ++hh) {
-                            uint4* dst = reinterpret_cast<uint4*>(p.out + (row0 + hh) * MLA_DV + it.dq * TC_DQ);
-                            for (int v = 0; v < TC_DQ / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
-                            if (p.lse != nullptr && it.dq == 0) p.lse[row0 + hh] = -INFINITY;
+                it.n = -1;
+                if (!last_done) {
+                    last_done = true;
+                    it = make_item(outer_l, b_last, ub_l, static_cast<int>(ls - ub_l), static_cast<int>(u1 - ls),
+                                   ctx_l, nb_l);
+                }
+                while (it.n < 0 && u < ls && !*abort_flag) {
+                    const int ctx = seq_ctx(b);
+                    const int nb = (ctx + TC_TOK - 1) / TC_TOK;
+                    if (blk >= nb) {                // next sequence (or next head tile / half)
+                        pre += nb;
+                        blk = 0;
+                        if (++b == p.batch) {
+                            b = 0;
+                            pre = 0;
+                            ++outer;
                         }
                         continue;
                     }
-                } else {
-                    it.n = -1;
+                    const int n = static_cast<int>(nb - blk < ls - u ? nb - blk : ls - u);
+                    it = make_item(outer, b, static_cast<long long>(outer) * S + pre, blk, n, ctx, nb);
+                    u += n;
+                    blk += n;
+                }
+                const bool last = it.n < 0;
+                if (!last) {
+                    // the item's queries (rows of its head tile, contiguous) into L2: the
+                    // softmax warps load them when the previous item is done
+                    const size_t qrow0 = static_cast<size_t>(it.b) * p.q_heads + it.ht * TC_M;
+                    const int nhq = min(TC_M, p.q_heads - it.ht * TC_M);
+                    prefetch_l2_bulk(p.q + qrow0 * MLA_DK, static_cast<uint32_t>(nhq) * MLA_DK * 2);
                 }
                 const int slot = k % TC_NITEM;
                 if (!mbar_wait_bounded(smem_u32(&ctl->item_empty[slot]),
@@ -228,33 +412,53 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 mbar_arrive(smem_u32(&ctl->item_full[slot]));
                 ++k;
                 if (last) break;
-                const int32_t* trow = p.tables + static_cast<size_t>(it.b) * p.max_blocks +
-                                      it.split * p.split_blocks;
-                int next_blk = it.n > 0 ? __ldg(trow) : -1;   // block id read one stage ahead
+                const int32_t* trow = p.tables + static_cast<size_t>(it.b) * p.max_blocks + it.blk0;
+                int next_blk = __ldg(trow);         // block id read one stage ahead
                 for (int s = 0; s < it.n; ++s, ++g) {
                     const int st = g % TC_NSTAGE;
-                    int blk = next_blk;
+                    const uint32_t ph = (static_cast<uint32_t>(g / TC_NSTAGE) & 1u) ^ 1u;
+                    int bid = next_blk;
                     if (s + 1 < it.n) next_blk = __ldg(trow + s + 1);
-                    if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty[st]),
-                                           (static_cast<uint32_t>(g / TC_NSTAGE) & 1u) ^ 1u) ||
-                        *abort_flag) {
+                    if (bid < 0 || bid >= p.num_blocks) {
+                        atomicOr(p.err, KV_DEVERR_BLOCK_ID);
+                        bid = -1;
+                    }
+                    const uint32_t dst = smem_u32(smem + st * TC_STAGE);
+                    // score-only pieces: free once the scores of the stage two back are done
+                    if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty_e[st]), ph) || *abort_flag) {
                         ok = false;
                         break;
                     }
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        atomicOr(p.err, KV_DEVERR_BLOCK_ID);
-                        blk = -1;
-                    }
-                    ctl->stage_blk[st] = blk;
-                    const uint32_t fb = smem_u32(&ctl->kv_full[st]);
-                    if (blk >= 0) {
-                        mbar_arrive_expect_tx(fb, TC_STAGE);
-                        const uint32_t dst = smem_u32(smem + st * TC_STAGE);
-                        for (int pc = 0; pc < TC_NPIECE; ++pc)
-                            tma_load_5d(dst + pc * TC_PIECE, &tmp, 0, pc, 0, 0, blk, fb);
+                    const uint32_t fe = smem_u32(&ctl->kv_full_e[st]);
+                    if (bid >= 0) {
+                        mbar_arrive_expect_tx(fe, TC_NEARLY * TC_PIECE);
+                        for (int j = 0; j < TC_NEARLY; ++j)
+                            tma_load_5d(dst + j * TC_PIECE, &tmp, 0, early_piece(it.dq, j), 0, 0, bid, fe);
+                        // the output pieces load later (when their slot frees): bring them
+                        // into L2 now so that load is short
+                        for (int j = 0; j < TC_NLATE; ++j)
+                            tma_prefetch_l2_5d(&tmp, 0, late_piece(it.dq, j), 0, 0, bid);
                     } else {
-                        mbar_arrive(fb);
+                        mbar_arrive(fe);
                     }
+                    ge = g + 1;
+                    // output pieces: free once that stage's output update is done (its
+                    // softmax, which reads stage_blk, is then over too)
+                    if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty_l[st]), ph) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    ctl->stage_blk[st] = bid;
+                    const uint32_t fl = smem_u32(&ctl->kv_full_l[st]);
+                    if (bid >= 0) {
+                        mbar_arrive_expect_tx(fl, TC_NLATE * TC_PIECE);
+                        for (int j = 0; j < TC_NLATE; ++j)
+                            tma_load_5d(dst + (TC_NEARLY + j) * TC_PIECE, &tmp, 0, late_piece(it.dq, j), 0,
+                                        0, bid, fl);
+                    } else {
+                        mbar_arrive(fl);
+                    }
+                    gl = g + 1;
                 }
                 if (!ok) break;
             }
@@ -263,8 +467,12 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 ctl->abort_flag = 1;
             }
             // copies still in flight must land before the CTA moves on
-            for (int j = max(0, g - TC_NSTAGE); j < g; ++j)
-                if (!mbar_wait_bounded(smem_u32(&ctl->kv_full[j % TC_NSTAGE]),
+            for (int j = max(0, ge - TC_NSTAGE); j < ge; ++j)
+                if (!mbar_wait_bounded(smem_u32(&ctl->kv_full_e[j % TC_NSTAGE]),
+                                       static_cast<uint32_t>(j / TC_NSTAGE) & 1u))
+                    break;
+            for (int j = max(0, gl - TC_NSTAGE); j < gl; ++j)
+                if (!mbar_wait_bounded(smem_u32(&ctl->kv_full_l[j % TC_NSTAGE]),
                                        static_cast<uint32_t>(j / TC_NSTAGE) & 1u))
                     break;
         }
@@ -272,6 +480,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
+            const uint32_t q_addr = smem_u32(qsm);
             bool ok = true;
             int g = 0;                              // stages processed (all items)
             for (int k = 0; ok; ++k) {
@@ -280,15 +489,15 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                                        static_cast<uint32_t>(k / TC_NITEM) & 1u);
                 if (!ok) break;
                 const int n = ctl->items[slot].n;
-                const int dq = ctl->items[slot].dq;
                 mbar_arrive(smem_u32(&ctl->item_empty[slot]));
                 if (n < 0) break;
                 ok = mbar_wait_bounded(smem_u32(&ctl->q_ready), static_cast<uint32_t>(k) & 1u);
                 for (int s = 0; ok && s < n; ++s) {
                     const int gs = g + s;
                     const int st = gs % TC_NSTAGE;
-                    ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]),
-                                           static_cast<uint32_t>(gs / TC_NSTAGE) & 1u);
+                    const uint32_t ph = static_cast<uint32_t>(gs / TC_NSTAGE) & 1u;
+                    const uint32_t stage_addr = smem_u32(smem + st * TC_STAGE);
+                    ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_e[st]), ph);
                     if (ok && gs >= 1)
                         ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(gs - 1) & 1u);
                     if (!ok || *abort_flag) {
@@ -296,15 +505,31 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         break;
                     }
                     tc_fence_after();
-                    issue_score_mma(tbase, smem_u32(smem + st * TC_STAGE));
-                    tc_commit(smem_u32(&ctl->s_full));
-                    if (s >= 1) {
-                        ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_output_mma(tbase, smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), dq, s == 1);
-                        tc_commit(smem_u32(&ctl->p_free));
-                        tc_commit(smem_u32(&ctl->kv_empty[(gs - 1) % TC_NSTAGE]));
+                    issue_score_early(tbase, stage_addr);
+                    // then, in whichever order their inputs are ready: the previous stage's
+                    // output update (its probabilities) and the scores over the output
+                    // pieces (their loads, issued once that previous update had finished
+                    // with the slot two stages back)
+                    bool o_todo = s >= 1, l_todo = true;
+                    const unsigned long long t0 = global_timer_ns();
+                    for (uint32_t spin = 0; ok && (o_todo || l_todo); ++spin) {
+                        if (o_todo && mbar_test(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u)) {
+                            tc_fence_after();
+                            issue_output_mma(tbase, smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), s == 1);
+                            tc_commit(smem_u32(&ctl->p_free));
+                            tc_commit(smem_u32(&ctl->kv_empty_l[(gs - 1) % TC_NSTAGE]));
+                            o_todo = false;
+                            continue;
+                        }
+                        if (l_todo && mbar_test(smem_u32(&ctl->kv_full_l[st]), ph)) {
+                            tc_fence_after();
+                            issue_score_late(tbase, stage_addr, q_addr);
+                            tc_commit(smem_u32(&ctl->s_full));
+                            tc_commit(smem_u32(&ctl->kv_empty_e[st]));
+                            l_todo = false;
+                            continue;
+                        }
+                        if ((spin & 63u) == 63u && global_timer_ns() - t0 > WAIT_LIMIT_NS) ok = false;
                     }
                 }
                 if (ok && n >= 1) {
@@ -313,9 +538,9 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gl) & 1u);
                     if (ok) {
                         tc_fence_after();
-                        issue_output_mma(tbase, smem_u32(smem + (gl % TC_NSTAGE) * TC_STAGE), dq, n == 1);
+                        issue_output_mma(tbase, smem_u32(smem + (gl % TC_NSTAGE) * TC_STAGE), n == 1);
                         tc_commit(smem_u32(&ctl->p_free));
-                        tc_commit(smem_u32(&ctl->kv_empty[gl % TC_NSTAGE]));
+                        tc_commit(smem_u32(&ctl->kv_empty_l[gl % TC_NSTAGE]));
                     }
                 }
                 g += n;
@@ -350,30 +575,78 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 break;
             }
             const int b = item.b, dq = item.dq, split = item.split, n = item.n, ctx = item.ctx;
-            const int ht = item.ht;
-            const int blk0 = split * p.split_blocks;
-            const int nblk = (ctx + TC_TOK - 1) / TC_TOK;
-            const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
+            const int ht = item.ht, blk0 = item.blk0, nsplit = item.nsplit;
             const int nh = min(TC_M, p.q_heads - ht * TC_M);
             const size_t row0 = static_cast<size_t>(b) * p.q_heads + ht * TC_M;
             {
-                // queries -> tensor memory (the previous item's score MMAs are complete:
-                // this thread waited for its last scores)
-                const uint4* qg = reinterpret_cast<const uint4*>(p.q + (row0 + (h < nh ? h : 0)) * MLA_DK);
-#pragma unroll 1
-                for (int c9 = half * 5; c9 < (half ? TC_NPIECE : 5); ++c9) {
+                // queries (the previous item's score MMAs are complete: this thread
+                // waited for its last scores).  The 128 rows of the tile are contiguous;
+                // they are copied piece by piece into the queries' shared memory with
+                // coalesced 16-byte asynchronous copies (consecutive threads: the eight
+                // 16-byte chunks of a row, then the next rows; K-major with the 128-byte
+                // swizzle, chunk c of row r at (c ^ (r & 7))), in three rounds: the four
+                // score-only latent pieces and then the rotary piece go on to tensor
+                // memory (each thread moving its head's row), the four pieces of this
+                // CTA's output half stay in shared memory for the MMAs.
+                const uint32_t qs = smem_u32(qsm);
+                const uint16_t* qtile = p.q + row0 * MLA_DK;
+                auto copy_pieces = [&](int npc, int first_slot, bool late) {
+                    for (int idx = st_id; idx < npc * TC_M * 8; idx += 256) {
+                        const int j = idx >> 10, r = (idx >> 3) & (TC_M - 1), cc = idx & 7;
+                        const int pc = late ? late_piece(dq, j) : early_piece(dq, first_slot + j);
+                        const uint32_t dst = qs + j * TC_QPIECE + r * 128 + ((cc ^ (r & 7)) << 4);
+                        if (r < nh)
+                            cp_async16(dst, qtile + static_cast<size_t>(r) * MLA_DK + pc * 64 + cc * 8);
+                        else
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+                    }
+                    cp_async_wait_all();
+                    named_barrier_sync(1, 256);
+                };
+                auto row_chunk = [&](int j, int cc) {
+                    uint4 v;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(qs + j * TC_QPIECE + h * 128 + ((cc ^ (h & 7)) << 4)));
+                    return v;
+                };
+                // round 1: score-only latent pieces -> tensor-memory slots 0-3 (2 per half)
+                copy_pieces(4, 0, false);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = half * 2 + jj;
                     uint32_t r[32];
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 x = h < nh ? __ldg(qg + c9 * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
-                        r[4 * v] = x.x;
-                        r[4 * v + 1] = x.y;
-                        r[4 * v + 2] = x.z;
-                        r[4 * v + 3] = x.w;
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = row_chunk(j, cc);
+                        r[4 * cc] = v.x;
+                        r[4 * cc + 1] = v.y;
+                        r[4 * cc + 2] = v.z;
+                        r[4 * cc + 3] = v.w;
                     }
-                    tc_st32(lrow + TM_Q + c9 * 32, r);
+                    tc_st32(lrow + TM_Q + j * 32, r);
                 }
                 tc_wait_st();
+                named_barrier_sync(1, 256);
+                // round 2: the rotary piece -> tensor-memory slot 4 (16 columns per half)
+                copy_pieces(1, 4, false);
+                {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 v = row_chunk(0, half * 4 + cc);
+                        r[4 * cc] = v.x;
+                        r[4 * cc + 1] = v.y;
+                        r[4 * cc + 2] = v.z;
+                        r[4 * cc + 3] = v.w;
+                    }
+                    tc_st16(lrow + TM_Q + 4 * 32 + half * 16, r);
+                }
+                tc_wait_st();
+                named_barrier_sync(1, 256);
+                // round 3: this half's pieces, kept in shared memory for the MMAs
+                copy_pieces(4, 0, true);
+                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ctl->q_ready));
@@ -382,7 +655,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             for (int s = 0; s < n; ++s) {
                 const int gs = g + s;
                 const int st = gs % TC_NSTAGE;
-                ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(gs / TC_NSTAGE) & 1u);
+                ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_l[st]), static_cast<uint32_t>(gs / TC_NSTAGE) & 1u);
                 if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->s_full), static_cast<uint32_t>(gs) & 1u);
                 ok = all_ok(ok);
                 if (!ok) failed = true;
@@ -439,9 +712,9 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c2 = 0; c2 < 2; ++c2) {
+                    for (int c2 = 0; c2 < 4; ++c2) {
                         uint32_t r[32];
-                        const uint32_t col = TM_O + half * 64 + c2 * 32;
+                        const uint32_t col = TM_O + half * 128 + c2 * 32;
                         tc_ld32(lrow + col, r);
                         tc_wait_ld();
 #pragma unroll
@@ -463,12 +736,13 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 l += ls;
                 if (nvalid_all < TC_TOK) {
                     // values of tokens past the cache (or of a skipped block) are zeroed so
-                    // that 0 * NaN cannot reach the output sums
-                    uint8_t* sp = smem + st * TC_STAGE + 2 * dq * TC_PIECE;
+                    // that 0 * NaN cannot reach the output sums (the scores of the stage,
+                    // which read these rows too, are complete)
+                    uint8_t* sp = smem + st * TC_STAGE + TC_NEARLY * TC_PIECE;
                     const int v0 = max(0, nvalid_all);
-                    for (int i = st_id; i < (TC_TOK - v0) * 16; i += 256) {
-                        const int row = v0 + (i >> 4);
-                        const int pc = (i >> 3) & 1;
+                    for (int i = st_id; i < (TC_TOK - v0) * 32; i += 256) {
+                        const int row = v0 + (i >> 5);
+                        const int pc = (i >> 3) & 3;
                         const int ch = i & 7;
                         *reinterpret_cast<uint4*>(sp + pc * TC_PIECE + row * 128 + (ch << 4)) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -505,102 +779,76 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             }
             l = ctl->xl[0][h] + ctl->xl[1][h];
 
-            // ---- epilogue: this thread's head, latent numbers 128 dq + 64 half .. + 63
-            const size_t bh = row0 + h;
+            // ---- epilogue: this thread's head, latent numbers 256 dq + 128 half .. + 127,
+            // in four chunks of 32.  A whole sequence's output goes through shared memory
+            // (the queries' shared-memory part, idle until the next item's queries are
+            // loaded by these threads) so that the global writes are whole rows: 32 heads
+            // x 32 numbers per warp, row r = head 32 (warp % 4) + r, 16-byte chunk j of a
+            // row at (j ^ (r & 7)).  A piece of a cut sequence leaves its partial for
+            // paged_mla_merge_tc, and every item records its sequence's piece count.
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool write = h < nh;
             const bool whole = nsplit == 1;
+            // piece index of a cut sequence's partial: (sequence, head tile, half, split)
+            const size_t piece = ((static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq) * p.max_splits + split;
+            if (!whole && h < nh && half == 0)
+                reinterpret_cast<float2*>(p.part_ml)[piece * TC_M + h] = make_float2(m_ref, l);
+            const uint32_t tile = smem_u32(qsm) + warp * 4096;
+            const int hq = (warp & 3) * 32;         // first head of this warp's rows
 #pragma unroll 1
-            for (int c2 = 0; c2 < 2; ++c2) {
+            for (int c2 = 0; c2 < 4; ++c2) {
                 uint32_t r[32];
                 if (n >= 1) {
-                    tc_ld32(lrow + TM_O + half * 64 + c2 * 32, r);
+                    tc_ld32(lrow + TM_O + half * 128 + c2 * 32, r);
                     tc_wait_ld();
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = 0u;
                 }
-                if (!write) continue;
-                const int d0 = dq * TC_DQ + half * 64 + c2 * 32;
-                if (whole) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0);
+                if (!whole) {
+                    // a piece of a cut sequence: its normalised partial in the piece layout
+                    // [32-number chunk][float4 slot][head], coalesced as written (thread =
+                    // head); its (max, sum) beside it
+                    float4* dst = reinterpret_cast<float4*>(p.part_o) + piece * (TC_M * TC_DQ / 4) +
+                                  static_cast<size_t>((half * 4 + c2) * 8) * TC_M + h;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(r[8 * v]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(p.part_o + (bh * p.max_splits + split) * MLA_DV + d0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                    for (int j = 0; j < 8; ++j)
+                        dst[j * TC_M] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                                    __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+                    continue;
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(tile + lane * 128 + ((j ^ (lane & 7)) << 4)),
+                                 "f"(__uint_as_float(r[4 * j]) * inv), "f"(__uint_as_float(r[4 * j + 1]) * inv),
+                                 "f"(__uint_as_float(r[4 * j + 2]) * inv), "f"(__uint_as_float(r[4 * j + 3]) * inv)
+                                 : "memory");
+                __syncwarp();
+                const int d0 = dq * TC_DQ + half * 128 + c2 * 32;
+                {
+                    // bf16 rows of 64 bytes: lane -> row it * 8 + lane / 4, numbers 8 (lane % 4) ..
+#pragma unroll
+                    for (int it = 0; it < 4; ++it) {
+                        const int rr = it * 8 + (lane >> 2), qd = lane & 3;
+                        float4 a, bq;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w)
+                                     : "r"(tile + rr * 128 + (((2 * qd) ^ (rr & 7)) << 4)));
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(bq.x), "=f"(bq.y), "=f"(bq.z), "=f"(bq.w)
+                                     : "r"(tile + rr * 128 + (((2 * qd + 1) ^ (rr & 7)) << 4)));
+                        if (hq + rr < nh)
+                            *reinterpret_cast<uint4*>(p.out + (row0 + hq + rr) * MLA_DV + d0 + qd * 8) =
+                                make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(bq.x, bq.y),
+                                           pack_bf16x2(bq.z, bq.w));
+                    }
+                }
+                __syncwarp();
             }
             tc_fence_before();
-            if (write && half == 0) {
-                if (whole) {
-                    if (p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(m_ref, l);
-                } else {
-                    // every quarter writes the same (max, sum); the merge of a quarter reads
-                    // the pairs its own siblings wrote before counting themselves
-                    p.part_ml[(bh * p.max_splits + split) * 2 + 0] = m_ref;
-                    p.part_ml[(bh * p.max_splits + split) * 2 + 1] = l;
-                }
-            }
-            if (!whole) {
-                __threadfence();
-                named_barrier_sync(1, 256);
-                int* ticket = p.tickets + (static_cast<size_t>(b) * p.head_tiles + ht) * 4 + dq;
-                if (st_id == 0) {
-                    const int last = atomicAdd(ticket, 1) == nsplit - 1;
-                    if (last) __threadfence();
-                    ctl->merge_flag = last;
-                }
-                named_barrier_sync(1, 256);
-                const bool merge = ctl->merge_flag != 0;
-                if (merge && h < nh) {
-                    const float* ml = p.part_ml + bh * p.max_splits * 2;
-                    float M = -INFINITY;
-                    for (int j = 0; j < nsplit; ++j)
-                        if (__ldcg(ml + 2 * j + 1) > 0.f) M = fmaxf(M, __ldcg(ml + 2 * j));
-                    float W = 0.f;
-                    for (int j = 0; j < nsplit; ++j) {
-                        const float lj = __ldcg(ml + 2 * j + 1);
-                        if (lj > 0.f) W += lj * fast_exp2(__ldcg(ml + 2 * j) - M);
-                    }
-                    const float winv = W > 0.f ? 1.f / W : 0.f;
-#pragma unroll 1
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const int d0 = dq * TC_DQ + half * 64 + c8 * 8;
-                        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        for (int j = 0; j < nsplit; ++j) {
-                            const float lj = __ldcg(ml + 2 * j + 1);
-                            if (!(lj > 0.f)) continue;
-                            const float wj = lj * fast_exp2(__ldcg(ml + 2 * j) - M);
-                            const float4* src = reinterpret_cast<const float4*>(
-                                p.part_o + (bh * p.max_splits + j) * MLA_DV + d0);
-                            const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
-                            acc[0] += wj * a0.x;
-                            acc[1] += wj * a0.y;
-                            acc[2] += wj * a0.z;
-                            acc[3] += wj * a0.w;
-                            acc[4] += wj * a1.x;
-                            acc[5] += wj * a1.y;
-                            acc[6] += wj * a1.z;
-                            acc[7] += wj * a1.w;
-                        }
-                        *reinterpret_cast<uint4*>(p.out + bh * MLA_DV + d0) =
-                            make_uint4(pack_bf16x2(acc[0] * winv, acc[1] * winv), pack_bf16x2(acc[2] * winv, acc[3] * winv),
-                                       pack_bf16x2(acc[4] * winv, acc[5] * winv), pack_bf16x2(acc[6] * winv, acc[7] * winv));
-                    }
-                    if (p.lse != nullptr && dq == 0 && half == 0) p.lse[bh] = lse_from(M, W);
-                }
-                if (merge && st_id == 0) *ticket = 0;
-                named_barrier_sync(1, 256);         // merge_flag is reused by the next item
-            }
+            const size_t bh = row0 + h;
+            if (h < nh && half == 0 && whole && p.lse != nullptr && dq == 0) p.lse[bh] = lse_from(m_ref, l);
+            if (st_id == 0 && p.tickets != nullptr)
+                p.tickets[(static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq] = nsplit;
             g += n;
         }
         if (failed && lane == 0) {
@@ -617,15 +865,74 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         tc_fence_after();
         tc_dealloc(tbase, TM_COLS);
     }
-    if (tid == 0) {
-        // the last CTA to finish resets the work counter for the next call
-        __threadfence();
-        if (atomicAdd(p.queue + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-            p.queue[0] = 0;
-            p.queue[1] = 0;
-            __threadfence();
+}
+
+// Merge of the pieces of every cut sequence: CTA (chunk of 32 latent numbers, head
+// tile and half, sequence), thread = head.  The pieces' (max, sum) pairs give the
+// weights w_j = l_j 2^(m_j - M) of the standard log-sum-exp merge; the output row is
+// sum_j w_j o_j / sum_j w_j, staged through shared memory for whole-row writes.
+__global__ void __launch_bounds__(TC_M)
+paged_mla_merge_tc(const MlaParams p)
+{
+    __shared__ uint32_t tile[TC_M][17];             // bf16 pairs, padded rows
+    grid_dependency_wait();
+    const int cg = blockIdx.x;                      // 32-number chunk of the half
+    const int ht = blockIdx.y >> 1, dq = blockIdx.y & 1;
+    const int b = blockIdx.z;
+    const int h = threadIdx.x;
+    const int ctx = __ldg(p.ctx + b);
+    // an empty sequence (or a negative length, read as empty) has no pieces
+    const int nsplit = ctx > 0 ? __ldcg(p.tickets + (static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq) : 1;
+    if (nsplit > 1) {
+        const int nh = min(TC_M, p.q_heads - ht * TC_M);
+        const size_t piece0 = ((static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq) * p.max_splits;
+        const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + piece0 * TC_M + h;
+        float M = -INFINITY, W = 0.f;
+        for (int j = 0; j < nsplit; ++j) {
+            const float2 mj = __ldcg(ml + static_cast<size_t>(j) * TC_M);
+            if (mj.y > 0.f) {
+                const float m2 = fmaxf(M, mj.x);
+                W = W * fast_exp2(M - m2) + mj.y * fast_exp2(mj.x - m2);
+                M = m2;
+            }
+        }
+        float acc[32];
+#pragma unroll
+        for (int v = 0; v < 32; ++v) acc[v] = 0.f;
+        const float4* po = reinterpret_cast<const float4*>(p.part_o) + piece0 * (TC_M * TC_DQ / 4) +
+                           static_cast<size_t>(cg * 8) * TC_M + h;
+        for (int j = 0; j < nsplit; ++j) {
+            const float2 mj = __ldcg(ml + static_cast<size_t>(j) * TC_M);
+            const float wj = mj.y > 0.f ? mj.y * fast_exp2(mj.x - M) : 0.f;
+            const float4* src = po + static_cast<size_t>(j) * (TC_M * TC_DQ / 4);
+            float4 x[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) x[v] = __ldcg(src + v * TC_M);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                acc[4 * v] += wj * x[v].x;
+                acc[4 * v + 1] += wj * x[v].y;
+                acc[4 * v + 2] += wj * x[v].z;
+                acc[4 * v + 3] += wj * x[v].w;
+            }
+        }
+        const float winv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) tile[h][v] = pack_bf16x2(acc[2 * v] * winv, acc[2 * v + 1] * winv);
+        if (p.lse != nullptr && dq == 0 && cg == 0 && h < nh)
+            p.lse[static_cast<size_t>(b) * p.q_heads + ht * TC_M + h] = lse_from(M, W);
+        __syncthreads();
+        // rows of 64 bytes: thread -> row it * 32 + h / 4, 16 bytes (h % 4)
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int rr = it * 32 + (h >> 2), qd = h & 3;
+            if (rr < nh)
+                *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(b) * p.q_heads + ht * TC_M + rr) * MLA_DV +
+                                          dq * TC_DQ + cg * 32 + qd * 8) =
+                    make_uint4(tile[rr][4 * qd], tile[rr][4 * qd + 1], tile[rr][4 * qd + 2], tile[rr][4 * qd + 3]);
         }
     }
+    grid_dependents_launch();
 }
 
 cudaError_t prepare_mla_decode_tc()
@@ -637,7 +944,9 @@ cudaError_t prepare_mla_decode_tc()
 cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
                                  cudaStream_t s)
 {
-    return launch_dependent(paged_mla_decode_tc, grid, dim3(TC_THREADS), TC_SMEM, s, tm, p);
+    cudaError_t e = launch_dependent(paged_mla_decode_tc, grid, dim3(TC_THREADS), TC_SMEM, s, tm, p);
+    if (e != cudaSuccess || p.max_splits <= 1) return e;
+    return launch_dependent(paged_mla_merge_tc, dim3(TC_DQ / 32, p.head_tiles * 2, p.batch), dim3(TC_M), 0, s, p);
 }
 
 }  // namespace kvp

@@ -33,7 +33,7 @@ struct DecodeParams {
     int batch, q_heads, kv_heads, group, head_groups;
     int q_len, rows;          // query tokens per sequence; rows per kv head = group * q_len
     int max_blocks, num_blocks;
-    int split_blocks, max_splits;
+    int split_blocks, max_splits;   // tcgen05 form: least blocks per CTA range; pieces per sequence
     float scale_log2;         // softmax scale * log2(e)
 };
 
@@ -65,14 +65,16 @@ struct MlaParams {
     const int32_t* ctx;       // [batch]
     uint16_t* out;            // bf16 [batch, q_heads, MLA_DV]
     float* lse;               // [batch, q_heads] or null
-    float* part_o;            // [batch, q_heads, max_splits, MLA_DV]
-    float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum), log2 units
+    float* part_o;            // [batch, q_heads, max_splits, MLA_DV]; tcgen05 form: per piece
+                              // (sequence, head tile, half, split) [8 chunks][8 float4][128 heads]
+    float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum), log2 units;
+                              // tcgen05 form: [piece][128 heads][2]
     uint32_t* err;
-    int* tickets;             // [batch, head_tiles]; zero between calls
-    int* queue;               // tcgen05 form: [0] next work item, [1] CTAs done; zero between calls
+    int* tickets;             // [batch, head_tiles]: finished chunks, zero between calls;
+                              // tcgen05 form: [batch, head_tiles, 2 halves] piece counts
     int batch, q_heads, head_tiles;
     int max_blocks, num_blocks;
-    int split_blocks, max_splits;
+    int split_blocks, max_splits;   // tcgen05 form: least blocks per CTA range; pieces per sequence
     float scale_log2;
 };
 
@@ -126,8 +128,8 @@ int mla_stage_tokens(int block_size, bool prod);
 cudaError_t prepare_mla_decode(int block_size);
 cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtensorMap& tm,
                               const MlaParams& p, cudaStream_t s);
-// The tcgen05 form: tiles of 128 heads, blocks of 64 tokens, four CTAs (latent
-// quarters) per (sequence, head tile, chunk); grid x = head tile * 4 + quarter.
+// The tcgen05 form: tiles of 128 heads, blocks of 64 tokens, two work items (latent
+// halves) per (sequence, head tile, chunk), taken by persistent CTAs (one per SM).
 constexpr int MLA_TC_HEADS = 128;
 constexpr int MLA_TC_BLOCK = 64;
 cudaError_t prepare_mla_decode_tc();

@@ -82,23 +82,59 @@ def decode_flops(w) -> int:
     return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads * s.q_len)
 
 
-def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16) -> dict:
+def mla_tc_pieces(w, split_blocks: int, grid: int) -> np.ndarray:
+    """Pieces each (latent half, head tile, sequence) is cut into by the tensor-core MLA
+    decode's partition: its units (half, head tile, sequence, block), T in all, are cut
+    into G = min(grid, T // split_blocks) (at least 1) equal contiguous ranges, range c =
+    [c T / G, (c + 1) T / G); a sequence with blocks is cut at every range boundary
+    inside it.  Same integer arithmetic as the kernel."""
+    nb = _nb(w)
+    tiles = -(-w.spec.q_heads // 128)
+    S = int(nb.sum())
+    T = S * tiles * 2
+    if T == 0:
+        return np.zeros(0, dtype=np.int64)
+    g = max(1, min(grid, T // max(1, split_blocks)))
+    pre = np.concatenate([[0], np.cumsum(nb)[:-1]]).astype(np.int64)
+    out = []
+    for outer in range(tiles * 2):
+        ub = outer * S + pre
+        for u, n in zip(ub, nb):
+            if n == 0:
+                continue
+            first = ((u + 1) * g - 1) // T
+            last = ((u + n) * g - 1) // T
+            out.append(last - first + 1)
+    return np.array(out, dtype=np.int64)
+
+
+def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0) -> dict:
     """Algorithmic bytes of one paged_mla_decode_attention call: every cached vector once
     (kv), the absorbed queries, the latent outputs, tables, lengths, LSE and the split
     partials.  l2_reads: vector bytes read by all head tiles (each tile of 16 heads
-    reads the sequence's vectors; the copies after the first come from L2)."""
+    reads the sequence's vectors; the copies after the first come from L2).
+
+    tc_grid > 0: the tensor-core form with that many CTAs -- tiles of 128 heads, two
+    latent halves each reading every vector, and pieces from mla_tc_pieces (each piece
+    of a cut sequence writes and the merge reads 128 heads x 256 fp32 numbers and a
+    (max, sum) pair per head)."""
     s = w.spec
     ctx = w.context_lens.astype(np.int64)
     nb = _nb(w)
     kv = int(ctx.sum()) * s.head_dim * 2
-    tiles = -(-s.q_heads // head_tile)
     rows = w.batch * s.q_heads
     qo = rows * (s.head_dim + s.latent_dim) * 2
     meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * rows
-    sb = max(1, split_tokens // s.block_size)
-    nsplit = np.maximum(1, (nb + sb - 1) // sb)
-    multi = nsplit > 1
-    partial = int(nsplit[multi].sum()) * s.q_heads * (s.latent_dim + 2) * 4 * 2
+    if tc_grid > 0:
+        tiles = -(-s.q_heads // 128) * 2
+        pieces = mla_tc_pieces(w, max(1, split_tokens // s.block_size), tc_grid)
+        partial = int(pieces[pieces > 1].sum()) * 128 * ((s.latent_dim // 2) * 4 + 8) * 2
+    else:
+        tiles = -(-s.q_heads // head_tile)
+        sb = max(1, split_tokens // s.block_size)
+        nsplit = np.maximum(1, (nb + sb - 1) // sb)
+        multi = nsplit > 1
+        partial = int(nsplit[multi].sum()) * s.q_heads * (s.latent_dim + 2) * 4 * 2
     other = qo + meta + partial
     return {"kv_logical": kv, "kv_unique": kv, "other": other, "total": kv + other,
             "total_unique": kv + other, "partials": partial, "l2_reads": kv * tiles}
