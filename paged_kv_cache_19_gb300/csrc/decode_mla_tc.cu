@@ -498,8 +498,17 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     const uint32_t ph = static_cast<uint32_t>(gs / TC_NSTAGE) & 1u;
                     const uint32_t stage_addr = smem_u32(smem + st * TC_STAGE);
                     ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_e[st]), ph);
-                    if (ok && gs >= 1)
-                        ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(gs - 1) & 1u);
+                    if (ok && gs >= 1) {
+                        // the score buffer frees right after the softmax has read it: poll
+                        // (test_wait does not suspend the thread)
+                        const uint32_t sf = smem_u32(&ctl->s_free), sp = static_cast<uint32_t>(gs - 1) & 1u;
+                        const unsigned long long t0 = global_timer_ns();
+                        for (uint32_t spin = 0; !mbar_test(sf, sp); ++spin)
+                            if ((spin & 63u) == 63u && global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+                                ok = false;
+                                break;
+                            }
+                    }
                     if (!ok || *abort_flag) {
                         ok = false;
                         break;
@@ -871,7 +880,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 // tile and half, sequence), thread = head.  The pieces' (max, sum) pairs give the
 // weights w_j = l_j 2^(m_j - M) of the standard log-sum-exp merge; the output row is
 // sum_j w_j o_j / sum_j w_j, staged through shared memory for whole-row writes.
-__global__ void __launch_bounds__(TC_M)
+__global__ void __launch_bounds__(TC_M, 4)
 paged_mla_merge_tc(const MlaParams p)
 {
     __shared__ uint32_t tile[TC_M][17];             // bf16 pairs, padded rows
@@ -887,33 +896,41 @@ paged_mla_merge_tc(const MlaParams p)
         const int nh = min(TC_M, p.q_heads - ht * TC_M);
         const size_t piece0 = ((static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq) * p.max_splits;
         const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + piece0 * TC_M + h;
+        const float4* po = reinterpret_cast<const float4*>(p.part_o) + piece0 * (TC_M * TC_DQ / 4) +
+                           static_cast<size_t>(cg * 8) * TC_M + h;
         float M = -INFINITY, W = 0.f;
-        for (int j = 0; j < nsplit; ++j) {
-            const float2 mj = __ldcg(ml + static_cast<size_t>(j) * TC_M);
-            if (mj.y > 0.f) {
-                const float m2 = fmaxf(M, mj.x);
-                W = W * fast_exp2(M - m2) + mj.y * fast_exp2(mj.x - m2);
-                M = m2;
-            }
-        }
         float acc[32];
 #pragma unroll
         for (int v = 0; v < 32; ++v) acc[v] = 0.f;
-        const float4* po = reinterpret_cast<const float4*>(p.part_o) + piece0 * (TC_M * TC_DQ / 4) +
-                           static_cast<size_t>(cg * 8) * TC_M + h;
-        for (int j = 0; j < nsplit; ++j) {
-            const float2 mj = __ldcg(ml + static_cast<size_t>(j) * TC_M);
-            const float wj = mj.y > 0.f ? mj.y * fast_exp2(mj.x - M) : 0.f;
-            const float4* src = po + static_cast<size_t>(j) * (TC_M * TC_DQ / 4);
-            float4 x[8];
+        // two pieces per round: their (max, sum) pairs and numbers are loaded together; the
+        // running max and the accumulators are rescaled when a later piece raises the max
+        for (int j0 = 0; j0 < nsplit; j0 += 2) {
+            float2 mj[2];
+            float4 x[2][8];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) x[v] = __ldcg(src + v * TC_M);
+            for (int i = 0; i < 2; ++i) {
+                const bool in = j0 + i < nsplit;
+                const size_t j = static_cast<size_t>(in ? j0 + i : j0);
+                mj[i] = in ? __ldcg(ml + j * TC_M) : make_float2(-INFINITY, 0.f);
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                acc[4 * v] += wj * x[v].x;
-                acc[4 * v + 1] += wj * x[v].y;
-                acc[4 * v + 2] += wj * x[v].z;
-                acc[4 * v + 3] += wj * x[v].w;
+                for (int v = 0; v < 8; ++v)
+                    x[i][v] = in ? __ldcg(po + j * (TC_M * TC_DQ / 4) + v * TC_M) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                if (!(mj[i].y > 0.f)) continue;
+                const float m2 = fmaxf(M, mj[i].x);
+                const float fo = fast_exp2(M - m2);        // 0 while nothing is accumulated
+                const float wj = mj[i].y * fast_exp2(mj[i].x - m2);
+                W = W * fo + wj;
+                M = m2;
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    acc[4 * v] = acc[4 * v] * fo + wj * x[i][v].x;
+                    acc[4 * v + 1] = acc[4 * v + 1] * fo + wj * x[i][v].y;
+                    acc[4 * v + 2] = acc[4 * v + 2] * fo + wj * x[i][v].z;
+                    acc[4 * v + 3] = acc[4 * v + 3] * fo + wj * x[i][v].w;
+                }
             }
         }
         const float winv = W > 0.f ? 1.f / W : 0.f;
