@@ -609,9 +609,10 @@ def run_ours(args, rank, world, local):
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
             "roofline": {"kernel": KERNEL_NAMES[kernel_kind(s)]
-                                   + " (one launch per decode call, in-kernel "
-                                   "split-KV merge; K launches timed back to back after the "
-                                   "timed steps)",
+                                   + (" + paged_mla_merge_tc (the decode call's two launches; "
+                                      if kernel_kind(s) == "mla_tc" and max_splits > 1 else
+                                      " (one launch per decode call, in-kernel split-KV merge; ")
+                                   + "K calls timed back to back after the timed steps)",
                          "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
