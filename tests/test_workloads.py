@@ -2,6 +2,7 @@
 import os
 
 import numpy as np
+import pytest
 
 import workloads
 from workloads import accounting
@@ -63,3 +64,43 @@ def test_decode_bytes_counts_kv_and_partials():
     assert one["kv_logical"] == 110 * 2 * 2 * 64 * 2 and one["partials"] == 0
     many = accounting.decode_bytes(w, split_tokens=32)         # sequence 0 -> 4 chunks
     assert many["partials"] == 4 * 8 * (64 + 2) * 4 * 2
+
+
+def _brute_force_pieces(nb, tiles, split_blocks, grid):
+    """Assign every unit (latent half / head tile, sequence, block) to its range by
+    scanning the range starts, then count the distinct ranges each sequence touches."""
+    units = [(outer, b) for outer in range(tiles * 2) for b, n in enumerate(nb) for _ in range(n)]
+    T = len(units)
+    g = max(1, min(grid, T // split_blocks))
+    starts = [c * T // g for c in range(g + 1)]
+    owner = []
+    c = 0
+    for u in range(T):
+        while starts[c + 1] <= u:
+            c += 1
+        owner.append(c)
+    sizes = [starts[c + 1] - starts[c] for c in range(g)]
+    seen = {}
+    for (key, c) in zip(units, owner):
+        seen.setdefault(key, set()).add(c)
+    pieces = [len(seen[(outer, b)]) for outer in range(tiles * 2) for b, n in enumerate(nb) if n > 0]
+    return pieces, sizes, g
+
+
+@pytest.mark.parametrize("ctx,heads,split_blocks,grid", [
+    ([1, 70, 300, 2, 4096, 65], 128, 1, 152),
+    ([640, 64, 3000, 129, 2000], 128, 16, 7),
+    ([100] * 40, 256, 4, 33),
+    ([5000, 1], 96, 8, 152),
+])
+def test_mla_tc_pieces_match_a_brute_force_partition(ctx, heads, split_blocks, grid):
+    w = workloads.make(workloads.mla(batch=len(ctx), q_heads=heads, block_size=64, ctx=ctx, seed=3))
+    nb = [-(-c // 64) for c in ctx]
+    want, sizes, g = _brute_force_pieces(nb, -(-heads // 128), split_blocks, grid)
+    got = accounting.mla_tc_pieces(w, split_blocks, grid)
+    assert list(got) == want
+    # every range but a lone one holds at least split_blocks units, and no sequence is cut
+    # into more pieces than the workspace bound ceil((max_blocks - 1) / split_blocks) + 1
+    if g > 1:
+        assert min(sizes) >= split_blocks
+    assert max(want) <= (max(nb) - 1 + split_blocks - 1) // split_blocks + 1
