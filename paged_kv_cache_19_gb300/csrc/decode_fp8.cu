@@ -27,14 +27,4 @@ cudaError_t prepare_decode_fp8(int head_dim, int block_size, int head_tile)
     return cudaErrorInvalidValue;
 }
 
-int smem_decode_fp8(int head_dim, int block_size, int head_tile)
-{
-#define KVP_CASE(D_, BS_, NT_) \
-    if (head_dim == D_ && block_size == BS_ && head_tile == NT_) \
-        return GridCfg<true, D_, BS_, NT_>::SMEM;
-    KVP_FP8_VARIANTS(KVP_CASE)
-#undef KVP_CASE
-    return 0;
-}
-
 }  // namespace kvp

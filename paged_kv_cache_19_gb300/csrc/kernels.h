@@ -108,10 +108,6 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 // Row tile of one CTA: 8 or 16 query rows of a kv head (padding unused rows).
 inline int head_tile_for_group(int rows) { return rows <= 8 ? 8 : 16; }
 
-// Dynamic shared memory of one main-kernel CTA (stages + barriers + alignment
-// slack); 0 when no variant exists for these sizes.
-int smem_decode_bf16(int head_dim, int block_size, int head_tile);
-int smem_decode_fp8(int head_dim, int block_size, int head_tile);
 // Raises the variant's dynamic shared-memory limit (once, at pool creation).
 cudaError_t prepare_decode_bf16(int head_dim, int block_size, int head_tile);
 cudaError_t prepare_decode_fp8(int head_dim, int block_size, int head_tile);
