@@ -486,9 +486,20 @@ def run_ours(args, rank, world, local):
     def append(kk, vv, tt, cc, sq, ps):
         kp.paged_kv_append(pool, kk, vv, tt, cc, token_seq=sq, token_pos=ps, stream=stream)
 
+    def run_step(kk, vv, qq, tt, cc, sq, ps):
+        """One decode step through the public API: paged_decode_step (append + attention in
+        one call, the attention overlapping the append) for K/V caches -- the step's tokens
+        are the last q_len of every sequence, in sequence order, which is its layout -- and
+        append then attention for latent pools."""
+        if s.mla:
+            append(kk, vv, tt, cc, sq, ps)
+            attend(qq, tt, cc)
+        else:
+            kp.paged_decode_step(pool, kk, vv, qq, tt, cc, w.scale, kv_split_tokens=split_req,
+                                 workspace=workspace, out=out, lse=lse, stream=stream)
+
     def step():
-        append(stp["k"], stp["v"], tables, ctx, stp["seq"], stp["pos"])
-        attend(q, tables, ctx)
+        run_step(stp["k"], stp["v"], q, tables, ctx, stp["seq"], stp["pos"])
 
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     dec_bytes = decode_bytes(w, split_tokens, sms)
@@ -572,8 +583,7 @@ def run_ours(args, rank, world, local):
         def e2e_step():
             for name in d:
                 d[name].copy_(h[name], non_blocking=True)
-            append(d["k"], d.get("v"), d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
-            attend(d["q"], d["tables"], d["ctx"])
+            run_step(d["k"], d.get("v"), d["q"], d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(max(3, args.warmup)):

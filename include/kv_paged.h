@@ -248,6 +248,30 @@ kv_status paged_multi_query_workspace_size(const kv_pool* pool, int batch, int q
                                            size_t* bytes);
 
 /*
+ * paged_decode_step -- one decode step of every sequence of the batch: the
+ * append of its q_len new tokens (xuewyang.github.io/posts/kv, "A toy vLLM",
+ * write_kv: the new token is appended first) followed by their attention over
+ * the cache (paged_attention_multi_query), both enqueued on `stream`.
+ *   k_new, v_new: bf16 [batch * q_len, kv_heads, head_dim]; row i is token
+ *     i % q_len of sequence i / q_len, written at position
+ *     context_lens[b] - q_len + i % q_len (context_lens already counts the new
+ *     tokens).  The pool must not be a latent pool (KV_ERR_INVALID_ARG).
+ *   Everything else -- q, tables, lengths, split, workspace, outputs, device
+ *   error bits -- as in paged_attention_multi_query; all arguments are checked
+ *   before anything is launched, so an error leaves the pool untouched.
+ *   The result equals paged_kv_append (with those positions) followed by
+ *   paged_attention_multi_query.  Because the attention kernel knows that the
+ *   preceding append writes only those last q_len positions, it reads every
+ *   other block of the cache while the append runs and waits for the append
+ *   only before loading a block that holds a new token.
+ */
+kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new, const void* q,
+                            int q_heads, int q_len, const int32_t* block_tables, int max_blocks,
+                            const int32_t* context_lens, int batch, float scale,
+                            int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                            void* out, float* lse_out, void* stream);
+
+/*
  * Allocation-free decode attention.  The paper has no counterpart to this call;
  * it exists for users of this library who cannot allocate device memory at the
  * call site: plug-in hosts that give a kernel only its input and output

@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_attention_multi_query",
+    "paged_decode_step",
     "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
     "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING", "kv_mla_pool_create",
     "paged_mla_decode_plan", "paged_mla_workspace_size", "paged_mla_decode_attention",
@@ -91,6 +92,8 @@ def load_library():
             "paged_attention_multi_query": ([P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
                                              P], I),
             "paged_multi_query_workspace_size": ([P, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "paged_decode_step": ([P, P, P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P],
+                                  I),
             "kv_bm_create": ([I, I, I, ctypes.POINTER(P)], I),
             "kv_bm_destroy": ([P], I),
             "kv_bm_add_sequence": ([P, L, ctypes.c_uint64], I),
@@ -340,6 +343,49 @@ def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale
                                            _ptr(workspace), int(ws_bytes), _ptr(out), _ptr(lse),
                                            _stream(stream)),
            "paged_attention_multi_query")
+    return out
+
+
+def paged_decode_step(pool: Pool, k_new, v_new, q, block_tables, context_lens,
+                      scale: float | None = None, kv_split_tokens: int = 0, workspace=None,
+                      out=None, lse=None, stream=None):
+    """One decode step: append k_new / v_new (bf16 [B * q_len, Hkv, d]; row i is token i %
+    q_len of sequence i / q_len, at position ctx - q_len + i % q_len), then the attention of
+    q (bf16 [B, Hq, q_len, d], or [B, Hq, d] for one token per sequence) over the cache.
+    Returns out (shaped like q)."""
+    lib = load_library()
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    if q.dim() == 3:
+        batch, q_heads, d = q.shape
+        q_len = 1
+    elif q.dim() == 4:
+        batch, q_heads, q_len, d = q.shape
+    else:
+        raise ValueError("q must be [batch, q_heads, head_dim] or [batch, q_heads, q_len, head_dim]")
+    if k_new.shape[0] != batch * q_len or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must hold batch * q_len tokens")
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = paged_multi_query_workspace_size(pool, batch, q_heads, q_len, max_blocks,
+                                                kv_split_tokens)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_decode_step(pool.handle, _ptr(k_new), _ptr(v_new), _ptr(q), int(q_heads),
+                                 int(q_len), _ptr(block_tables), int(max_blocks), _ptr(context_lens),
+                                 int(batch), float(scale), int(kv_split_tokens), _ptr(workspace),
+                                 int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
+           "paged_decode_step")
     return out
 
 

@@ -398,6 +398,7 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
     p.kv_heads = pool->kv_heads;
     p.head_dim = pool->head_dim;
     p.fp8 = pool->dtype == KV_DTYPE_FP8_E4M3;
+    p.q_len = 1;
     return kvp::launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
                                                                                    : KV_ERR_CUDA;
 }
@@ -448,12 +449,17 @@ kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_head
                                             bytes);
 }
 
-kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_heads, int q_len,
-                                      const int32_t* block_tables, int max_blocks,
-                                      const int32_t* context_lens, int batch, float scale,
-                                      int kv_split_tokens, void* workspace,
-                                      size_t workspace_bytes, void* out, float* lse_out,
-                                      void* stream)
+}  // extern "C"
+
+namespace {
+
+// Validates a decode call and fills its kernel parameters and grid (nothing launched).
+kv_status make_decode_launch(const kv_pool* pool, const void* q, int q_heads, int q_len,
+                             const int32_t* block_tables, int max_blocks,
+                             const int32_t* context_lens, int batch, float scale,
+                             int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                             void* out, float* lse_out, Plan* plan_out, kvp::DecodeParams* pp,
+                             dim3* grid)
 {
     Plan plan;
     kv_status st = make_plan(pool, batch, q_heads, q_len, max_blocks, kv_split_tokens, &plan);
@@ -474,7 +480,7 @@ kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_
     if (st != KV_OK) return st;
 
     const WorkspaceLayout wl = workspace_layout(pool, batch, plan);
-    kvp::DecodeParams p;
+    kvp::DecodeParams& p = *pp;
     p.q = static_cast<const uint16_t*>(q);
     p.tables = block_tables;
     p.ctx = context_lens;
@@ -499,17 +505,91 @@ kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.dep_tail = 0;
     // chunk-major grid: x = (kv head, row tile), y = sequence, z = chunk
-    const dim3 grid(static_cast<unsigned>(pool->kv_heads * plan.head_groups),
-                    static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));
+    *grid = dim3(static_cast<unsigned>(pool->kv_heads * plan.head_groups),
+                 static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));
+    *plan_out = plan;
+    return KV_OK;
+}
+
+kv_status launch_decode(const kv_pool* pool, const Plan& plan, dim3 grid, const kvp::DecodeParams& p,
+                        void* stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = pool->dtype == KV_DTYPE_BF16
                         ? kvp::launch_decode_bf16(pool->head_dim, pool->block_size, plan.head_tile,
                                                   grid, pool->tmk, pool->tmv, p, s)
                         : kvp::launch_decode_fp8(pool->head_dim, pool->block_size, plan.head_tile,
                                                  grid, pool->tmk, pool->tmv, p, s);
     return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status paged_attention_multi_query(const kv_pool* pool, const void* q, int q_heads, int q_len,
+                                      const int32_t* block_tables, int max_blocks,
+                                      const int32_t* context_lens, int batch, float scale,
+                                      int kv_split_tokens, void* workspace,
+                                      size_t workspace_bytes, void* out, float* lse_out,
+                                      void* stream)
+{
+    Plan plan;
+    kvp::DecodeParams p;
+    dim3 grid;
+    const kv_status st = make_decode_launch(pool, q, q_heads, q_len, block_tables, max_blocks,
+                                            context_lens, batch, scale, kv_split_tokens, workspace,
+                                            workspace_bytes, out, lse_out, &plan, &p, &grid);
+    if (st != KV_OK || batch == 0) return st;
+    return launch_decode(pool, plan, grid, p, stream);
+}
+
+kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new, const void* q,
+                            int q_heads, int q_len, const int32_t* block_tables, int max_blocks,
+                            const int32_t* context_lens, int batch, float scale,
+                            int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                            void* out, float* lse_out, void* stream)
+{
+    if (pool == nullptr || q_len < 1) return KV_ERR_INVALID_ARG;
+    // everything is checked before anything is launched
+    Plan plan;
+    kvp::DecodeParams p;
+    dim3 grid;
+    kv_status st = make_decode_launch(pool, q, q_heads, q_len, block_tables, max_blocks,
+                                      context_lens, batch, scale, kv_split_tokens, workspace,
+                                      workspace_bytes, out, lse_out, &plan, &p, &grid);
+    if (st != KV_OK || batch == 0) return st;
+    if (k_new == nullptr || v_new == nullptr || !aligned(k_new, 16) || !aligned(v_new, 16))
+        return KV_ERR_INVALID_ARG;
+    if (static_cast<long long>(batch) * q_len > std::numeric_limits<int>::max())
+        return KV_ERR_UNSUPPORTED;
+    kvp::AppendParams a;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    a.token_seq = nullptr;
+    a.token_pos = nullptr;
+    a.tables = block_tables;
+    a.ctx = context_lens;
+    a.k_pool = pool->k;
+    a.v_pool = pool->v;
+    a.k_scale = pool->k_scale;
+    a.v_scale = pool->v_scale;
+    a.err = pool->err;
+    a.num_tokens = batch * q_len;
+    a.batch = batch;
+    a.max_blocks = max_blocks;
+    a.num_blocks = pool->num_blocks;
+    a.block_size = pool->block_size;
+    a.kv_heads = pool->kv_heads;
+    a.head_dim = pool->head_dim;
+    a.fp8 = pool->dtype == KV_DTYPE_FP8_E4M3;
+    a.q_len = q_len;
+    if (kvp::launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
+    // the append wrote only the last q_len positions of each sequence
+    p.dep_tail = q_len;
+    return launch_decode(pool, plan, grid, p, stream);
 }
 
 kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads,

@@ -6,8 +6,8 @@
 namespace kvp {
 
 // ---------------------------------------------------------------------------
-// Append: token i goes to sequence token_seq[i] (or i) at position
-// token_pos[i] (or ctx - 1): block table entry pos / block_size, slot
+// Append: token i goes to sequence token_seq[i] (or i / q_len) at position
+// token_pos[i] (or ctx - q_len + i % q_len): block table entry pos / block_size, slot
 // pos % block_size, all kv heads (xuewyang.github.io/posts/kv, "A toy vLLM",
 // write_kv; brunomaga.github.io, PagedKVCache.append).  One CTA per token;
 // each thread moves 8 elements (16 bytes of bf16 input) per step.
@@ -19,12 +19,12 @@ __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams
     grid_dependency_wait();                        // inputs of the preceding kernel are ready
     grid_dependents_launch();
     const int i = blockIdx.x;
-    const int seq = p.token_seq != nullptr ? __ldg(p.token_seq + i) : i;
+    const int seq = p.token_seq != nullptr ? __ldg(p.token_seq + i) : i / p.q_len;
     if (seq < 0 || seq >= p.batch) {
         if (threadIdx.x == 0) atomicOr(p.err, KV_DEVERR_SEQ);
         return;
     }
-    const int pos = p.token_pos != nullptr ? __ldg(p.token_pos + i) : __ldg(p.ctx + seq) - 1;
+    const int pos = p.token_pos != nullptr ? __ldg(p.token_pos + i) : __ldg(p.ctx + seq) - p.q_len + i % p.q_len;
     if (pos < 0 || pos / p.block_size >= p.max_blocks) {
         if (threadIdx.x == 0) atomicOr(p.err, KV_DEVERR_POSITION);
         return;

@@ -66,7 +66,10 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         fence_mbar_init();
     }
-    grid_dependency_wait();                          // inputs of the preceding kernel are ready
+    // Inputs of the preceding kernel are ready -- unless it only appended the last
+    // dep_tail positions of each sequence: then only the producer waits, before the first
+    // load of a block that holds one of them.
+    if (p.dep_tail == 0) grid_dependency_wait();
 
     // Independent loads in flight together: the context length, the chunk's
     // first 32 table entries (producer) and the query fragments (consumers).
@@ -106,6 +109,8 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         int issued = 0;
         bool ok = true;
+        bool waited = p.dep_tail == 0;
+        const int tail_blk = (ctx - p.dep_tail) / BS;    // first block written by the append
         for (int base = 0; base < nb && ok; base += 32) {
             const int j = base + lane;
             int id = -1;
@@ -124,6 +129,10 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const uint32_t ph = static_cast<uint32_t>(it / C::NSTAGE) & 1u;
                 int good = 1;
                 if (lane == 0) {
+                    if (!waited && blk0 + it >= tail_blk) {
+                        grid_dependency_wait();
+                        waited = true;
+                    }
                     if (!mbar_wait_bounded(smem_u32(empty + st), ph ^ 1u)) {
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         good = 0;

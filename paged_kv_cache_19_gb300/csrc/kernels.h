@@ -33,8 +33,13 @@ struct DecodeParams {
     int batch, q_heads, kv_heads, group, head_groups;
     int q_len, rows;          // query tokens per sequence; rows per kv head = group * q_len
     int max_blocks, num_blocks;
-    int split_blocks, max_splits;   // tcgen05 form: least blocks per CTA range; pieces per sequence
+    int split_blocks, max_splits;   // chunk length in blocks; most chunks a sequence can have
     float scale_log2;         // softmax scale * log2(e)
+    // 0: the preceding kernel on the stream may have written anything this one reads, so
+    // wait for it before the first read.  n > 0: it wrote only the last n positions of
+    // each sequence in the pool (the step's append), so blocks holding none of them are
+    // read at once and only the loads of the others wait for it.
+    int dep_tail;
 };
 
 struct AppendParams {
@@ -51,6 +56,8 @@ struct AppendParams {
     uint32_t* err;
     int num_tokens, batch, max_blocks, num_blocks, block_size, kv_heads, head_dim;
     int fp8;
+    int q_len;                // without token_seq / token_pos: token i is token i % q_len of
+                              // sequence i / q_len, at position ctx - q_len + i % q_len
 };
 
 // Absorbed multi-head latent attention over a latent pool [num_blocks,
@@ -74,7 +81,8 @@ struct MlaParams {
                               // tcgen05 form: [batch, head_tiles, 2 halves] piece counts
     int batch, q_heads, head_tiles;
     int max_blocks, num_blocks;
-    int split_blocks, max_splits;   // tcgen05 form: least blocks per CTA range; pieces per sequence
+    int split_blocks, max_splits;   // chunk length in blocks (tcgen05 form: least blocks per CTA
+                                    // range); most chunks (pieces) a sequence can have
     float scale_log2;
 };
 

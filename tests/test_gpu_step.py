@@ -1,0 +1,133 @@
+"""GPU parity of paged_decode_step: the append of the step's new tokens and their attention
+in one call, the attention streaming the blocks the append does not touch while it runs.
+
+The pool after the step must equal the oracle's append image bit for bit, the outputs the
+oracle within the attention tolerances, and both must be bit-identical to the separate
+paged_kv_append + attention calls (the same kernels; only the dependency differs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_19_gb300 as kp
+import workloads
+from gpu_util import LSE_ABS, MAX_ABS, REL_L2, Staged, compare
+
+pytestmark = pytest.mark.gpu
+
+C = workloads.custom
+STEP = {
+    "tiny": workloads.CONFIGS["tiny"],
+    "g4_one_chunk": C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                      ctx=[1, 16, 203], seed=301),
+    "g8_split64": C(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,
+                    ctx=[37, 300, 1000], seed=302, split_tokens=64),
+    "g2_d64_bs32_ctx_on_block_edges": C(batch=5, q_heads=4, kv_heads=2, head_dim=64, block_size=32,
+                                        ctx=[1, 32, 33, 64, 700], seed=303, split_tokens=96),
+    "fp8_g4": C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                ctx=[3, 150, 400], seed=304, cache_dtype="fp8_e4m3", split_tokens=32),
+    "verify_t4": C(batch=4, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                   ctx=[4, 17, 130, 700], q_len=4, seed=305),
+    "verify_t3_fp8": C(batch=3, q_heads=4, kv_heads=4, head_dim=128, block_size=32,
+                       ctx=[3, 64, 200], q_len=3, seed=306, cache_dtype="fp8_e4m3"),
+    "long_ragged_auto_split": C(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,
+                                ctx=[5000, 17, 2500], seed=307),
+}
+
+
+def _step_inputs(st):
+    w = st.w
+    if w.q_len > 1:
+        return st.k_step, st.v_step, st.q_multi
+    return st.k_new, st.v_new, st.q
+
+
+def _lse_shape(q):
+    return q.shape[:3] if q.dim() == 4 else q.shape[:2]
+
+
+@pytest.mark.parametrize("name", sorted(STEP))
+def test_step_matches_the_oracle_and_the_separate_calls(name):
+    w = workloads.make(STEP[name])
+    fused = Staged(w, step_append=False)
+    k, v, q = _step_inputs(fused)
+    out = torch.empty_like(q)
+    lse = torch.empty(_lse_shape(q), dtype=torch.float32, device="cuda")
+    kp.paged_decode_step(fused.pool, k, v, q, fused.tables, fused.ctx, w.scale,
+                         kv_split_tokens=w.spec.split_tokens, out=out, lse=lse)
+    torch.cuda.synchronize()
+
+    # the pool: bit for bit the oracle's image after the append
+    kimg, vimg = oracle.pool_image(w, after_step=True)
+    kr, vr = fused.pool.raw_bytes()
+    assert np.array_equal(kr.cpu().numpy(), kimg)
+    assert np.array_equal(vr.cpu().numpy(), vimg)
+
+    # the outputs: the oracle within tolerance
+    if w.q_len > 1:
+        ref, ref_lse = oracle.decode_multi_workload(w, w.q_multi, w.q_len)
+    else:
+        ref, ref_lse = oracle.decode_workload(w)
+    max_abs, rel, got = compare(out, ref)
+    assert np.isfinite(got).all()
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+    assert np.nanmax(np.abs(lse.cpu().numpy() - ref_lse)) <= LSE_ABS
+    assert fused.pool.device_errors() == 0
+
+    # the separate calls give the same bits
+    sep = Staged(w, step_append=True)
+    if w.q_len > 1:
+        out2, lse2 = sep.multi()
+    else:
+        out2, lse2 = sep.decode()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    sep.destroy()
+    fused.destroy()
+
+
+def test_repeated_steps_on_one_stream_stay_exact():
+    """Several steps back to back on one stream (each step's attention overlapping the
+    append that precedes it), each checked against the oracle of its own step."""
+    spec = C(batch=4, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+             ctx=[15, 16, 17, 300], seed=308, split_tokens=64)
+    w = workloads.make(spec)
+    st = Staged(w, step_append=False)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            out = torch.empty_like(st.q)
+            kp.paged_decode_step(st.pool, st.k_new, st.v_new, st.q, st.tables, st.ctx, w.scale,
+                                 kv_split_tokens=spec.split_tokens, out=out, stream=s)
+            outs.append(out)
+    s.synchronize()
+    ref, _ = oracle.decode_workload(w)
+    for out in outs:                                   # the same step repeated: same result
+        max_abs, rel, _ = compare(out, ref)
+        assert max_abs <= MAX_ABS and rel <= REL_L2
+        assert torch.equal(out, outs[0])
+    assert st.pool.device_errors() == 0
+    st.destroy()
+
+
+def test_step_rejects_bad_arguments_before_launching():
+    w = workloads.make(C(batch=2, q_heads=4, kv_heads=2, head_dim=64, block_size=16,
+                         ctx=[10, 40], seed=309))
+    st = Staged(w, step_append=False)
+    before = [t.clone() for t in st.pool.raw_bytes()]
+    bad_q = torch.empty(2, 5, 64, dtype=torch.bfloat16, device="cuda")   # 5 heads over 2 kv heads
+    with pytest.raises(kp.KVError):
+        kp.paged_decode_step(st.pool, st.k_new, st.v_new, bad_q, st.tables, st.ctx, w.scale)
+    torch.cuda.synchronize()
+    after = st.pool.raw_bytes()
+    assert all(torch.equal(a, b) for a, b in zip(before, after))      # nothing was appended
+    st.destroy()
+    lat = kp.kv_mla_pool_create(8, 64, 512, 64)
+    with pytest.raises(kp.KVError):
+        kp.paged_decode_step(lat, torch.zeros(1, 576, dtype=torch.bfloat16, device="cuda"),
+                             torch.zeros(1, 576, dtype=torch.bfloat16, device="cuda"),
+                             torch.zeros(1, 16, 576, dtype=torch.bfloat16, device="cuda"),
+                             torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
+                             torch.ones(1, dtype=torch.int32, device="cuda"))
+    lat.destroy()
