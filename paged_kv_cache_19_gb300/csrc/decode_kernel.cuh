@@ -30,7 +30,7 @@ template <bool FP8, int D, int BS, int NT>
 struct GridCfg : DecodeCfg<FP8, D, BS, NT> {
     using C = DecodeCfg<FP8, D, BS, NT>;
     static constexpr int SMEM = 1024 + C::NSTAGE * C::STAGE + C::NSTAGE * (8 + 8 + 4) + 16;
-    static constexpr int MINB = NT == 8 ? 3 : 2;
+    static constexpr int MINB = 3;                  // CTAs per SM (row tiles of 8 and 16)
     static_assert(C::RED_BYTES <= C::NSTAGE * C::STAGE, "epilogue buffer reuses the stages");
 };
 
