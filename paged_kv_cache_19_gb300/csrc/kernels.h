@@ -132,8 +132,10 @@ int mla_stage_tokens(int block_size, bool prod);
 cudaError_t prepare_mla_decode(int block_size);
 cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtensorMap& tm,
                               const MlaParams& p, cudaStream_t s);
-// The tcgen05 form: tiles of 128 heads, blocks of 64 tokens, two work items (latent
-// halves) per (sequence, head tile, chunk), taken by persistent CTAs (one per SM).
+// The tcgen05 form: tiles of 128 heads, blocks of 64 tokens, one CTA per SM taking an
+// equal contiguous range of the (latent half, head tile, sequence, block) units; the
+// pieces of sequences cut by a range boundary are merged by a second kernel, launched
+// by launch_mla_decode_tc when max_splits > 1.
 constexpr int MLA_TC_HEADS = 128;
 constexpr int MLA_TC_BLOCK = 64;
 cudaError_t prepare_mla_decode_tc();
