@@ -69,20 +69,27 @@ KERNEL_SOURCES = {
     "gqa": ["decode_kernel.cuh", "decode_common.cuh", "decode_bf16.cu", "decode_fp8.cu",
             "device_common.cuh"],
     "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
-    "mla_tc": ["decode_mla_tc.cu", "tcgen05.cuh", "decode_common.cuh", "device_common.cuh"],
+    "mla_tc": ["decode_mla_tc.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
+               "device_common.cuh"],
+    "mla_tcn": ["decode_mla_tcn.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
+                "device_common.cuh"],
 }
 
 
 def kernel_kind(spec) -> str:
-    """Which decode kernel a workload runs: the GQA kernel, or the mma.sync / tcgen05 form of
-    the latent decode (tcgen05 for blocks of 64 and at least 64 query heads)."""
+    """Which decode kernel a workload runs: the GQA kernel, or a form of the latent decode
+    (tcgen05 for blocks of 64: the wide form for at least 64 query heads, the narrow one
+    below; mma.sync for other block sizes)."""
     if not spec.mla:
         return "gqa"
-    return "mla_tc" if spec.block_size == 64 and spec.q_heads >= 64 else "mla"
+    if spec.block_size != 64:
+        return "mla"
+    return "mla_tc" if spec.q_heads >= 64 else "mla_tcn"
 
 
 KERNEL_NAMES = {"gqa": "paged_decode_main", "mla": "paged_mla_decode_main (mma.sync)",
-                "mla_tc": "paged_mla_decode_tc (tcgen05)"}
+                "mla_tc": "paged_mla_decode_tc (tcgen05)",
+                "mla_tcn": "paged_mla_decode_tcn (tcgen05, 16-head tiles)"}
 
 
 def kernel_source_sha(kind: str = "gqa") -> str:
@@ -243,14 +250,17 @@ def tc_grid(w, split_tokens, sms=152):
     """CTAs of the tensor-core MLA launch (the library's rule: one per SM, no more than
     ranges of split_blocks units the batch could hold)."""
     s = w.spec
-    units = -(-s.q_heads // 128) * 2 * w.batch * w.max_blocks
+    outer = -(-s.q_heads // 128) * 2 if kernel_kind(s) == "mla_tc" else -(-s.q_heads // 16)
+    units = outer * w.batch * w.max_blocks
     return min(sms, max(1, units // max(1, split_tokens // s.block_size)))
 
 
 def decode_bytes(w, split_tokens, sms=152):
     if w.spec.mla:
-        grid = tc_grid(w, split_tokens, sms) if kernel_kind(w.spec) == "mla_tc" else 0
-        return accounting.mla_decode_bytes(w, split_tokens, tc_grid=grid)
+        kind = kernel_kind(w.spec)
+        grid = tc_grid(w, split_tokens, sms) if kind in ("mla_tc", "mla_tcn") else 0
+        return accounting.mla_decode_bytes(w, split_tokens, tc_grid=grid,
+                                           form="wide" if kind == "mla_tc" else "narrow")
     return accounting.decode_bytes(w, split_tokens)
 
 
@@ -505,9 +515,10 @@ def run_ours(args, rank, world, local):
     dec_bytes = decode_bytes(w, split_tokens, sms)
     app_bytes = accounting.mla_append_bytes(w) if s.mla else accounting.append_bytes(w)
     step_bytes = dec_bytes["total"] + app_bytes
-    # append + decode; the tensor-core MLA form adds its merge kernel when sequences can be
-    # cut into pieces (the other forms merge inside the decode kernel)
-    launches_per_step = 3 if kernel_kind(s) == "mla_tc" and max_splits > 1 else 2
+    # append + decode; the tensor-core MLA forms add their merge kernel when sequences can
+    # be cut into pieces (the other kernels merge inside the decode kernel)
+    two_kernels = kernel_kind(s) in ("mla_tc", "mla_tcn") and max_splits > 1
+    launches_per_step = 3 if two_kernels else 2
     # (the decode-only roofline loop after the timed region launches K more decode kernels)
 
     for _ in range(max(3, args.warmup)):
@@ -633,8 +644,9 @@ def run_ours(args, rank, world, local):
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
             "roofline": {"kernel": KERNEL_NAMES[kernel_kind(s)]
-                                   + (" + paged_mla_merge_tc (the decode call's two launches; "
-                                      if kernel_kind(s) == "mla_tc" and max_splits > 1 else
+                                   + ((" + paged_mla_merge_tc" + ("n" if kernel_kind(s) == "mla_tcn" else "")
+                                       + " (the decode call's two launches; ")
+                                      if two_kernels else
                                       " (one launch per decode call, in-kernel split-KV merge; ")
                                    + "K calls timed back to back after the timed steps)",
                          "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,

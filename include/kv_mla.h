@@ -50,15 +50,18 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
  * block_size (0 = automatic, from the batch, heads and SM count: 768 .. 2048
  * tokens), and the most chunks a sequence can have.
  *
- * Two kernels serve this call.  Latent pools with blocks of 64 tokens and at
- * least 64 query heads run the tcgen05 form: tiles of 128 heads on the MMA's M
- * dimension, accumulators in tensor memory, one CTA per SM.  Its work units
- * (latent half, head tile, sequence, block) are cut into equal contiguous ranges,
- * one per CTA; a sequence cut by a range boundary is merged from its pieces by a
- * second kernel.  For it the chunk argument is the least number of tokens a range
- * holds (0 = automatic: 256 .. 1024 tokens), and max_splits the most pieces a
- * sequence can be cut into.  Other shapes run the mma.sync form with tiles of 16
- * heads. */
+ * Three kernels serve this call.  Latent pools with blocks of 64 tokens run a
+ * tcgen05 form, accumulators in tensor memory, one CTA per SM: the wide one for at
+ * least 64 query heads (tiles of 128 heads on the MMA's M dimension, each CTA
+ * producing one half of the 512 latent outputs), the narrow one below that (tiles
+ * of 16 heads; each MMA covers the 16 heads of a tile and 64 tokens, or 128 latent
+ * numbers for the output).  Their work units ((latent half,) head tile, sequence,
+ * block) are cut into equal contiguous ranges, one per CTA; a sequence cut by a
+ * range boundary is merged from its pieces by a second kernel.  For them the chunk
+ * argument is the least number of tokens a range holds (0 = automatic: 256 .. 1024
+ * tokens), and max_splits the most pieces a sequence can be cut into.  Pools with
+ * other block sizes run the mma.sync form with tiles of 16 heads, a CTA per
+ * (sequence, head tile, chunk) and the merge inside the kernel. */
 kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                 int kv_split_tokens, int* split_tokens, int* max_splits);
 

@@ -612,15 +612,24 @@ namespace {
 
 constexpr int kMlaHeadTile = 16;
 
-struct MlaPlan {
-    int head_tiles, split_blocks, max_splits;
-    int tc;                 // tcgen05 form: head tiles of 128, two latent halves each
+// The three forms of the latent decode.
+enum MlaForm {
+    kMlaMma = 0,            // mma.sync, head tiles of 16, a CTA per (tile, sequence, chunk)
+    kMlaWide = 1,           // tcgen05, head tiles of 128, two latent halves each
+    kMlaNarrow = 2,         // tcgen05, head tiles of 16
 };
 
-// The tcgen05 form takes wide head tiles (at least 64 real heads of 128 rows).
-bool use_tc(const kv_pool* pl, int q_heads)
+struct MlaPlan {
+    int head_tiles, split_blocks, max_splits;
+    int form;               // MlaForm
+};
+
+// Blocks of 64 tokens take a tcgen05 form: the wide one for at least 64 heads (tiles of
+// 128 rows), the narrow one below that.
+int mla_form(const kv_pool* pl, int q_heads)
 {
-    return pl->has_tc && q_heads >= 64;
+    if (!pl->has_tc) return kMlaMma;
+    return q_heads >= 64 ? kMlaWide : kMlaNarrow;
 }
 
 // Automatic chunk: about eight chunks per SM over the worst case, kept between
@@ -637,19 +646,20 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
     if (static_cast<long long>(max_blocks) * pl->block_size > std::numeric_limits<int>::max())
         return KV_ERR_INVALID_ARG;
     MlaPlan p;
-    p.tc = use_tc(pl, q_heads) ? 1 : 0;
-    const int tile = p.tc ? kvp::MLA_TC_HEADS : kMlaHeadTile;
+    p.form = mla_form(pl, q_heads);
+    const int tile = p.form == kMlaWide ? kvp::MLA_TC_HEADS : kMlaHeadTile;
     p.head_tiles = (q_heads + tile - 1) / tile;
-    if (p.tc) {
-        // the units (latent half, head tile, sequence, block) are cut into one contiguous
+    if (p.form != kMlaMma) {
+        // the units ((latent half,) head tile, sequence, block) are cut into one contiguous
         // range per CTA; split_blocks is the least a range holds (the chunk argument, or
         // automatically about half the worst-case share of an SM, 4..16 blocks), so a
         // sequence of max_blocks blocks is cut into at most ceil((max_blocks - 1) /
         // split_blocks) + 1 pieces, each merged from its own partial
+        const int outer = p.head_tiles * (p.form == kMlaWide ? 2 : 1);
         if (split_tokens > 0) {
             p.split_blocks = split_tokens / pl->block_size;
         } else {
-            const long long units = static_cast<long long>(batch > 0 ? batch : 1) * p.head_tiles * 2 * max_blocks;
+            const long long units = static_cast<long long>(batch > 0 ? batch : 1) * outer * max_blocks;
             const long long share = units / (2LL * (pl->num_sms > 0 ? pl->num_sms : 148));
             p.split_blocks = static_cast<int>(share < 4 ? 4 : (share > 16 ? 16 : share));
         }
@@ -657,7 +667,7 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
         p.max_splits = (max_blocks - 1 + p.split_blocks - 1) / p.split_blocks + 1;
         if (p.max_splits > max_blocks) p.max_splits = max_blocks;
         // the partition's arithmetic: units x CTAs must stay far inside 64 bits
-        const long long units_max = static_cast<long long>(batch) * p.head_tiles * 2 * max_blocks;
+        const long long units_max = static_cast<long long>(batch) * outer * max_blocks;
         if (units_max > (1LL << 40)) return KV_ERR_UNSUPPORTED;
         if (p.max_splits > 65535 || p.head_tiles > 32767 || batch > 65535) return KV_ERR_UNSUPPORTED;
         *out = p;
@@ -687,7 +697,15 @@ kv_status make_mla_plan(const kv_pool* pl, int batch, int q_heads, int max_block
 WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
 {
     WorkspaceLayout w{0, 0, 0, 0, 0};
-    if (p.max_splits > 1 && p.tc) {
+    if (p.max_splits > 1 && p.form == kMlaNarrow) {
+        // pieces (sequence, head tile, split): fp32 partials of 16 heads x 512 latent
+        // numbers, (max, sum) per head, then the piece count of each (sequence, head tile)
+        const size_t pieces = static_cast<size_t>(batch) * p.head_tiles * p.max_splits;
+        w.part_ml = round_up(pieces * kvp::MLA_TCN_HEADS * kvp::MLA_DV * sizeof(float), kAlign);
+        w.tickets = w.part_ml + round_up(pieces * kvp::MLA_TCN_HEADS * 2 * sizeof(float), kAlign);
+        w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * sizeof(int);
+        w.total = w.tickets + w.ticket_bytes;
+    } else if (p.max_splits > 1 && p.form == kMlaWide) {
         // pieces (sequence, head tile, latent half, split): fp32 partials of 128 heads x
         // 256 latent numbers, (max, sum) per head, then the piece count of each
         // (sequence, head tile, half) -- read by the merge kernel
@@ -764,6 +782,7 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
     if (st == KV_OK && block_size == kvp::MLA_TC_BLOCK) {
         st = encode_pool_map(p, p->k, &p->tmt, block_size, 1);
         if (st == KV_OK && kvp::prepare_mla_decode_tc() != cudaSuccess) st = KV_ERR_CUDA;
+        if (st == KV_OK && kvp::prepare_mla_decode_tcn() != cudaSuccess) st = KV_ERR_CUDA;
         p->has_tc = 1;
     }
     if (st == KV_OK && kvp::prepare_mla_decode(block_size) != cudaSuccess) st = KV_ERR_CUDA;
@@ -841,18 +860,20 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (plan.tc) {
+    if (plan.form != kMlaMma) {
         // persistent: one CTA per SM, each taking a contiguous range of the units
-        // (latent half, head tile, sequence, block); no more CTAs than ranges of
+        // ((latent half,) head tile, sequence, block); no more CTAs than ranges of
         // split_blocks units the longest batch could have
-        const long long units_max = static_cast<long long>(plan.head_tiles) * 2 * batch * max_blocks;
+        const int outer = plan.head_tiles * (plan.form == kMlaWide ? 2 : 1);
+        const long long units_max = static_cast<long long>(outer) * batch * max_blocks;
         const long long ranges = units_max / plan.split_blocks > 0 ? units_max / plan.split_blocks : 1;
         const int sms = pool->num_sms > 0 ? pool->num_sms : 148;
         const dim3 grid(static_cast<unsigned>(ranges < sms ? ranges : sms));
-        return kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream)) ==
-                       cudaSuccess
-                   ? KV_OK
-                   : KV_ERR_CUDA;
+        const cudaError_t e =
+            plan.form == kMlaWide
+                ? kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream))
+                : kvp::launch_mla_decode_tcn(grid, pool->tmt, p, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
     }
     // chunk-major grid: x = head tile, y = sequence, z = chunk.  Grids of up to
     // three CTAs per SM run the producer-warp variant (32-token stages, two CTAs

@@ -4,17 +4,17 @@
 // get full-size keys and values back?": every head scores the shared cached
 // vector -- 512 latent + 64 rotary-key numbers -- and averages its latent part).
 //
-// Work item = (sequence, tile of 128 heads, half of the latent output, split
-// chunk).  The two halves of a chunk run on two CTAs that each compute the full
-// scores and one 256-wide half of the output: the fp32 output of 128 heads x 512
-// latent numbers alone would fill an SM's tensor memory.
+// A CTA computes one 256-wide half of the latent output of a tile of 128 heads, and
+// the full scores: the fp32 output of 128 heads x 512 latent numbers alone would fill
+// an SM's tensor memory.
 //
-// Persistent: one CTA per SM holds its tensor memory for the whole launch and
-// takes items from a counter in the workspace, first chunks first; the last CTA
-// to finish resets the counter.  320 threads:
-//   * warp 8 takes the next item, skips empty ones (chunks past a sequence's
-//     end), passes the item to the other roles through a 4-slot ring in shared
-//     memory, and streams the item's 64-token blocks, one per stage, with nine
+// Persistent: one CTA per SM holds its tensor memory for the whole launch and takes
+// one equal contiguous range of the units (latent half, head tile, sequence, block)
+// (mla_partition.cuh); a sequence cut by a range boundary leaves fp32 partials,
+// merged by paged_mla_merge_tc.  320 threads:
+//   * warp 8 walks the range's segments (item = a run of blocks of one sequence,
+//     head tile and half), passes each to the other roles through a 4-slot ring in
+//     shared memory, and streams its 64-token blocks, one per stage, with nine
 //     TMA loads (one per 128-byte piece of the 576 numbers, 128-byte swizzle):
 //     a stage is nine K-major [64 tokens x 64 numbers] tiles, 72 KB, 2 stages.
 //     The five pieces only the scores read (the other half's latent numbers and
@@ -50,6 +50,7 @@
 // frees its tensor memory before it exits.
 #include "decode_common.cuh"
 #include "kernels.h"
+#include "mla_partition.cuh"
 #include "tcgen05.cuh"
 
 namespace kvp {
@@ -261,159 +262,31 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 
     if (warp == 8) {
         // ------------------------------------------------------------ partition, items, loads
-        // Units: (half dq, head tile ht, sequence b, block) in that order, T in all;
-        // CTA c takes the contiguous range [c T / G, (c + 1) T / G) with G active
-        // CTAs chosen so that a range holds at least split_blocks units.  Every CTA
-        // derives the same partition from the context lengths.
-        const int cap = p.max_blocks * TC_TOK;
-        long long S = 0;                            // blocks of the batch
-        for (int b0 = 0; b0 < p.batch; b0 += 256) {
-            int raw[8];                             // eight lengths per lane in flight
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int b = b0 + i * 32 + lane;
-                raw[i] = b < p.batch ? __ldg(p.ctx + b) : 0;
-            }
-            int nbs = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int b = b0 + i * 32 + lane;
-                int ctx = raw[i];
-                if (b < p.batch && (ctx < 0 || ctx > cap)) {
-                    if (blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
-                    ctx = ctx < 0 ? 0 : cap;
-                }
-                const int nb = (ctx + TC_TOK - 1) / TC_TOK;
-                nbs += nb;
-                if (b < p.batch && nb == 0 && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
-                    // an empty sequence has no units: its output is 0 and its LSE -inf,
-                    // written by CTA b mod G
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(b) * p.q_heads * MLA_DV);
-                    for (int v = 0; v < p.q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
-                    if (p.lse != nullptr)
-                        for (int hh = 0; hh < p.q_heads; ++hh) p.lse[static_cast<size_t>(b) * p.q_heads + hh] = -INFINITY;
-                }
-            }
-            long long sum = nbs;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL_MASK, sum, o);
-            S += sum;
-        }
-        const int nouter = p.head_tiles * 2;
-        const long long T = S * nouter;
-        long long gact = T / p.split_blocks;
-        if (gact < 1) gact = 1;
-        if (gact > gridDim.x) gact = gridDim.x;
-        const long long c = blockIdx.x;
-        const long long u0 = c < gact ? c * T / gact : T;
-        const long long u1 = c < gact ? (c + 1) * T / gact : T;
-        // the sequence holding a unit: prefix sums of the block counts, 32 at a time
-        // (all lanes; u < T)
-        auto locate = [&](long long u, int& b_at, long long& pre_at) {
-            const long long v = u % S;
-            long long pre = 0;
-            b_at = 0;
-            pre_at = 0;
-            for (int b0 = 0; b0 < p.batch; b0 += 32) {
-                const int b = b0 + lane;
-                int nb = 0;
-                if (b < p.batch) {
-                    int ctx = __ldg(p.ctx + b);
-                    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-                    nb = (ctx + TC_TOK - 1) / TC_TOK;
-                }
-                int incl = nb;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(FULL_MASK, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const unsigned past = __ballot_sync(FULL_MASK, pre + incl > v);
-                if (past != 0u) {
-                    const int fl = __ffs(past) - 1;
-                    b_at = b0 + fl;
-                    pre_at = pre + __shfl_sync(FULL_MASK, incl, fl) - __shfl_sync(FULL_MASK, nb, fl);
-                    return;
-                }
-                pre += __shfl_sync(FULL_MASK, incl, 31);
-            }
-        };
-        int b_first = 0, b_last = 0;
-        long long pre_first = 0, pre_last = 0;
-        if (u0 < u1) {
-            locate(u0, b_first, pre_first);
-            locate(u1 - 1, b_last, pre_last);
-        }
+        // Units: (half dq, head tile ht, sequence b, block) in that order (outer index
+        // dq * head_tiles + ht), cut into equal contiguous ranges (mla_partition.cuh).
+        MlaPartition<TC_TOK> part;
+        part.init(p, p.head_tiles * 2, lane);
         if (lane == 0) {
             prefetch_tensormap(&tmp);
-            // the CTA whose range holds unit x
-            auto cta_of = [&](long long x) { return static_cast<int>(((x + 1) * gact - 1) / T); };
-            // the item for blocks blk .. blk + n - 1 of the sequence whose units start at ub
-            auto make_item = [&](int outer, int b, long long ub, int blk, int n, int ctx, int nb) {
-                TcItem it;
-                const int cf = cta_of(ub);
-                it.b = b;
-                it.dq = outer / p.head_tiles;
-                it.ht = outer - it.dq * p.head_tiles;
-                it.split = static_cast<int>(c) - cf;
-                it.nsplit = cta_of(ub + nb - 1) - cf + 1;
-                it.blk0 = blk;
-                it.n = n;
-                it.ctx = ctx;
-                return it;
-            };
-            auto seq_ctx = [&](int b) {
-                const int ctx = __ldg(p.ctx + b);
-                return ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-            };
             int k = 0;                              // items handed on
             int g = 0;                              // stages issued (all items)
             int ge = 0, gl = 0;                     // stages with score-only / output loads issued
             bool ok = true;
-            // Order: the range's last segment first, then the rest from the start.  A
-            // sequence cut between CTA c and c + 1 is then worked on first by both, and
-            // its merge (by the second to finish) overlaps their other work.
-            long long ls = u1;                      // start of the last segment
-            int outer_l = 0, ctx_l = 0, nb_l = 0;
-            long long ub_l = 0;
-            if (u0 < u1) {
-                outer_l = static_cast<int>((u1 - 1) / S);
-                ub_l = static_cast<long long>(outer_l) * S + pre_last;
-                ls = ub_l > u0 ? ub_l : u0;
-                ctx_l = seq_ctx(b_last);
-                nb_l = (ctx_l + TC_TOK - 1) / TC_TOK;
-            }
-            bool last_done = !(u0 < u1);
-            long long u = u0;
-            int outer = u0 < u1 ? static_cast<int>(u0 / S) : 0;
-            int b = b_first;
-            long long pre = pre_first;
-            int blk = u0 < u1 ? static_cast<int>(u0 % S - pre_first) : 0;
             for (;;) {
                 TcItem it{};
                 it.n = -1;
-                if (!last_done) {
-                    last_done = true;
-                    it = make_item(outer_l, b_last, ub_l, static_cast<int>(ls - ub_l), static_cast<int>(u1 - ls),
-                                   ctx_l, nb_l);
-                }
-                while (it.n < 0 && u < ls && !*abort_flag) {
-                    const int ctx = seq_ctx(b);
-                    const int nb = (ctx + TC_TOK - 1) / TC_TOK;
-                    if (blk >= nb) {                // next sequence (or next head tile / half)
-                        pre += nb;
-                        blk = 0;
-                        if (++b == p.batch) {
-                            b = 0;
-                            pre = 0;
-                            ++outer;
-                        }
-                        continue;
+                if (!*abort_flag) {
+                    const MlaSegment sg = part.next();
+                    it.n = sg.n;
+                    if (sg.n >= 0) {
+                        it.b = sg.b;
+                        it.dq = sg.outer / p.head_tiles;
+                        it.ht = sg.outer - it.dq * p.head_tiles;
+                        it.split = sg.split;
+                        it.nsplit = sg.nsplit;
+                        it.blk0 = sg.blk0;
+                        it.ctx = sg.ctx;
                     }
-                    const int n = static_cast<int>(nb - blk < ls - u ? nb - blk : ls - u);
-                    it = make_item(outer, b, static_cast<long long>(outer) * S + pre, blk, n, ctx, nb);
-                    u += n;
-                    blk += n;
                 }
                 const bool last = it.n < 0;
                 if (!last) {

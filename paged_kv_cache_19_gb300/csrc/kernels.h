@@ -141,6 +141,15 @@ constexpr int MLA_TC_BLOCK = 64;
 cudaError_t prepare_mla_decode_tc();
 cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
                                  cudaStream_t s);
+// The narrow tcgen05 form: tiles of 16 heads (rows of an M = 64 score MMA), blocks of 64
+// tokens, one CTA per SM taking an equal contiguous range of the (head tile, sequence,
+// block) units; cut sequences are merged by a second kernel when max_splits > 1.
+// Partials: part_o [piece][16 heads][MLA_DV], part_ml [piece][16 heads] (max, sum),
+// piece = (sequence, head tile, split); tickets [batch, head_tiles] piece counts.
+constexpr int MLA_TCN_HEADS = 16;
+cudaError_t prepare_mla_decode_tcn();
+cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
+                                  cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
                                cudaStream_t s);

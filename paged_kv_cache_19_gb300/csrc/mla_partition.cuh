@@ -1,0 +1,230 @@
+// mla_partition.cuh -- the balanced static partition of the latent-attention
+// work shared by the tcgen05 MLA kernels.
+//
+// Units are (outer, sequence b, block) in that order, T = S * nouter of them, S
+// being the blocks of the whole batch (a sequence of ctx tokens has
+// ceil(ctx / tok) blocks) and `outer` whatever the kernel splits the heads into
+// (head tiles, times the latent halves for the wide form).  CTA c of the G that
+// have work takes the contiguous range [c T / G, (c + 1) T / G), with G chosen
+// so that a range holds at least split_blocks units; every CTA derives the same
+// partition from the context lengths, so no CTA waits for another.  A sequence
+// cut by range boundaries leaves one piece per CTA that holds some of its
+// units: piece `split` of `nsplit`, merged afterwards by log-sum-exp.
+//
+// A CTA walks its range as segments (runs of blocks of one sequence and one
+// outer index), the last segment first: a sequence cut between CTA c and c + 1
+// is then worked on first by both, so the merge of its pieces does not wait for
+// the end of either range.
+#pragma once
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace kvp {
+
+// One segment: blocks blk0 .. blk0 + n - 1 of sequence b for outer index `outer`;
+// n < 0 marks the end of the range.
+struct MlaSegment {
+    int outer, b, blk0, n, ctx, split, nsplit;
+};
+
+template <int TOK>
+struct MlaPartition {
+    const MlaParams* p;
+    long long S, T, gact, u0, u1, c;
+    int cap;
+    // the cursor (lane 0 only after init)
+    long long u, ls, ub_l, pre;
+    int outer, b, blk, outer_l, b_last, ctx_l, nb_l;
+    bool last_done;
+
+    __device__ __forceinline__ int seq_ctx(int bb) const
+    {
+        const int x = __ldg(p->ctx + bb);
+        return x < 0 ? 0 : (x > cap ? cap : x);
+    }
+
+    // the CTA whose range holds unit x
+    __device__ __forceinline__ int cta_of(long long x) const { return static_cast<int>(((x + 1) * gact - 1) / T); }
+
+    // Warp-wide (all 32 lanes): block count of the batch, the range of this CTA and the
+    // sequences at its ends.  Out-of-range context lengths are flagged and clamped; an
+    // empty sequence has no units, so its output (0) and LSE (-inf) are written here, by
+    // CTA b mod gridDim.x.  Batches of up to 256 sequences keep their lengths and block
+    // prefix sums in registers (sequence 32 i + lane in slot i), so that the range ends
+    // are located without loading the lengths again.
+    __device__ void init(const MlaParams& params, int nouter, int lane)
+    {
+        p = &params;
+        cap = p->max_blocks * TOK;
+        S = 0;
+        int ctxv[8], nbv[8], incl[8];
+        for (int b0 = 0; b0 < p->batch; b0 += 256) {
+            int raw[8];                             // eight lengths per lane in flight
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int bb = b0 + i * 32 + lane;
+                raw[i] = bb < p->batch ? __ldg(p->ctx + bb) : 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int bb = b0 + i * 32 + lane;
+                int x = raw[i];
+                if (bb < p->batch && (x < 0 || x > cap)) {
+                    if (blockIdx.x == 0) atomicOr(p->err, KV_DEVERR_CONTEXT);
+                    x = x < 0 ? 0 : cap;
+                }
+                const int nb = (x + TOK - 1) / TOK;
+                if (bb < p->batch && nb == 0 && bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+                    uint4* dst = reinterpret_cast<uint4*>(p->out + static_cast<size_t>(bb) * p->q_heads * MLA_DV);
+                    for (int v = 0; v < p->q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (p->lse != nullptr)
+                        for (int hh = 0; hh < p->q_heads; ++hh) p->lse[static_cast<size_t>(bb) * p->q_heads + hh] = -INFINITY;
+                }
+                int in = nb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(FULL_MASK, in, o);
+                    if (lane >= o) in += y;
+                }
+                ctxv[i] = x;
+                nbv[i] = nb;
+                incl[i] = in;
+                S += __shfl_sync(FULL_MASK, in, 31);
+            }
+        }
+        T = S * nouter;
+        gact = T / p->split_blocks;
+        if (gact < 1) gact = 1;
+        if (gact > gridDim.x) gact = gridDim.x;
+        c = blockIdx.x;
+        u0 = c < gact ? c * T / gact : T;
+        u1 = c < gact ? (c + 1) * T / gact : T;
+        int b_first = 0;
+        long long pre_first = 0, pre_last = 0;
+        b_last = 0;
+        ctx_l = 0;
+        if (u0 < u1) {
+            if (p->batch <= 256) {
+                // both ends at once from the registers
+                const long long v0 = u0 % S, v1 = (u1 - 1) % S;
+                long long acc = 0;
+                bool f0 = false, f1 = false;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const unsigned p0 = __ballot_sync(FULL_MASK, acc + incl[i] > v0);
+                    const unsigned p1 = __ballot_sync(FULL_MASK, acc + incl[i] > v1);
+                    if (!f0 && p0 != 0u) {
+                        const int fl = __ffs(p0) - 1;
+                        b_first = i * 32 + fl;
+                        pre_first = acc + __shfl_sync(FULL_MASK, incl[i] - nbv[i], fl);
+                        f0 = true;
+                    }
+                    if (!f1 && p1 != 0u) {
+                        const int fl = __ffs(p1) - 1;
+                        b_last = i * 32 + fl;
+                        pre_last = acc + __shfl_sync(FULL_MASK, incl[i] - nbv[i], fl);
+                        ctx_l = __shfl_sync(FULL_MASK, ctxv[i], fl);
+                        f1 = true;
+                    }
+                    acc += __shfl_sync(FULL_MASK, incl[i], 31);
+                }
+            } else {
+                locate(u0, b_first, pre_first, lane);
+                locate(u1 - 1, b_last, pre_last, lane);
+                ctx_l = seq_ctx(b_last);
+            }
+        }
+        // cursor: the last segment first, then the rest of the range from its start
+        ls = u1;
+        outer_l = nb_l = 0;
+        ub_l = 0;
+        if (u0 < u1) {
+            outer_l = static_cast<int>((u1 - 1) / S);
+            ub_l = static_cast<long long>(outer_l) * S + pre_last;
+            ls = ub_l > u0 ? ub_l : u0;
+            nb_l = (ctx_l + TOK - 1) / TOK;
+        }
+        last_done = !(u0 < u1);
+        u = u0;
+        outer = u0 < u1 ? static_cast<int>(u0 / S) : 0;
+        b = b_first;
+        pre = pre_first;
+        blk = u0 < u1 ? static_cast<int>(u0 % S - pre_first) : 0;
+    }
+
+    // Warp-wide: the sequence holding unit x < T, and the number of blocks before it
+    // (prefix sums of the block counts, 32 sequences at a time).
+    __device__ void locate(long long x, int& b_at, long long& pre_at, int lane) const
+    {
+        const long long v = x % S;
+        long long acc = 0;
+        b_at = 0;
+        pre_at = 0;
+        for (int b0 = 0; b0 < p->batch; b0 += 32) {
+            const int bb = b0 + lane;
+            const int nb = bb < p->batch ? (seq_ctx(bb) + TOK - 1) / TOK : 0;
+            int in = nb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL_MASK, in, o);
+                if (lane >= o) in += y;
+            }
+            const unsigned past = __ballot_sync(FULL_MASK, acc + in > v);
+            if (past != 0u) {
+                const int fl = __ffs(past) - 1;
+                b_at = b0 + fl;
+                pre_at = acc + __shfl_sync(FULL_MASK, in, fl) - __shfl_sync(FULL_MASK, nb, fl);
+                return;
+            }
+            acc += __shfl_sync(FULL_MASK, in, 31);
+        }
+    }
+
+    __device__ __forceinline__ MlaSegment make(int o, int bb, long long ub, int blk0, int n, int x, int nb) const
+    {
+        MlaSegment it;
+        const int cf = cta_of(ub);
+        it.outer = o;
+        it.b = bb;
+        it.blk0 = blk0;
+        it.n = n;
+        it.ctx = x;
+        it.split = static_cast<int>(c) - cf;
+        it.nsplit = cta_of(ub + nb - 1) - cf + 1;
+        return it;
+    }
+
+    // One thread: the next segment of the range (n < 0: none left).
+    __device__ MlaSegment next()
+    {
+        MlaSegment it{};
+        it.n = -1;
+        if (!last_done) {
+            last_done = true;
+            return make(outer_l, b_last, ub_l, static_cast<int>(ls - ub_l), static_cast<int>(u1 - ls), ctx_l, nb_l);
+        }
+        while (u < ls) {
+            const int x = seq_ctx(b);
+            const int nb = (x + TOK - 1) / TOK;
+            if (blk >= nb) {                        // next sequence (or next outer index)
+                pre += nb;
+                blk = 0;
+                if (++b == p->batch) {
+                    b = 0;
+                    pre = 0;
+                    ++outer;
+                }
+                continue;
+            }
+            const int n = static_cast<int>(nb - blk < ls - u ? nb - blk : ls - u);
+            it = make(outer, b, static_cast<long long>(outer) * S + pre, blk, n, x, nb);
+            u += n;
+            blk += n;
+            return it;
+        }
+        return it;
+    }
+};
+
+}  // namespace kvp

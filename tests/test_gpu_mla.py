@@ -32,13 +32,20 @@ SMALL = {
                              seed=209, split_tokens=64),
     "bs32_h64_many_ctas": M(batch=24, q_heads=64, block_size=32, ctx_uniform=(1, 400),
                             seed=210, split_tokens=64),
-    # blocks of 64 and at least 64 heads run the tcgen05 form (128-head tiles, latent quarters)
+    # blocks of 64 and at least 64 heads run the wide tcgen05 form (128-head tiles, latent halves)
     "tc_h128_split128": M(batch=4, q_heads=128, block_size=64, ctx=[1, 64, 65, 700], seed=211,
                           split_tokens=128),
     "tc_h96_padded_tile": M(batch=3, q_heads=96, block_size=64, ctx=[63, 200, 1000], seed=212),
     "tc_h256_two_tiles": M(batch=2, q_heads=256, block_size=64, ctx=[130, 900], seed=213,
                            split_tokens=256),
     "tc_h64_long": M(batch=2, q_heads=64, block_size=64, ctx=[5000, 3], seed=214),
+    # blocks of 64 and fewer heads run the narrow tcgen05 form (16-head tiles); these cut
+    # many sequences into pieces and give CTAs several segments
+    "tcn_h16_many_segments": M(batch=10, q_heads=16, block_size=64, ctx_uniform=(1, 1500), seed=215,
+                               split_tokens=64),
+    "tcn_h48_three_tiles": M(batch=3, q_heads=48, block_size=64, ctx=[65, 640, 3000], seed=216,
+                             split_tokens=128),
+    "tcn_h8_partial_tile": M(batch=4, q_heads=8, block_size=64, ctx=[1, 2, 4000, 127], seed=217),
 }
 
 
@@ -94,7 +101,7 @@ def test_repeated_calls_are_identical(staged):
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
-@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128)])
+@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128), (64, 16)])
 def test_empty_sequence_and_out_of_range_length(bs, heads):
     w = workloads.make(M(batch=2, q_heads=heads, block_size=bs, ctx=[40, 20], seed=207))
     st = Staged(w)
@@ -113,7 +120,7 @@ def test_empty_sequence_and_out_of_range_length(bs, heads):
     st.destroy()
 
 
-@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128)])
+@pytest.mark.parametrize("bs,heads", [(16, 16), (64, 128), (64, 16)])
 def test_bad_block_ids_are_skipped_and_flagged(bs, heads):
     w = workloads.make(M(batch=2, q_heads=heads, block_size=bs, ctx=[150, 150], seed=208))
     st = Staged(w)

@@ -66,10 +66,10 @@ def test_decode_bytes_counts_kv_and_partials():
     assert many["partials"] == 4 * 8 * (64 + 2) * 4 * 2
 
 
-def _brute_force_pieces(nb, tiles, split_blocks, grid):
+def _brute_force_pieces(nb, tiles, split_blocks, grid, halves=2):
     """Assign every unit (latent half / head tile, sequence, block) to its range by
     scanning the range starts, then count the distinct ranges each sequence touches."""
-    units = [(outer, b) for outer in range(tiles * 2) for b, n in enumerate(nb) for _ in range(n)]
+    units = [(outer, b) for outer in range(tiles * halves) for b, n in enumerate(nb) for _ in range(n)]
     T = len(units)
     g = max(1, min(grid, T // split_blocks))
     starts = [c * T // g for c in range(g + 1)]
@@ -83,7 +83,7 @@ def _brute_force_pieces(nb, tiles, split_blocks, grid):
     seen = {}
     for (key, c) in zip(units, owner):
         seen.setdefault(key, set()).add(c)
-    pieces = [len(seen[(outer, b)]) for outer in range(tiles * 2) for b, n in enumerate(nb) if n > 0]
+    pieces = [len(seen[(outer, b)]) for outer in range(tiles * halves) for b, n in enumerate(nb) if n > 0]
     return pieces, sizes, g
 
 
@@ -101,6 +101,24 @@ def test_mla_tc_pieces_match_a_brute_force_partition(ctx, heads, split_blocks, g
     assert list(got) == want
     # every range but a lone one holds at least split_blocks units, and no sequence is cut
     # into more pieces than the workspace bound ceil((max_blocks - 1) / split_blocks) + 1
+    if g > 1:
+        assert min(sizes) >= split_blocks
+    assert max(want) <= (max(nb) - 1 + split_blocks - 1) // split_blocks + 1
+
+
+@pytest.mark.parametrize("ctx,heads,split_blocks,grid", [
+    ([1, 70, 300, 2, 4096, 65], 16, 1, 152),
+    ([640, 64, 3000, 129, 2000], 40, 13, 7),
+    ([100] * 40, 16, 4, 33),
+    ([5000, 1], 48, 8, 152),
+])
+def test_mla_narrow_pieces_match_a_brute_force_partition(ctx, heads, split_blocks, grid):
+    """The narrow tensor-core form: units (head tile of 16, sequence, block), no halves."""
+    w = workloads.make(workloads.mla(batch=len(ctx), q_heads=heads, block_size=64, ctx=ctx, seed=3))
+    nb = [-(-c // 64) for c in ctx]
+    want, sizes, g = _brute_force_pieces(nb, -(-heads // 16), split_blocks, grid, halves=1)
+    got = accounting.mla_tc_pieces(w, split_blocks, grid, head_tile=16, halves=1)
+    assert list(got) == want
     if g > 1:
         assert min(sizes) >= split_blocks
     assert max(want) <= (max(nb) - 1 + split_blocks - 1) // split_blocks + 1

@@ -82,22 +82,23 @@ def decode_flops(w) -> int:
     return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads * s.q_len)
 
 
-def mla_tc_pieces(w, split_blocks: int, grid: int) -> np.ndarray:
-    """Pieces each (latent half, head tile, sequence) is cut into by the tensor-core MLA
-    decode's partition: its units (half, head tile, sequence, block), T in all, are cut
-    into G = min(grid, T // split_blocks) (at least 1) equal contiguous ranges, range c =
-    [c T / G, (c + 1) T / G); a sequence with blocks is cut at every range boundary
-    inside it.  Same integer arithmetic as the kernel."""
+def mla_tc_pieces(w, split_blocks: int, grid: int, head_tile: int = 128, halves: int = 2) -> np.ndarray:
+    """Pieces each (outer, sequence) is cut into by a tensor-core MLA decode's partition:
+    its units (outer, sequence, block) -- outer = (latent half, head tile) for the wide
+    form (tiles of 128 heads, two halves), the head tile for the narrow one (tiles of 16,
+    halves=1) -- T in all, are cut into G = min(grid, T // split_blocks) (at least 1) equal
+    contiguous ranges, range c = [c T / G, (c + 1) T / G); a sequence with blocks is cut at
+    every range boundary inside it.  Same integer arithmetic as the kernels."""
     nb = _nb(w)
-    tiles = -(-w.spec.q_heads // 128)
+    tiles = -(-w.spec.q_heads // head_tile)
     S = int(nb.sum())
-    T = S * tiles * 2
+    T = S * tiles * halves
     if T == 0:
         return np.zeros(0, dtype=np.int64)
     g = max(1, min(grid, T // max(1, split_blocks)))
     pre = np.concatenate([[0], np.cumsum(nb)[:-1]]).astype(np.int64)
     out = []
-    for outer in range(tiles * 2):
+    for outer in range(tiles * halves):
         ub = outer * S + pre
         for u, n in zip(ub, nb):
             if n == 0:
@@ -108,16 +109,18 @@ def mla_tc_pieces(w, split_blocks: int, grid: int) -> np.ndarray:
     return np.array(out, dtype=np.int64)
 
 
-def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0) -> dict:
+def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0,
+                     form: str = "wide") -> dict:
     """Algorithmic bytes of one paged_mla_decode_attention call: every cached vector once
     (kv), the absorbed queries, the latent outputs, tables, lengths, LSE and the split
-    partials.  l2_reads: vector bytes read by all head tiles (each tile of 16 heads
-    reads the sequence's vectors; the copies after the first come from L2).
+    partials.  l2_reads: vector bytes read by all head tiles (each tile reads the
+    sequence's vectors; the copies after the first come from L2).
 
-    tc_grid > 0: the tensor-core form with that many CTAs -- tiles of 128 heads, two
-    latent halves each reading every vector, and pieces from mla_tc_pieces (each piece
-    of a cut sequence writes and the merge reads 128 heads x 256 fp32 numbers and a
-    (max, sum) pair per head)."""
+    tc_grid > 0: a tensor-core form with that many CTAs and pieces from mla_tc_pieces --
+    form "wide": tiles of 128 heads, two latent halves each reading every vector, each
+    piece of a cut sequence writing (and the merge reading) 128 heads x 256 fp32 numbers
+    and a (max, sum) pair per head; form "narrow": tiles of 16 heads, 16 x 512 numbers
+    and 16 pairs per piece."""
     s = w.spec
     ctx = w.context_lens.astype(np.int64)
     nb = _nb(w)
@@ -125,10 +128,14 @@ def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0
     rows = w.batch * s.q_heads
     qo = rows * (s.head_dim + s.latent_dim) * 2
     meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * rows
-    if tc_grid > 0:
+    if tc_grid > 0 and form == "wide":
         tiles = -(-s.q_heads // 128) * 2
         pieces = mla_tc_pieces(w, max(1, split_tokens // s.block_size), tc_grid)
         partial = int(pieces[pieces > 1].sum()) * 128 * ((s.latent_dim // 2) * 4 + 8) * 2
+    elif tc_grid > 0:
+        tiles = -(-s.q_heads // 16)
+        pieces = mla_tc_pieces(w, max(1, split_tokens // s.block_size), tc_grid, 16, 1)
+        partial = int(pieces[pieces > 1].sum()) * 16 * (s.latent_dim * 4 + 8) * 2
     else:
         tiles = -(-s.q_heads // head_tile)
         sb = max(1, split_tokens // s.block_size)
