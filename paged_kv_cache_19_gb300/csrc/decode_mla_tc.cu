@@ -28,9 +28,10 @@
 //     in shared memory.  Then O[128 heads x 256 latent] += P . C[:, half]: A =
 //     the probabilities in tensor memory, B = the four output pieces read
 //     MN-major (the latent numbers of a token are contiguous), 4 MMAs of N =
-//     256.  Completion is signalled by tcgen05.commit on mbarriers.  The scores
-//     of stage i+1 are computed while the softmax of stage i runs, and the
-//     output update of stage i while the softmax of stage i+1 runs.
+//     256.  Completion is signalled by tcgen05.commit on mbarriers.  A fixed
+//     order with blocking waits: the score-only MMAs of stage i+1 run while the
+//     softmax of stage i does, then the other score MMAs of stage i+1 with the
+//     output update of stage i spread among them.
 //   * warps 0-7: head h (tensor-memory lane h) belongs to two threads, one in
 //     warp h / 32 (tokens 0-31 of a stage, output columns 0-127) and one in warp
 //     h / 32 + 4 (tokens 32-63, columns 128-255) -- a warp can only reach its
@@ -111,51 +112,6 @@ struct TcCtl {
     float xl[2][TC_M];                              // [token half][head]
 };
 static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
-
-// L2 prefetch of `bytes` (a multiple of 16) contiguous bytes of global memory.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
-
-// Non-blocking probe of an mbarrier phase (test_wait never suspends the thread).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// L2 prefetch of one TMA box (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
-
-// Named barrier that also returns, to every participant, the OR of their `pred`.
-__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
 
 // Scores over the five score-only pieces: 20 MMAs of K = 16 with A = the queries'
 // matching numbers in tensor memory.  The descriptor of slice ks is the stage's
@@ -392,59 +348,34 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     const uint32_t ph = static_cast<uint32_t>(gs / TC_NSTAGE) & 1u;
                     const uint32_t stage_addr = smem_u32(smem + st * TC_STAGE);
                     ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_e[st]), ph);
-                    if (ok && gs >= 1) {
-                        // the score buffer frees right after the softmax has read it: poll
-                        // (test_wait does not suspend the thread)
-                        const uint32_t sf = smem_u32(&ctl->s_free), sp = static_cast<uint32_t>(gs - 1) & 1u;
-                        const unsigned long long t0 = global_timer_ns();
-                        for (uint32_t spin = 0; !mbar_test(sf, sp); ++spin)
-                            if ((spin & 63u) == 63u && global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-                                ok = false;
-                                break;
-                            }
-                    }
+                    // the score buffer is free once the softmax has read the stage before
+                    if (ok && gs >= 1) ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(gs - 1) & 1u);
                     if (!ok || *abort_flag) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue_score_early(tbase, stage_addr);
-                    // then, in whichever order their inputs are ready: the previous stage's
-                    // output update (its probabilities) and the scores over the output
-                    // pieces (their loads, issued once that previous update had finished
-                    // with the slot two stages back)
-                    bool o_todo = s >= 1, l_todo = true;
-                    const unsigned long long t0 = global_timer_ns();
-                    for (uint32_t spin = 0; ok && (o_todo || l_todo); ++spin) {
-                        if (o_todo && l_todo && mbar_test(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u) &&
-                            mbar_test(smem_u32(&ctl->kv_full_l[st]), ph)) {
-                            tc_fence_after();
-                            issue_score_late_and_output(tbase, stage_addr, q_addr,
-                                                        smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), s == 1);
-                            tc_commit(smem_u32(&ctl->s_full));
-                            tc_commit(smem_u32(&ctl->kv_empty_e[st]));
-                            tc_commit(smem_u32(&ctl->p_free));
-                            tc_commit(smem_u32(&ctl->kv_empty_l[(gs - 1) % TC_NSTAGE]));
-                            o_todo = l_todo = false;
-                            continue;
-                        }
-                        if (o_todo && mbar_test(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u)) {
-                            tc_fence_after();
-                            issue_output_mma(tbase, smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), s == 1);
-                            tc_commit(smem_u32(&ctl->p_free));
-                            tc_commit(smem_u32(&ctl->kv_empty_l[(gs - 1) % TC_NSTAGE]));
-                            o_todo = false;
-                            continue;
-                        }
-                        if (l_todo && mbar_test(smem_u32(&ctl->kv_full_l[st]), ph)) {
-                            tc_fence_after();
-                            issue_score_late(tbase, stage_addr, q_addr);
-                            tc_commit(smem_u32(&ctl->s_full));
-                            tc_commit(smem_u32(&ctl->kv_empty_e[st]));
-                            l_todo = false;
-                            continue;
-                        }
-                        if ((spin & 63u) == 63u && global_timer_ns() - t0 > WAIT_LIMIT_NS) ok = false;
+                    // then the scores over the output pieces (their loads, issued once the
+                    // previous update had finished with the slot two stages back) with the
+                    // previous stage's output update spread among them; both waits block
+                    // (try_wait) rather than poll
+                    if (s >= 1)
+                        ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u);
+                    if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_l[st]), ph);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (s >= 1) {
+                        issue_score_late_and_output(tbase, stage_addr, q_addr,
+                                                    smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), s == 1);
+                        tc_commit(smem_u32(&ctl->s_full));
+                        tc_commit(smem_u32(&ctl->kv_empty_e[st]));
+                        tc_commit(smem_u32(&ctl->p_free));
+                        tc_commit(smem_u32(&ctl->kv_empty_l[(gs - 1) % TC_NSTAGE]));
+                    } else {
+                        issue_score_late(tbase, stage_addr, q_addr);
+                        tc_commit(smem_u32(&ctl->s_full));
+                        tc_commit(smem_u32(&ctl->kv_empty_e[st]));
                     }
                 }
                 if (ok && n >= 1) {

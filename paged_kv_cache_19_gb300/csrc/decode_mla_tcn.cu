@@ -104,26 +104,6 @@ struct TnCtl {
 };
 static_assert(sizeof(TnCtl) <= TN_CTL, "control block");
 
-__device__ __forceinline__ bool all_ok(bool ok) { return __all_sync(FULL_MASK, ok); }
-
-__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
-
 // One score MMA of S[128 x 64] = Q . C^T (rows 0-15 are the heads), slice ks of the 36
 // (16 numbers each): slices 0-31 are the latent numbers, A = the queries in tensor memory
 // (8 columns per slice), slices 32-35 the rotary key, A = the rotary queries in shared
