@@ -493,17 +493,15 @@ def run_ours(args, rank, world, local):
             kp.paged_attention_multi_query(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
                                            workspace=workspace, out=out, lse=lse, stream=stream)
 
-    def append(kk, vv, tt, cc, sq, ps):
-        kp.paged_kv_append(pool, kk, vv, tt, cc, token_seq=sq, token_pos=ps, stream=stream)
-
     def run_step(kk, vv, qq, tt, cc, sq, ps):
-        """One decode step through the public API: paged_decode_step (append + attention in
-        one call, the attention overlapping the append) for K/V caches -- the step's tokens
-        are the last q_len of every sequence, in sequence order, which is its layout -- and
-        append then attention for latent pools."""
+        """One decode step through the public API: append + attention in one call, the
+        attention overlapping the append -- paged_decode_step for K/V caches,
+        paged_mla_decode_step for latent pools.  The step's tokens are the last q_len of
+        every sequence, in sequence order, which is the layout both calls take."""
         if s.mla:
-            append(kk, vv, tt, cc, sq, ps)
-            attend(qq, tt, cc)
+            kp.paged_mla_decode_step(pool, kk, qq, tt, cc, w.scale, kv_split_tokens=split_req,
+                                     workspace=workspace, out=out, lse=lse, stream=stream,
+                                     latent_dim=s.latent_dim)
         else:
             kp.paged_decode_step(pool, kk, vv, qq, tt, cc, w.scale, kv_split_tokens=split_req,
                                  workspace=workspace, out=out, lse=lse, stream=stream)

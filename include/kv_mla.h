@@ -95,6 +95,22 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
                                      int kv_split_tokens, void* workspace, size_t workspace_bytes,
                                      void* out, float* lse, void* stream);
 
+/*
+ * One decode step over a latent pool in one call: append each sequence's new cached
+ * vector at position context_lens[b] - 1 (as paged_kv_append with token i = sequence i
+ * and no V half), then paged_mla_decode_attention.  The attention kernel starts while
+ * the append runs and waits for it only before loading the block that holds the new
+ * vector.  Results are bit-identical to the two separate calls.
+ *   kv_new: bf16 [batch, 576], 16-byte aligned (512 latent + 64 rotary-key numbers).
+ *   Every other argument as for paged_mla_decode_attention.  All arguments are checked
+ *   before anything is launched; on an error nothing is appended.
+ */
+kv_status paged_mla_decode_step(kv_pool* pool, const void* kv_new, const void* q, int q_heads,
+                                const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, int batch, float scale,
+                                int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

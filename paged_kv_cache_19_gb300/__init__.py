@@ -22,6 +22,7 @@ __all__ = [
     "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
     "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING", "kv_mla_pool_create",
     "paged_mla_decode_plan", "paged_mla_workspace_size", "paged_mla_decode_attention",
+    "paged_mla_decode_step",
     "DEVERR_BLOCK_ID", "DEVERR_CONTEXT", "DEVERR_SEQ", "DEVERR_POSITION", "DEVERR_TIMEOUT",
 ]
 
@@ -111,6 +112,7 @@ def load_library():
             "paged_mla_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_mla_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
                                             P], I),
+            "paged_mla_decode_step": ([P, P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -558,4 +560,35 @@ def paged_mla_decode_attention(pool: Pool, q, block_tables, context_lens, scale:
                                           float(scale), int(kv_split_tokens), _ptr(workspace),
                                           int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
            "paged_mla_decode_attention")
+    return out
+
+
+def paged_mla_decode_step(pool: Pool, kv_new, q, block_tables, context_lens, scale: float,
+                          kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
+                          stream=None, latent_dim: int = 512):
+    """One step over a latent pool: append kv_new bf16 [B, latent + rope] at position
+    context_lens[b] - 1 of each sequence, then the absorbed MLA decode (one call, the
+    attention overlapping the append).  Returns out bf16 [B, Hq, latent]."""
+    lib = load_library()
+    _need(kv_new, torch.bfloat16, "kv_new")
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    batch, q_heads = q.shape[0], q.shape[1]
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty(batch, q_heads, latent_dim, dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if workspace is None:
+        need = paged_mla_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
+        workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_mla_decode_step(pool.handle, _ptr(kv_new), _ptr(q), int(q_heads),
+                                     _ptr(block_tables), int(max_blocks), _ptr(context_lens),
+                                     int(batch), float(scale), int(kv_split_tokens),
+                                     _ptr(workspace), int(ws_bytes), _ptr(out), _ptr(lse),
+                                     _stream(stream)),
+           "paged_mla_decode_step")
     return out

@@ -819,11 +819,15 @@ kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, 
     return KV_OK;
 }
 
-kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_heads,
-                                     const int32_t* block_tables, int max_blocks,
-                                     const int32_t* context_lens, int batch, float scale,
-                                     int kv_split_tokens, void* workspace, size_t workspace_bytes,
-                                     void* out, float* lse_out, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Everything paged_mla_decode_attention checks and sets up before its launch.
+kv_status make_mla_launch(const kv_pool* pool, const void* q, int q_heads, const int32_t* block_tables,
+                          int max_blocks, const int32_t* context_lens, int batch, float scale,
+                          int kv_split_tokens, void* workspace, size_t workspace_bytes, void* out,
+                          float* lse_out, MlaPlan* plan_out, kvp::MlaParams* params)
 {
     MlaPlan plan;
     kv_status st = make_mla_plan(pool, batch, q_heads, max_blocks, kv_split_tokens, &plan);
@@ -841,7 +845,7 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     st = check_device(pool);
     if (st != KV_OK) return st;
 
-    kvp::MlaParams p;
+    kvp::MlaParams& p = *params;
     p.q = static_cast<const uint16_t*>(q);
     p.tables = block_tables;
     p.ctx = context_lens;
@@ -860,12 +864,19 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.dep_tail = 0;
+    *plan_out = plan;
+    return KV_OK;
+}
+
+kv_status launch_mla(const kv_pool* pool, const MlaPlan& plan, const kvp::MlaParams& p, void* stream)
+{
     if (plan.form != kMlaMma) {
         // persistent: one CTA per SM, each taking a contiguous range of the units
         // ((latent half,) head tile, sequence, block); no more CTAs than ranges of
         // split_blocks units the longest batch could have
         const int outer = plan.head_tiles * (plan.form == kMlaWide ? 2 : 1);
-        const long long units_max = static_cast<long long>(outer) * batch * max_blocks;
+        const long long units_max = static_cast<long long>(outer) * p.batch * p.max_blocks;
         const long long ranges = units_max / plan.split_blocks > 0 ? units_max / plan.split_blocks : 1;
         const int sms = pool->num_sms > 0 ? pool->num_sms : 148;
         const dim3 grid(static_cast<unsigned>(ranges < sms ? ranges : sms));
@@ -878,14 +889,73 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
     // chunk-major grid: x = head tile, y = sequence, z = chunk.  Grids of up to
     // three CTAs per SM run the producer-warp variant (32-token stages, two CTAs
     // per SM), larger ones the three-CTAs-per-SM variant (16-token stages).
-    const dim3 grid(static_cast<unsigned>(plan.head_tiles), static_cast<unsigned>(batch),
+    const dim3 grid(static_cast<unsigned>(plan.head_tiles), static_cast<unsigned>(p.batch),
                     static_cast<unsigned>(plan.max_splits));
-    const long long ctas = static_cast<long long>(plan.head_tiles) * batch * plan.max_splits;
+    const long long ctas = static_cast<long long>(plan.head_tiles) * p.batch * plan.max_splits;
     const bool prod = ctas <= 3LL * (pool->num_sms > 0 ? pool->num_sms : 148);
     return kvp::launch_mla_decode(pool->block_size, prod, grid, prod ? pool->tmk : pool->tmv, p,
                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KV_OK
                : KV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_heads,
+                                     const int32_t* block_tables, int max_blocks,
+                                     const int32_t* context_lens, int batch, float scale,
+                                     int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                     void* out, float* lse_out, void* stream)
+{
+    MlaPlan plan;
+    kvp::MlaParams p;
+    kv_status st = make_mla_launch(pool, q, q_heads, block_tables, max_blocks, context_lens, batch, scale,
+                                   kv_split_tokens, workspace, workspace_bytes, out, lse_out, &plan, &p);
+    if (st != KV_OK || batch == 0) return st;
+    return launch_mla(pool, plan, p, stream);
+}
+
+kv_status paged_mla_decode_step(kv_pool* pool, const void* kv_new, const void* q, int q_heads,
+                                const int32_t* block_tables, int max_blocks,
+                                const int32_t* context_lens, int batch, float scale,
+                                int kv_split_tokens, void* workspace, size_t workspace_bytes,
+                                void* out, float* lse_out, void* stream)
+{
+    if (pool == nullptr) return KV_ERR_INVALID_ARG;
+    // everything is checked before anything is launched
+    MlaPlan plan;
+    kvp::MlaParams p;
+    kv_status st = make_mla_launch(pool, q, q_heads, block_tables, max_blocks, context_lens, batch, scale,
+                                   kv_split_tokens, workspace, workspace_bytes, out, lse_out, &plan, &p);
+    if (st != KV_OK || batch == 0) return st;
+    if (kv_new == nullptr || !aligned(kv_new, 16)) return KV_ERR_INVALID_ARG;
+    kvp::AppendParams a;
+    a.k_new = static_cast<const uint16_t*>(kv_new);
+    a.v_new = nullptr;
+    a.token_seq = nullptr;
+    a.token_pos = nullptr;
+    a.tables = block_tables;
+    a.ctx = context_lens;
+    a.k_pool = pool->k;
+    a.v_pool = nullptr;
+    a.k_scale = pool->k_scale;
+    a.v_scale = pool->v_scale;
+    a.err = pool->err;
+    a.num_tokens = batch;
+    a.batch = batch;
+    a.max_blocks = max_blocks;
+    a.num_blocks = pool->num_blocks;
+    a.block_size = pool->block_size;
+    a.kv_heads = pool->kv_heads;
+    a.head_dim = pool->head_dim;
+    a.fp8 = false;
+    a.q_len = 1;
+    if (kvp::launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
+    // the append wrote only the last position of each sequence
+    p.dep_tail = 1;
+    return launch_mla(pool, plan, p, stream);
 }
 
 }  // extern "C"

@@ -91,10 +91,15 @@ __device__ __forceinline__ uint32_t swz_off(int tok, int ch)
 template <class C, int SUB, int NSTAGE>
 __device__ __forceinline__ void issue_stage(int it, const int32_t* trow, int num_blocks,
                                             uint8_t* smem, uint64_t* full, int* stage_blk,
-                                            const CUtensorMap* tmc, uint32_t* err)
+                                            const CUtensorMap* tmc, uint32_t* err, int tail_j,
+                                            bool& waited)
 {
     const int j = it / C::SPB;
     const int sub = it - j * C::SPB;
+    if (!waited && j >= tail_j) {                  // a block the preceding append wrote to
+        grid_dependency_wait();
+        waited = true;
+    }
     int blk = __ldg(trow + j);
     if (blk < 0 || blk >= num_blocks) {
         atomicOr(err, KV_DEVERR_BLOCK_ID);
@@ -145,7 +150,9 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         flags[0] = 0;
         fence_mbar_init();
     }
-    grid_dependency_wait();
+    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
+    // positions of each sequence: then the loads of the blocks that hold them wait.
+    if (p.dep_tail == 0) grid_dependency_wait();
 
     const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
     int id_first = -1;
@@ -173,6 +180,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         ctx = ctx < 0 ? 0 : cap;
     }
     const int nblk = (ctx + BS - 1) / BS;
+    const int tail_blk = (ctx - p.dep_tail) / BS;   // first block the preceding append wrote
     const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
     const int nb = max(0, min(nblk - blk0, p.split_blocks));
     const int nstages = nb * C::SPB;
@@ -187,6 +195,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         if (lane == 0) prefetch_tensormap(&tmc);
         int issued = 0;
         bool ok = true;
+        bool waited = p.dep_tail == 0;
         for (int base = 0; base < nb && ok; base += 32) {
             const int j = base + lane;
             int id = -1;
@@ -207,6 +216,10 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                     const uint32_t ph = static_cast<uint32_t>(it / NSTAGE) & 1u;
                     int good = 1;
                     if (lane == 0) {
+                        if (!waited && blk0 + base + k >= tail_blk) {
+                            grid_dependency_wait();
+                            waited = true;
+                        }
                         if (!mbar_wait_bounded(smem_u32(empty + st), ph ^ 1u)) {
                             atomicOr(p.err, KV_DEVERR_TIMEOUT);
                             good = 0;
@@ -246,11 +259,12 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 
     // ------------------------------------------------------------ consumer warps
     int issued = 0;                                  // thread 0 (not PROD): loads issued
+    bool dep_waited = p.dep_tail == 0;               // thread 0 (not PROD): waited for the append
     if (!PROD && threadIdx.x == 0) {
         prefetch_tensormap(&tmc);
         for (; issued < min(NSTAGE, nstages); ++issued)
             issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
-                                        p.err);
+                                        p.err, tail_blk - blk0, dep_waited);
     }
 
     MlaState st;
@@ -328,7 +342,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         if (flags[0]) break;                        // a stage never arrived: all warps leave
         if (!PROD && threadIdx.x == 0 && it >= 1 && issued < nstages) {
             issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
-                                        p.err);   // into the slot of stage it - 1
+                                        p.err, tail_blk - blk0, dep_waited);   // into the slot of stage it - 1
             ++issued;
         }
         if (blk < 0) {                              // skipped (bad id): nothing to fold in

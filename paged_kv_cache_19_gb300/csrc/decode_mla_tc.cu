@@ -210,7 +210,10 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         fence_mbar_init();
     }
     if (warp == 9) tc_alloc(smem_u32(&ctl->tmem_base), TM_COLS);
-    grid_dependency_wait();
+    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
+    // positions of each sequence: then the producer waits, before the first load of a block
+    // that holds one of them.
+    if (p.dep_tail == 0) grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -228,6 +231,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             int g = 0;                              // stages issued (all items)
             int ge = 0, gl = 0;                     // stages with score-only / output loads issued
             bool ok = true;
+            bool waited = p.dep_tail == 0;
             for (;;) {
                 TcItem it{};
                 it.n = -1;
@@ -278,6 +282,10 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty_e[st]), ph) || *abort_flag) {
                         ok = false;
                         break;
+                    }
+                    if (!waited && it.blk0 + s >= (it.ctx - p.dep_tail) / TC_TOK) {
+                        grid_dependency_wait();
+                        waited = true;
                     }
                     const uint32_t fe = smem_u32(&ctl->kv_full_e[st]);
                     if (bid >= 0) {

@@ -11,7 +11,8 @@
 // are chosen for few instructions per token:
 //   * scores S[16 heads x 64 tokens] = Q . C^T: an M = 128 MMA whose rows 0-15
 //     (tensor-memory lanes 0-15) are the tile's heads, the other rows never read --
-//     A = the queries in tensor memory, B = the stage's nine K-major pieces -- 36
+//     A = the queries (latent part in tensor memory, rotary part in shared memory),
+//     B = the stage's nine K-major pieces -- 36
 //     MMAs of K = 16 per block.  (An M = 64 form costs the same per MMA, but
 //     alternating it with the M = 128 output MMAs left ~700 idle cycles at every
 //     switch in a trace of this kernel on GB300.)
@@ -19,10 +20,10 @@
 //     latent numbers, A = two pieces of the stage read MN-major (a token's latent
 //     numbers are contiguous), B = the probabilities P^T[16 x 64] in shared
 //     memory -- 16 MMAs of K = 16 per block.
-// About 2,800 cycles of MMA issue per 72 KB block: below the ~3,400 cycles an SM's
+// About 3,100 cycles of MMA issue per 72 KB block: below the ~3,400 cycles an SM's
 // share of the HBM bandwidth needs for it.
 //
-// Persistent, one CTA per SM (227 KB of shared memory, 480 tensor-memory columns);
+// Persistent, one CTA per SM (224 KB of shared memory, all 512 tensor-memory columns);
 // the units (head tile, sequence, block) are cut into one equal contiguous range
 // per CTA (mla_partition.cuh), a sequence cut by a range boundary leaving fp32
 // partials merged by paged_mla_merge_tcn.  192 threads:
@@ -44,8 +45,9 @@
 //     cache (their value rows are zeroed: 0 * NaN must not reach the sums); at the
 //     end of a segment each warp normalises and writes its quarter of the latent
 //     rows.
-//   * tensor memory: queries [0, 288), scores [288, 352), output tiles at 352,
-//     384, 416, 448 (16 columns each).
+//   * tensor memory: the queries' latent numbers [0, 256), two score buffers [256,
+//     384), output tiles at 384, 416, 448, 480 (16 columns each); the queries' 64
+//     rotary numbers sit in shared memory.
 // Every wait is bounded; a late barrier sets KV_DEVERR_TIMEOUT and every role leaves
 // its loop, waits (bounded) for its copies and MMAs in flight, and the CTA frees its
 // tensor memory before it exits.
@@ -259,7 +261,10 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         fence_mbar_init();
     }
     if (warp == 5) tc_alloc(smem_u32(&ctl->tmem_base), TN_COLS);
-    grid_dependency_wait();
+    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
+    // positions of each sequence: then the producer waits, before the first load of a block
+    // that holds one of them.
+    if (p.dep_tail == 0) grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -274,6 +279,7 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             int k = 0;                              // segments handed on
             int g = 0;                              // stages issued (all segments)
             bool ok = true;
+            bool waited = p.dep_tail == 0;
             for (;;) {
                 const MlaSegment it = *abort_flag ? MlaSegment{0, 0, 0, -1, 0, 0, 0} : part.next();
                 const bool last = it.n < 0;
@@ -309,6 +315,10 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         break;
                     }
                     ctl->stage_blk[st] = bid;
+                    if (!waited && it.blk0 + s >= (it.ctx - p.dep_tail) / TN_TOK) {
+                        grid_dependency_wait();
+                        waited = true;
+                    }
                     const uint32_t fb = smem_u32(&ctl->kv_full[st]);
                     if (bid >= 0) {
                         const uint32_t dst = smem_u32(stages + st * TN_STAGE);

@@ -84,6 +84,9 @@ struct MlaParams {
     int split_blocks, max_splits;   // chunk length in blocks (tcgen05 form: least blocks per CTA
                                     // range); most chunks (pieces) a sequence can have
     float scale_log2;
+    int dep_tail;             // 0: wait for the preceding kernel before reading anything; n > 0:
+                              // it wrote only the last n positions of each sequence (the step's
+                              // append), and only the loads of the blocks holding them wait
 };
 
 // Launch with programmatic stream serialisation: the kernel may begin launching

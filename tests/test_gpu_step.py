@@ -131,3 +131,70 @@ def test_step_rejects_bad_arguments_before_launching():
                              torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
                              torch.ones(1, dtype=torch.int32, device="cuda"))
     lat.destroy()
+
+
+# ---- latent pools: paged_mla_decode_step, one case per form of the attention kernel
+M = workloads.mla
+MLA_STEP = {
+    "mma_bs16_h16": M(batch=4, q_heads=16, block_size=16, ctx=[1, 16, 17, 300], seed=311,
+                      split_tokens=64),
+    "narrow_bs64_h16": M(batch=5, q_heads=16, block_size=64, ctx=[1, 64, 65, 700, 2000], seed=312,
+                         split_tokens=64),
+    "narrow_bs64_h40": M(batch=3, q_heads=40, block_size=64, ctx=[63, 129, 1500], seed=313),
+    "wide_bs64_h128": M(batch=3, q_heads=128, block_size=64, ctx=[1, 70, 900], seed=314,
+                        split_tokens=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MLA_STEP))
+def test_mla_step_matches_the_oracle_and_the_separate_calls(name):
+    w = workloads.make(MLA_STEP[name])
+    s = w.spec
+    fused = Staged(w, step_append=False)
+    out = torch.empty(w.batch, s.q_heads, s.latent_dim, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.batch, s.q_heads, dtype=torch.float32, device="cuda")
+    kp.paged_mla_decode_step(fused.pool, fused.k_new, fused.q, fused.tables, fused.ctx, w.scale,
+                             kv_split_tokens=s.split_tokens, out=out, lse=lse,
+                             latent_dim=s.latent_dim)
+    torch.cuda.synchronize()
+    # the pool holds every vector, the appended ones included, bit for bit
+    k, _, _, _ = fused.pool.tensors()
+    pool = k.view(torch.int16).cpu().numpy().view(np.uint16)[:, :, 0, :]
+    for b in range(w.batch):
+        n = int(w.context_lens[b])
+        t = np.arange(n)
+        assert np.array_equal(pool[w.block_tables[b, t // s.block_size], t % s.block_size],
+                              w.seq_k(b)[:, 0, :]), b
+    ref, ref_lse = oracle.mla_decode_workload(w)
+    max_abs, rel, got = compare(out, ref)
+    assert np.isfinite(got).all()
+    assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
+    assert np.nanmax(np.abs(lse.cpu().numpy() - ref_lse)) <= LSE_ABS
+    assert fused.pool.device_errors() == 0
+    # the separate calls give the same bits
+    sep = Staged(w, step_append=True)
+    out2, lse2 = sep.mla()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    sep.destroy()
+    fused.destroy()
+
+
+def test_mla_step_rejects_bad_arguments_before_launching():
+    w = workloads.make(M(batch=2, q_heads=16, block_size=64, ctx=[10, 100], seed=315))
+    st = Staged(w, step_append=False)
+    before = [t.clone() for t in st.pool.raw_bytes() if t is not None]
+    buf = torch.empty(2 * 16 * 512 + 8, dtype=torch.bfloat16, device="cuda")
+    bad_out = buf[1:1 + 2 * 16 * 512].view(2, 16, 512)               # 2 bytes off a 16-byte boundary
+    with pytest.raises(kp.KVError):
+        kp.paged_mla_decode_step(st.pool, st.k_new, st.q, st.tables, st.ctx, w.scale, out=bad_out)
+    torch.cuda.synchronize()
+    after = [t for t in st.pool.raw_bytes() if t is not None]
+    assert all(torch.equal(a, b) for a, b in zip(before, after))      # nothing was appended
+    st.destroy()
+    gqa = kp.kv_pool_create(8, 16, 2, 64)
+    with pytest.raises(kp.KVError):                                   # not a latent pool
+        kp.paged_mla_decode_step(gqa, torch.zeros(1, 576, dtype=torch.bfloat16, device="cuda"),
+                                 torch.zeros(1, 16, 576, dtype=torch.bfloat16, device="cuda"),
+                                 torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
+                                 torch.ones(1, dtype=torch.int32, device="cuda"), 0.1)
+    gqa.destroy()
