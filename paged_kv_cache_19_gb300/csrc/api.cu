@@ -698,19 +698,19 @@ WorkspaceLayout mla_workspace_layout(int batch, int q_heads, const MlaPlan& p)
 {
     WorkspaceLayout w{0, 0, 0, 0, 0};
     if (p.max_splits > 1 && p.form == kMlaNarrow) {
-        // pieces (sequence, head tile, split): fp32 partials of 16 heads x 512 latent
-        // numbers, (max, sum) per head, then the piece count of each (sequence, head tile)
+        // pieces (sequence, head tile, split): fp16 partials of 16 heads x 512 latent
+        // numbers, fp32 (max, sum) per head, then the piece count of each (sequence, head tile)
         const size_t pieces = static_cast<size_t>(batch) * p.head_tiles * p.max_splits;
-        w.part_ml = round_up(pieces * kvp::MLA_TCN_HEADS * kvp::MLA_DV * sizeof(float), kAlign);
+        w.part_ml = round_up(pieces * kvp::MLA_TCN_HEADS * kvp::MLA_DV * 2, kAlign);
         w.tickets = w.part_ml + round_up(pieces * kvp::MLA_TCN_HEADS * 2 * sizeof(float), kAlign);
         w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * sizeof(int);
         w.total = w.tickets + w.ticket_bytes;
     } else if (p.max_splits > 1 && p.form == kMlaWide) {
-        // pieces (sequence, head tile, latent half, split): fp32 partials of 128 heads x
-        // 256 latent numbers, (max, sum) per head, then the piece count of each
+        // pieces (sequence, head tile, latent half, split): fp16 partials of 128 heads x
+        // 256 latent numbers, fp32 (max, sum) per head, then the piece count of each
         // (sequence, head tile, half) -- read by the merge kernel
         const size_t pieces = static_cast<size_t>(batch) * p.head_tiles * 2 * p.max_splits;
-        w.part_ml = round_up(pieces * kvp::MLA_TC_HEADS * (kvp::MLA_DV / 2) * sizeof(float), kAlign);
+        w.part_ml = round_up(pieces * kvp::MLA_TC_HEADS * (kvp::MLA_DV / 2) * 2, kAlign);
         w.tickets = w.part_ml + round_up(pieces * kvp::MLA_TC_HEADS * 2 * sizeof(float), kAlign);
         w.ticket_bytes = static_cast<size_t>(batch) * p.head_tiles * 2 * sizeof(int);
         w.total = w.tickets + w.ticket_bytes;

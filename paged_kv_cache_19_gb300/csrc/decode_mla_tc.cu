@@ -659,15 +659,16 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     for (int j = 0; j < 32; ++j) r[j] = 0u;
                 }
                 if (!whole) {
-                    // a piece of a cut sequence: its normalised partial in the piece layout
-                    // [32-number chunk][float4 slot][head], coalesced as written (thread =
-                    // head); its (max, sum) beside it
-                    float4* dst = reinterpret_cast<float4*>(p.part_o) + piece * (TC_M * TC_DQ / 4) +
-                                  static_cast<size_t>((half * 4 + c2) * 8) * TC_M + h;
+                    // a piece of a cut sequence: its normalised partial, in fp16 (values of
+                    // the cache averaged: well inside its range, 11 significant bits against
+                    // the output's 8), in the piece layout [32-number chunk][4-number slot]
+                    // [head], coalesced as written (thread = head); its (max, sum) beside it
+                    uint2* dst = reinterpret_cast<uint2*>(p.part_o) + piece * (TC_M * TC_DQ / 4) +
+                                 static_cast<size_t>((half * 4 + c2) * 8) * TC_M + h;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        dst[j * TC_M] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                                                    __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+                        dst[j * TC_M] = make_uint2(pack_f16x2(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv),
+                                                   pack_f16x2(__uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv));
                     continue;
                 }
 #pragma unroll
@@ -741,8 +742,8 @@ paged_mla_merge_tc(const MlaParams p)
         const int nh = min(TC_M, p.q_heads - ht * TC_M);
         const size_t piece0 = ((static_cast<size_t>(b) * p.head_tiles + ht) * 2 + dq) * p.max_splits;
         const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + piece0 * TC_M + h;
-        const float4* po = reinterpret_cast<const float4*>(p.part_o) + piece0 * (TC_M * TC_DQ / 4) +
-                           static_cast<size_t>(cg * 8) * TC_M + h;
+        const uint2* po = reinterpret_cast<const uint2*>(p.part_o) + piece0 * (TC_M * TC_DQ / 4) +
+                          static_cast<size_t>(cg * 8) * TC_M + h;
         float M = -INFINITY, W = 0.f;
         float acc[32];
 #pragma unroll
@@ -758,8 +759,11 @@ paged_mla_merge_tc(const MlaParams p)
                 const size_t j = static_cast<size_t>(in ? j0 + i : j0);
                 mj[i] = in ? __ldcg(ml + j * TC_M) : make_float2(-INFINITY, 0.f);
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    x[i][v] = in ? __ldcg(po + j * (TC_M * TC_DQ / 4) + v * TC_M) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int v = 0; v < 8; ++v) {
+                    const uint2 u = __ldcg(po + j * (TC_M * TC_DQ / 4) + v * TC_M);
+                    const float2 a = unpack_f16x2(u.x), c = unpack_f16x2(u.y);
+                    x[i][v] = make_float4(a.x, a.y, c.x, c.y);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {

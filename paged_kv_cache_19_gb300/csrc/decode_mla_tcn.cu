@@ -624,9 +624,12 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     for (int j = 0; j < TN_H; ++j)
                         if (j < nh) dst[static_cast<size_t>(j) * MLA_DV] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]) * inv[j], 0.f));
                 } else {
-                    float* dst = p.part_o + piece * (TN_H * MLA_DV) + d;
+                    // fp16: averages of cached values, well inside its range, 11 significant
+                    // bits against the output's 8
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.part_o) + piece * (TN_H * MLA_DV) + d;
 #pragma unroll
-                    for (int j = 0; j < TN_H; ++j) dst[j * MLA_DV] = __uint_as_float(r[j]) * inv[j];
+                    for (int j = 0; j < TN_H; ++j)
+                        dst[j * MLA_DV] = static_cast<uint16_t>(pack_f16x2(__uint_as_float(r[j]) * inv[j], 0.f));
                 }
             }
             tc_fence_before();
@@ -674,7 +677,8 @@ paged_mla_merge_tcn(const MlaParams p)
     if (nsplit > 1 && h < nh) {
         const size_t piece0 = (static_cast<size_t>(b) * p.head_tiles + ht) * p.max_splits;
         const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + piece0 * TN_H + h;
-        const float4* po = reinterpret_cast<const float4*>(p.part_o + (piece0 * TN_H + h) * MLA_DV + qd * 128 + cg * 8);
+        const uint4* po = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.part_o) +
+                                                         (piece0 * TN_H + h) * MLA_DV + qd * 128 + cg * 8);
         float M = -INFINITY, W = 0.f;
         float acc[8];
 #pragma unroll
@@ -687,8 +691,11 @@ paged_mla_merge_tcn(const MlaParams p)
                 const bool in = j0 + i < nsplit;
                 const size_t j = static_cast<size_t>(in ? j0 + i : j0);
                 mj[i] = in ? __ldcg(ml + j * TN_H) : make_float2(-INFINITY, 0.f);
-                x[i][0] = __ldcg(po + j * (TN_H * MLA_DV / 4));
-                x[i][1] = __ldcg(po + j * (TN_H * MLA_DV / 4) + 1);
+                const uint4 u = __ldcg(po + j * (TN_H * MLA_DV / 8));
+                const float2 a = unpack_f16x2(u.x), bq = unpack_f16x2(u.y), c = unpack_f16x2(u.z),
+                             e = unpack_f16x2(u.w);
+                x[i][0] = make_float4(a.x, a.y, bq.x, bq.y);
+                x[i][1] = make_float4(c.x, c.y, e.x, e.y);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

@@ -205,6 +205,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v)
+{
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 // Two e4m3 codes (low byte = first element) -> two exact f16 values.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
 {

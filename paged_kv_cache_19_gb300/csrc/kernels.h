@@ -72,13 +72,16 @@ struct MlaParams {
     const int32_t* ctx;       // [batch]
     uint16_t* out;            // bf16 [batch, q_heads, MLA_DV]
     float* lse;               // [batch, q_heads] or null
-    float* part_o;            // [batch, q_heads, max_splits, MLA_DV]; tcgen05 form: per piece
-                              // (sequence, head tile, half, split) [8 chunks][8 float4][128 heads]
+    float* part_o;            // [batch, q_heads, max_splits, MLA_DV]; the tcgen05 forms store
+                              // fp16 here: wide, per piece (sequence, head tile, half, split)
+                              // [8 chunks][8 slots of 4][128 heads]; narrow, per piece (sequence,
+                              // head tile, split) [16 heads][MLA_DV]
     float* part_ml;           // [batch, q_heads, max_splits, 2]: (max, sum), log2 units;
-                              // tcgen05 form: [piece][128 heads][2]
+                              // tcgen05 forms: [piece][128 or 16 heads][2]
     uint32_t* err;
     int* tickets;             // [batch, head_tiles]: finished chunks, zero between calls;
-                              // tcgen05 form: [batch, head_tiles, 2 halves] piece counts
+                              // tcgen05 forms: piece counts, [batch, head_tiles, 2 halves]
+                              // (wide) or [batch, head_tiles] (narrow)
     int batch, q_heads, head_tiles;
     int max_blocks, num_blocks;
     int split_blocks, max_splits;   // chunk length in blocks (tcgen05 form: least blocks per CTA

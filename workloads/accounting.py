@@ -118,9 +118,9 @@ def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0
 
     tc_grid > 0: a tensor-core form with that many CTAs and pieces from mla_tc_pieces --
     form "wide": tiles of 128 heads, two latent halves each reading every vector, each
-    piece of a cut sequence writing (and the merge reading) 128 heads x 256 fp32 numbers
-    and a (max, sum) pair per head; form "narrow": tiles of 16 heads, 16 x 512 numbers
-    and 16 pairs per piece."""
+    piece of a cut sequence writing (and the merge reading) 128 heads x 256 fp16 numbers
+    and an fp32 (max, sum) pair per head; form "narrow": tiles of 16 heads, 16 x 512 fp16
+    numbers and 16 pairs per piece."""
     s = w.spec
     ctx = w.context_lens.astype(np.int64)
     nb = _nb(w)
@@ -131,11 +131,11 @@ def mla_decode_bytes(w, split_tokens: int, head_tile: int = 16, tc_grid: int = 0
     if tc_grid > 0 and form == "wide":
         tiles = -(-s.q_heads // 128) * 2
         pieces = mla_tc_pieces(w, max(1, split_tokens // s.block_size), tc_grid)
-        partial = int(pieces[pieces > 1].sum()) * 128 * ((s.latent_dim // 2) * 4 + 8) * 2
+        partial = int(pieces[pieces > 1].sum()) * 128 * ((s.latent_dim // 2) * 2 + 8) * 2
     elif tc_grid > 0:
         tiles = -(-s.q_heads // 16)
         pieces = mla_tc_pieces(w, max(1, split_tokens // s.block_size), tc_grid, 16, 1)
-        partial = int(pieces[pieces > 1].sum()) * 16 * (s.latent_dim * 4 + 8) * 2
+        partial = int(pieces[pieces > 1].sum()) * 16 * (s.latent_dim * 2 + 8) * 2
     else:
         tiles = -(-s.q_heads // head_tile)
         sb = max(1, split_tokens // s.block_size)
