@@ -143,6 +143,10 @@ MLA_STEP = {
     "narrow_bs64_h40": M(batch=3, q_heads=40, block_size=64, ctx=[63, 129, 1500], seed=313),
     "wide_bs64_h128": M(batch=3, q_heads=128, block_size=64, ctx=[1, 70, 900], seed=314,
                         split_tokens=64),
+    # a grid of more than three CTAs per SM: the mma.sync form without a producer warp, whose
+    # loads are issued by a consumer thread (the one that waits for the append)
+    "mma_bs16_h128_many_ctas": M(batch=24, q_heads=128, block_size=16, ctx_uniform=(1, 300),
+                                 seed=316, split_tokens=64),
 }
 
 
@@ -198,3 +202,29 @@ def test_mla_step_rejects_bad_arguments_before_launching():
                                  torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
                                  torch.ones(1, dtype=torch.int32, device="cuda"), 0.1)
     gqa.destroy()
+
+
+def test_repeated_mla_steps_on_one_stream_stay_exact():
+    """Several latent steps back to back on one stream, each attention overlapping the append
+    before it (the same step repeated: same bits each time)."""
+    w = workloads.make(M(batch=4, q_heads=16, block_size=64, ctx=[15, 64, 65, 600], seed=317,
+                         split_tokens=64))
+    st = Staged(w, step_append=False)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            out = torch.empty(w.batch, w.spec.q_heads, w.spec.latent_dim, dtype=torch.bfloat16,
+                              device="cuda")
+            kp.paged_mla_decode_step(st.pool, st.k_new, st.q, st.tables, st.ctx, w.scale,
+                                     kv_split_tokens=w.spec.split_tokens, out=out, stream=s,
+                                     latent_dim=w.spec.latent_dim)
+            outs.append(out)
+    s.synchronize()
+    ref, _ = oracle.mla_decode_workload(w)
+    for out in outs:
+        max_abs, rel, _ = compare(out, ref)
+        assert max_abs <= MAX_ABS and rel <= REL_L2
+        assert torch.equal(out, outs[0])
+    assert st.pool.device_errors() == 0
+    st.destroy()
