@@ -336,13 +336,22 @@ def cpu_baseline(w, target_s: float, gpu_out=None):
         t0 = time.perf_counter()
         out, _ = oracle_step_sample(w, seqs, threads)
         dt = time.perf_counter() - t0
+    passes = 1
+    if dt < target_s / 3:                         # the whole batch is quick: repeat it
+        more = int(min(200, (target_s / 3) / max(dt, 1e-3)))
+        t0 = time.perf_counter()
+        for _ in range(more):
+            oracle_step_sample(w, seqs, threads)
+        dt = (dt + time.perf_counter() - t0) / (more + 1)
+        passes = more + 1
     nbytes, ntok = sample_bytes(w, seqs)
     used = 1 if w.spec.mla else threads           # the MLA oracle runs on one thread
     res = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": used,
            "kind": "oracle",
            "sample": (f"append + decode of {len(seqs)} of {w.batch} sequences ({ntok} cached "
                       f"tokens, all {w.spec.q_heads} query heads), float64 C oracle, "
-                      f"{used} thread{'s' if used > 1 else ''}, {dt:.2f} s"),
+                      f"{used} thread{'s' if used > 1 else ''}, {dt * 1e3:.1f} ms per pass, "
+                      f"mean of {passes} pass{'es' if passes > 1 else ''} ({dt * passes:.1f} s)"),
            "kv_tokens_per_s": round(ntok / dt, 1)}
     if gpu_out is not None:
         got = gpu_out[seqs].float().cpu().double().numpy()
