@@ -65,9 +65,10 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
 kv_status paged_mla_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                                 int kv_split_tokens, int* split_tokens, int* max_splits);
 
-/* Bytes of device workspace for these sizes (fp32 partials, (max, sum) pairs and
- * one 32-bit counter per (sequence, head tile[, latent half])); 0 when no sequence
- * can be cut into pieces.  The workspace must be zero-filled before its first use;
+/* Bytes of device workspace for these sizes: the partial outputs of cut sequences
+ * (fp16 in the tcgen05 forms, fp32 in the mma.sync form), an fp32 (max, sum) pair
+ * per head and piece, and one 32-bit counter per (sequence, head tile[, latent
+ * half]); 0 when no sequence can be cut into pieces.  The workspace must be zero-filled before its first use;
  * every call leaves the counters ready for the next.  Calls sharing a workspace
  * must not overlap in time. */
 kv_status paged_mla_workspace_size(const kv_pool* pool, int batch, int q_heads, int max_blocks,

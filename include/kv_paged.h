@@ -199,8 +199,9 @@ kv_status paged_decode_workspace_size(const kv_pool* pool, int batch, int q_head
  *     scaled scores (NULL to skip).
  *   kv_split_tokens: split-KV chunk in tokens (0 = automatic; else a positive
  *     multiple of block_size).  Chunk j of a sequence covers tokens
- *     [j * split, (j+1) * split); chunks are merged by log-sum-exp in a second
- *     kernel.  The result does not depend on the split up to rounding.
+ *     [j * split, (j+1) * split); the chunks of a sequence are merged by
+ *     log-sum-exp by whichever of its chunk CTAs finishes last.  The result
+ *     does not depend on the split up to rounding.
  *   workspace: device memory of at least paged_decode_workspace_size() bytes
  *     (may be NULL when that size is 0).  It must be zero-filled before its
  *     first use: it holds the counters that tell the last chunk of a sequence
@@ -215,6 +216,26 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
                                  const int32_t* context_lens, int batch, float scale,
                                  int kv_split_tokens, void* workspace, size_t workspace_bytes,
                                  void* out, float* lse_out, void* stream);
+
+/*
+ * paged_decode_attention_split_merge -- the same attention in two kernels: the
+ * split-KV grid leaves the fp32 partial (normalised output, maximum, sum) of
+ * every chunk of a cut sequence in the workspace, and a separate log-sum-exp
+ * merge kernel combines them (learn.mohebi.ai lesson 12, section 6: split-KV
+ * decoding).  Sequences of one chunk are finished by the grid.  The merge does
+ * the fused form's arithmetic in the same order: outputs and lse are bit-
+ * identical to paged_decode_attention with the same arguments.
+ *   Arguments, workspace size and errors as for paged_decode_attention; the
+ *   workspace's chunk counters are not used (it need not be zero-filled).
+ *   Two kernel launches when some sequence can have more than one chunk, one
+ *   otherwise.
+ */
+kv_status paged_decode_attention_split_merge(const kv_pool* pool, const void* q, int q_heads,
+                                             const int32_t* block_tables, int max_blocks,
+                                             const int32_t* context_lens, int batch, float scale,
+                                             int kv_split_tokens, void* workspace,
+                                             size_t workspace_bytes, void* out, float* lse_out,
+                                             void* stream);
 
 /*
  * paged_attention_multi_query -- attention of q_len new tokens per sequence

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
-    "paged_decode_workspace_size", "paged_decode_attention", "paged_attention_multi_query",
+    "paged_decode_workspace_size", "paged_decode_attention", "paged_decode_attention_split_merge",
+    "paged_attention_multi_query",
     "paged_decode_step",
     "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
     "kv_copy_blocks", "BM_FIFO", "BM_LIFO", "BM_PREFIX_CACHING", "kv_mla_pool_create",
@@ -90,6 +91,8 @@ def load_library():
             "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
+            "paged_decode_attention_split_merge": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P,
+                                                    P, P], I),
             "paged_attention_multi_query": ([P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
                                              P], I),
             "paged_multi_query_workspace_size": ([P, I, I, I, I, I, ctypes.POINTER(S)], I),
@@ -301,6 +304,36 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
                                       float(scale), int(kv_split_tokens), _ptr(workspace),
                                       int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)),
            "paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_split_merge(pool: Pool, q, block_tables, context_lens,
+                                       scale: float | None = None, kv_split_tokens: int = 0,
+                                       workspace=None, out=None, lse=None, stream=None):
+    """paged_decode_attention as two kernels: the split-KV grid, then a separate
+    log-sum-exp merge kernel (same bits).  Returns out (shape of q)."""
+    lib = load_library()
+    _need(q, torch.bfloat16, "q")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    batch, q_heads = q.shape[0], q.shape[1]
+    d = q.shape[-1]
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        need = paged_decode_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
+    _need(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(lib.paged_decode_attention_split_merge(
+        pool.handle, _ptr(q), int(q_heads), _ptr(block_tables), int(max_blocks),
+        _ptr(context_lens), int(batch), float(scale), int(kv_split_tokens), _ptr(workspace),
+        int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)), "paged_decode_attention_split_merge")
     return out
 
 

@@ -506,6 +506,7 @@ kv_status make_decode_launch(const kv_pool* pool, const void* q, int q_heads, in
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.dep_tail = 0;
+    p.merge_kernel = 0;
     // chunk-major grid: x = (kv head, row tile), y = sequence, z = chunk
     *grid = dim3(static_cast<unsigned>(pool->kv_heads * plan.head_groups),
                  static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));
@@ -601,6 +602,29 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
     return paged_attention_multi_query(pool, q, q_heads, 1, block_tables, max_blocks,
                                        context_lens, batch, scale, kv_split_tokens, workspace,
                                        workspace_bytes, out, lse_out, stream);
+}
+
+kv_status paged_decode_attention_split_merge(const kv_pool* pool, const void* q, int q_heads,
+                                             const int32_t* block_tables, int max_blocks,
+                                             const int32_t* context_lens, int batch, float scale,
+                                             int kv_split_tokens, void* workspace,
+                                             size_t workspace_bytes, void* out, float* lse_out,
+                                             void* stream)
+{
+    Plan plan;
+    kvp::DecodeParams p;
+    dim3 grid;
+    const kv_status st = make_decode_launch(pool, q, q_heads, 1, block_tables, max_blocks,
+                                            context_lens, batch, scale, kv_split_tokens, workspace,
+                                            workspace_bytes, out, lse_out, &plan, &p, &grid);
+    if (st != KV_OK || batch == 0) return st;
+    p.merge_kernel = plan.max_splits > 1;
+    kv_status r = launch_decode(pool, plan, grid, p, stream);
+    if (r != KV_OK || !p.merge_kernel) return r;
+    return kvp::launch_decode_merge(p, pool->head_dim, pool->block_size,
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KV_OK
+               : KV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -8,7 +8,8 @@
 // leaves an fp32 partial (normalised output, max, sum) and counts itself on
 // the unit's ticket, and the CTA that completes the count merges the chunks by
 // log-sum-exp (learn.mohebi.ai lesson 12, section 6: split-KV decoding) and
-// resets the ticket -- no second kernel.
+// resets the ticket -- no second kernel.  With merge_kernel set the chunk CTAs
+// only leave their partials and paged_decode_merge (merge.cu) combines them.
 //
 //   * One producer warp streams K and V blocks with 5-D TMA tensor loads
 //     (cp.async.bulk.tensor, 128-byte swizzle) into a ring of NSTAGE shared-
@@ -225,7 +226,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             __threadfence();                        // partial visible before the ticket
         }
     }
-    if (nsplit == 1) return;
+    if (nsplit == 1 || p.merge_kernel) return;      // done, or merged by paged_decode_merge
 
     // ---- ticket: the last chunk of this unit to finish merges all chunks
     named_barrier_sync(1, C::NCW * 32);

@@ -40,6 +40,9 @@ struct DecodeParams {
     // each sequence in the pool (the step's append), so blocks holding none of them are
     // read at once and only the loads of the others wait for it.
     int dep_tail;
+    // 0: the last chunk CTA of a cut sequence merges the chunks (tickets).  1: chunk CTAs
+    // only leave their partials, and paged_decode_merge (launch_decode_merge) merges them.
+    int merge_kernel;
 };
 
 struct AppendParams {
@@ -131,6 +134,11 @@ cudaError_t launch_decode_bf16(int head_dim, int block_size, int head_tile, dim3
 cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 grid,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
+// The separate log-sum-exp merge of the chunk partials that paged_decode_main leaves
+// with merge_kernel = 1: one thread per 4 numbers of a query row, sequences of one
+// chunk skipped (their chunk wrote the output).
+cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int block_size,
+                                cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 // Tokens per pipeline stage of the latent decode (0: block size not supported);
 // prod: the variant with a producer warp (small grids), else the three-CTA one.

@@ -121,6 +121,33 @@ def test_chunk_counters_return_to_zero(staged):
     assert torch.count_nonzero(counters) == 0
 
 
+def _split_merge(st, split):
+    out = torch.empty_like(st.q)
+    lse = torch.empty(st.q.shape[:2], dtype=torch.float32, device="cuda")
+    kp.paged_decode_attention_split_merge(st.pool, st.q, st.tables, st.ctx, st.w.scale,
+                                          kv_split_tokens=split, out=out, lse=lse)
+    return out, lse
+
+
+def test_separate_merge_kernel_gives_the_fused_bits(staged):
+    """The two-kernel form (split-KV grid, then a separate log-sum-exp merge kernel) against
+    the fused form, whose last chunk CTA merges: identical output and lse bits at one block
+    per chunk, three blocks per chunk and the automatic chunk, and within tolerance of the
+    oracle."""
+    w = staged.w
+    bs = w.spec.block_size
+    ref, ref_lse = oracle.decode_workload(w)
+    for split in (bs, 3 * bs, 0):
+        a, la = staged.decode(split_tokens=split)
+        b, lb = _split_merge(staged, split)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), split
+        assert torch.equal(la.view(torch.int32), lb.view(torch.int32)), split
+        max_abs, rel, _ = compare(b, ref)
+        assert max_abs <= MAX_ABS and rel <= REL_L2, (split, max_abs, rel)
+        assert np.max(np.abs(lb.cpu().numpy() - ref_lse)) <= LSE_ABS
+    assert staged.pool.device_errors() == 0
+
+
 def test_block_permutation_gives_identical_bits():
     w = workloads.make(SMALL["g4_d128_bs16"])
     st = Staged(w)
@@ -350,4 +377,8 @@ def test_full_size_config_sampled_parity(name):
         raw, _ = oracle.decode_workload(w, seqs=seqs, threads=os.cpu_count() or 1, cache_dtype="bf16")
         long_ctx = w.context_lens[seqs] >= FP8_GATE_MIN_CTX
         assert np.max(np.abs(got - raw)[long_ctx]) <= FP8_VS_UNQUANTISED_MAX_ABS
+    # the two-kernel form (separate log-sum-exp merge) gives the same bits at this size
+    out2, lse2 = _split_merge(st, s.split_tokens)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
     st.destroy()
