@@ -238,6 +238,29 @@ kv_status paged_decode_attention_split_merge(const kv_pool* pool, const void* q,
                                              void* stream);
 
 /*
+ * paged_merge_attention_states -- combines attention results over disjoint key
+ * sets into the result over their union: source r attended over its own keys
+ * and gave o_r and lse_r, and
+ *   LSE = log sum_r exp(lse_r),   out = sum_r exp(lse_r - LSE) o_r
+ * (the log-sum-exp merge of split-KV decoding, learn.mohebi.ai lesson 12,
+ * section 6, with the chunks' (max, sum) pairs folded into lse).  It is the one
+ * exchange a sequence split across devices needs: each device runs
+ * paged_decode_attention over its share of the sequence's blocks (with
+ * lse_out), the (out, lse) pairs are gathered, and this call merges them.
+ *   outs: bf16 [n_src, rows, head_dim], 16-byte aligned; lses: fp32 [n_src,
+ *   rows], natural log, -inf for a source that saw no key (left out).
+ *   out: bf16 [rows, head_dim] (round to nearest even), 16-byte aligned;
+ *   lse_out: fp32 [rows] or NULL.  A row whose sources are all empty gets
+ *   out = 0, lse = -inf.
+ *   n_src >= 1; head_dim a multiple of 8 in [8, 1024]; rows == 0 is a no-op.
+ *   fp32 arithmetic.  Asynchronous on `stream`; no allocation.  out must not
+ *   overlap outs.
+ */
+kv_status paged_merge_attention_states(const void* outs, const float* lses, int n_src,
+                                       long long rows, int head_dim, void* out, float* lse_out,
+                                       void* stream);
+
+/*
  * paged_attention_multi_query -- attention of q_len new tokens per sequence
  * over the paged cache: the verify pass of speculative decoding (the target
  * model scores the draft's guesses in one pass) and the chunks of a chunked

@@ -2,7 +2,9 @@
 
 Only the tests, the smoke check and the bench's CPU-baseline / reference arm
 may import this package.  The product path never does, and the two share no
-code: this file only marshals numpy arrays into ``kv_oracle.c``.
+code: this file marshals numpy arrays into ``kv_oracle.c`` and holds one numpy
+function of its own, ``merge_states`` (the merge of attention results over
+disjoint key sets).
 
 The C source states each step with its source page and section.
 """
@@ -183,6 +185,34 @@ def attend_split(q, k, v, scale: float, split_tokens: int, num_chunks: int | Non
     lse = np.zeros(hq, dtype=np.float64)
     lib.kvo_attend_split(_ptr(q), hq, hkv, d, _ptr(k), _ptr(v), ctx, float(scale), split_tokens,
                          num_chunks, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def merge_states(outs, lses):
+    """Attention over the union of disjoint key sets from the attention over each set.
+
+    outs [n, rows, d] (normalised outputs), lses [n, rows] (natural-log log-sum-exp of the
+    scaled scores; -inf for a set with no key) -> (out [rows, d], lse [rows]).  Written out
+    from the split-KV merge (learn.mohebi.ai lesson 12, section 6: split-KV decoding), with
+    each set's (max, sum) pair folded into lse = max + log(sum):
+        LSE = log sum_r exp(lse_r),   out = sum_r exp(lse_r - LSE) out_r.
+    Sets with no key are left out; a row with none gets out = 0, lse = -inf."""
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    n, rows, d = outs.shape
+    out = np.zeros((rows, d), dtype=np.float64)
+    lse = np.full(rows, -np.inf)
+    for i in range(rows):
+        used = [r for r in range(n) if lses[r, i] > -np.inf]
+        if not used:
+            continue
+        m = max(lses[r, i] for r in used)
+        w = {r: np.exp(lses[r, i] - m) for r in used}
+        total = sum(w.values())
+        for r in used:
+            out[i] += w[r] * outs[r, i]
+        out[i] /= total
+        lse[i] = m + np.log(total)
     return out, lse
 
 

@@ -18,6 +18,7 @@ import torch
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_decode_attention_split_merge",
+    "paged_merge_attention_states",
     "paged_attention_multi_query",
     "paged_decode_step",
     "paged_multi_query_workspace_size", "library_path", "load_library", "BlockManager",
@@ -91,6 +92,7 @@ def load_library():
             "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
+            "paged_merge_attention_states": ([P, P, I, L, I, P, P, P], I),
             "paged_decode_attention_split_merge": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P,
                                                     P, P], I),
             "paged_attention_multi_query": ([P, P, I, I, P, I, P, I, ctypes.c_float, I, P, S, P, P,
@@ -334,6 +336,30 @@ def paged_decode_attention_split_merge(pool: Pool, q, block_tables, context_lens
         pool.handle, _ptr(q), int(q_heads), _ptr(block_tables), int(max_blocks),
         _ptr(context_lens), int(batch), float(scale), int(kv_split_tokens), _ptr(workspace),
         int(ws_bytes), _ptr(out), _ptr(lse), _stream(stream)), "paged_decode_attention_split_merge")
+    return out
+
+
+def paged_merge_attention_states(outs, lses, out=None, lse=None, stream=None):
+    """Attention over the union of disjoint key sets from the results over each set.
+
+    outs: bf16 [n_src, *rows, d]; lses: fp32 [n_src, *rows] (natural log, -inf for a set
+    with no key).  Returns out bf16 [*rows, d]; writes lse fp32 [*rows] when given."""
+    lib = load_library()
+    _need(outs, torch.bfloat16, "outs")
+    _need(lses, torch.float32, "lses")
+    n_src, d = outs.shape[0], outs.shape[-1]
+    if tuple(lses.shape) != tuple(outs.shape[:-1]):
+        raise ValueError("lses must have the shape of outs without its last dimension")
+    rows = lses[0].numel() if n_src else 0
+    if out is None:
+        out = torch.empty(outs.shape[1:], dtype=torch.bfloat16, device=outs.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if out.numel() != rows * d or (lse is not None and lse.numel() != rows):
+        raise ValueError("out / lse sizes do not match outs")
+    _check(lib.paged_merge_attention_states(_ptr(outs), _ptr(lses), int(n_src), int(rows), int(d),
+                                            _ptr(out), _ptr(lse), _stream(stream)),
+           "paged_merge_attention_states")
     return out
 
 

@@ -604,6 +604,22 @@ kv_status paged_decode_attention(const kv_pool* pool, const void* q, int q_heads
                                        workspace_bytes, out, lse_out, stream);
 }
 
+kv_status paged_merge_attention_states(const void* outs, const float* lses, int n_src, long long rows,
+                                       int head_dim, void* out, float* lse_out, void* stream)
+{
+    if (n_src < 1 || rows < 0 || head_dim < 8 || head_dim > 1024 || head_dim % 8 != 0)
+        return KV_ERR_INVALID_ARG;
+    if (rows == 0) return KV_OK;
+    if (outs == nullptr || lses == nullptr || out == nullptr) return KV_ERR_INVALID_ARG;
+    if (!aligned(outs, 16) || !aligned(out, 16) || !aligned(lses, 4) || !aligned(lse_out, 4))
+        return KV_ERR_INVALID_ARG;
+    return kvp::launch_merge_attention_states(
+               static_cast<const uint16_t*>(outs), lses, n_src, rows, head_dim,
+               static_cast<uint16_t*>(out), lse_out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KV_OK
+               : KV_ERR_CUDA;
+}
+
 kv_status paged_decode_attention_split_merge(const kv_pool* pool, const void* q, int q_heads,
                                              const int32_t* block_tables, int max_blocks,
                                              const int32_t* context_lens, int batch, float scale,

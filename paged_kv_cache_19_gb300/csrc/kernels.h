@@ -139,6 +139,11 @@ cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 
 // chunk skipped (their chunk wrote the output).
 cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int block_size,
                                 cudaStream_t s);
+// Merge of attention results over disjoint key sets: outs bf16 [n_src, rows, head_dim],
+// lses [n_src, rows] (natural log) -> out bf16 [rows, head_dim], lse_out [rows] or null.
+cudaError_t launch_merge_attention_states(const uint16_t* outs, const float* lses, int n_src,
+                                          long long rows, int head_dim, uint16_t* out,
+                                          float* lse_out, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 // Tokens per pipeline stage of the latent decode (0: block size not supported);
 // prod: the variant with a producer warp (small grids), else the three-CTA one.

@@ -48,6 +48,54 @@ def _rank_main(rank, world, port, out_dir):
         json.dump(res, fh)
 
 
+def _shard_main(rank, world, port, out_dir):
+    """One long sequence split by blocks across the ranks: each rank attends over its own
+    blocks, the (out, lse) pairs are gathered -- the one exchange of a sequence split --
+    and merged."""
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import oracle
+    import workloads
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        spec = workloads.custom(batch=1, q_heads=8, kv_heads=2, head_dim=64, block_size=16,
+                                ctx=[1000], seed=121)
+        w = workloads.make(spec)
+        n = int(w.context_lens[0])                              # the sequence's K/V, contiguous
+        k = workloads.bf16_bits_to_f32(w.k[:n]).astype(np.float64)
+        v = workloads.bf16_bits_to_f32(w.v[:n]).astype(np.float64)
+        q = workloads.bf16_bits_to_f32(w.q[0]).astype(np.float64).reshape(8, 64)
+        nblk = -(-k.shape[0] // 16)
+        per = -(-nblk // world)
+        a, b = min(rank * per * 16, k.shape[0]), min((rank + 1) * per * 16, k.shape[0])
+        o, l = oracle.attend(q, k[a:b], v[a:b], w.scale)
+        o_all = [torch.zeros(8, 64, dtype=torch.float64) for _ in range(world)]
+        l_all = [torch.zeros(8, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(o_all, torch.from_numpy(o))
+        dist.all_gather(l_all, torch.from_numpy(l))
+        merged, lse = oracle.merge_states(np.stack([t.numpy() for t in o_all]),
+                                          np.stack([t.numpy() for t in l_all]))
+        ref, ref_lse = oracle.attend(q, k, v, w.scale)
+        res = {"err": float(np.max(np.abs(merged - ref))),
+               "lse_err": float(np.max(np.abs(lse - ref_lse))), "shard": [a, b]}
+    finally:
+        dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"shard{rank}.json"), "w") as fh:
+        json.dump(res, fh)
+
+
+def test_sequence_split_across_two_gloo_ranks_merges_to_the_whole_attention(tmp_path):
+    port = _free_port()
+    mp.start_processes(_shard_main, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn")
+    r = [json.load(open(tmp_path / f"shard{i}.json")) for i in range(2)]
+    assert r[0]["shard"] == [0, 512] and r[1]["shard"] == [512, 1000]
+    for x in r:
+        assert x["err"] < 1e-12 and x["lse_err"] < 1e-12
+
+
 def test_two_gloo_ranks_reduce_time_and_bytes_and_seed_their_own_batches(tmp_path):
     port = _free_port()
     mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn")

@@ -303,6 +303,43 @@ def test_split_merge_equals_unsplit(split):
     assert np.max(np.abs(o2 - o1)) < 1e-12 and np.max(np.abs(l2 - l1)) < 1e-12
 
 
+@pytest.mark.parametrize("cuts", [(0, 157), (0, 64, 157), (0, 0, 40, 41, 100, 157), (0, 157, 157)])
+def test_merge_of_shards_equals_attention_over_all_keys(cuts):
+    """A context cut into consecutive shards (some empty), attended shard by shard and merged
+    from the (out, lse) pairs alone, gives attention over the whole context."""
+    q = _f64(_bf16((8, 32), 51))
+    k = _f64(_bf16((157, 2, 32), 52, scale=2.0))
+    v = _f64(_bf16((157, 2, 32), 53))
+    o_all, l_all = oracle.attend(q, k, v, 0.2)
+    outs, lses = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if b > a:
+            o, l = oracle.attend(q, k[a:b], v[a:b], 0.2)
+        else:                                   # a shard with no key
+            o, l = np.full((8, 32), np.nan), np.full(8, -np.inf)
+        outs.append(o)
+        lses.append(l)
+    o_m, l_m = oracle.merge_states(np.stack(outs), np.stack(lses))
+    assert np.max(np.abs(o_m - o_all)) < 1e-12 and np.max(np.abs(l_m - l_all)) < 1e-12
+
+
+def test_merge_states_special_cases():
+    rng = np.random.default_rng(54)
+    o = rng.standard_normal((3, 5, 8))
+    # one source: unchanged
+    m1, l1 = oracle.merge_states(o[:1], np.array([[0.5, -1.0, 2.0, 0.0, 3.0]]))
+    assert np.array_equal(m1, o[0]) and np.allclose(l1, [0.5, -1.0, 2.0, 0.0, 3.0], atol=1e-15)
+    # equal lse: the plain mean, and lse grows by log n
+    m3, l3 = oracle.merge_states(o, np.zeros((3, 5)))
+    assert np.allclose(m3, o.mean(0), atol=1e-15) and np.allclose(l3, np.log(3.0), atol=1e-15)
+    # weights exp(lse_r) / sum: lse (0, log 3) gives weights 1/4 and 3/4
+    m2, _ = oracle.merge_states(o[:2], np.stack([np.zeros(5), np.full(5, np.log(3.0))]))
+    assert np.allclose(m2, 0.25 * o[0] + 0.75 * o[1], atol=1e-14)
+    # a row whose sources are all empty: out 0, lse -inf
+    me, le = oracle.merge_states(o[:2], np.full((2, 5), -np.inf))
+    assert np.array_equal(me, np.zeros((5, 8))) and np.all(le == -np.inf)
+
+
 def test_empty_context_attends_to_nothing():
     q = _f64(_bf16((4, 8), 49))
     out, lse = oracle.attend(q, np.zeros((0, 2, 8)), np.zeros((0, 2, 8)), 0.5)
