@@ -31,7 +31,9 @@ def declared_functions(header=None):
 
 def test_header_declares_the_expected_calls():
     names = declared_functions("kv_paged.h")
-    for must in ("kv_pool_create", "paged_kv_append", "paged_decode_attention"):
+    for must in ("kv_pool_create", "paged_kv_append", "paged_decode_attention",
+                 "paged_decode_attention_split_merge", "paged_merge_attention_states",
+                 "paged_decode_step", "paged_attention_multi_query"):
         assert must in names
     assert len(names) >= 12
     bm = declared_functions("kv_block_manager.h")
@@ -70,9 +72,29 @@ def test_calls_on_a_null_pool_are_rejected(lib):
         kp.KV_ERR_INVALID_ARG
     assert lib.paged_decode_attention(None, None, 8, None, 4, None, 1, 1.0, 0, None, 0, None, None,
                                       None) == kp.KV_ERR_INVALID_ARG
+    assert lib.paged_decode_attention_split_merge(None, None, 8, None, 4, None, 1, 1.0, 0, None, 0,
+                                                  None, None, None) == kp.KV_ERR_INVALID_ARG
     assert lib.kv_pool_destroy(None) == kp.KV_OK
     bits = ctypes.c_uint32()
     assert lib.kv_pool_device_errors(None, ctypes.byref(bits), 0) == kp.KV_ERR_INVALID_ARG
+
+
+def test_merge_attention_states_validates_on_the_host(lib):
+    """Bad sizes, missing or misaligned pointers are rejected before any launch (the
+    pointers are never dereferenced); no rows is a no-op."""
+    bad = kp.KV_ERR_INVALID_ARG
+    a16, a4 = 1 << 20, (1 << 20) + 4                  # 16-byte and only 4-byte aligned values
+    assert lib.paged_merge_attention_states(a16, a16, 0, 4, 64, a16, None, None) == bad
+    assert lib.paged_merge_attention_states(a16, a16, 2, -1, 64, a16, None, None) == bad
+    for d in (0, 4, 12, 1032):
+        assert lib.paged_merge_attention_states(a16, a16, 2, 4, d, a16, None, None) == bad
+    assert lib.paged_merge_attention_states(None, a16, 2, 4, 64, a16, None, None) == bad
+    assert lib.paged_merge_attention_states(a16, None, 2, 4, 64, a16, None, None) == bad
+    assert lib.paged_merge_attention_states(a16, a16, 2, 4, 64, None, None, None) == bad
+    assert lib.paged_merge_attention_states(a4, a16, 2, 4, 64, a16, None, None) == bad
+    assert lib.paged_merge_attention_states(a16, a16, 2, 4, 64, a4, None, None) == bad
+    assert lib.paged_merge_attention_states(a16, a16, 2, 4, 64, a16, a16 + 2, None) == bad
+    assert lib.paged_merge_attention_states(None, None, 2, 0, 64, None, None, None) == kp.KV_OK
 
 
 def test_pool_create_without_a_gpu_reports_a_cuda_error(lib):
