@@ -599,6 +599,17 @@ def run_ours(args, rank, world, local):
     d_end.record(stream)
     torch.cuda.synchronize()
     dec_avg_ms = d_start.elapsed_time(d_end) / args.steps
+
+    # ---- the append kernel alone: K launches back to back (rewriting the same slots)
+    a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a_start.record(stream)
+    for _ in range(args.steps):
+        kp.paged_kv_append(pool, stp["k"], stp["v"], tables, ctx, token_seq=stp["seq"],
+                           token_pos=stp["pos"], stream=stream)
+    a_end.record(stream)
+    torch.cuda.synchronize()
+    app_avg_ms = a_start.elapsed_time(a_end) / args.steps
     assert pool.device_errors() == 0, "device-side error during the timed region"
     if sampler is not None:
         time.sleep(0.2)
@@ -680,6 +691,12 @@ def run_ours(args, rank, world, local):
             "pct_of_peak": round(100 * value / peak, 2),
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
+            "append": {"kernel": "paged_kv_append_kernel (K launches back to back after the timed "
+                                 "steps)",
+                       "ms_per_call": round(app_avg_ms, 5), "bytes_per_call": app_bytes,
+                       "achieved_gbs": round(app_bytes / (app_avg_ms / 1e3) / 1e9, 2),
+                       "frac": round(app_bytes / (app_avg_ms / 1e3) / 1e9 / peak, 4),
+                       "bound": "launch latency (a few hundred KB per call)"},
             "roofline": {"kernel": KERNEL_NAMES[kernel_kind(s)]
                                    + ((" + paged_mla_merge_tc" + ("n" if kernel_kind(s) == "mla_tcn" else "")
                                        + " (the decode call's two launches; ")
