@@ -253,8 +253,9 @@ kv_status paged_decode_attention_split_merge(const kv_pool* pool, const void* q,
  *   lse_out: fp32 [rows] or NULL.  A row whose sources are all empty gets
  *   out = 0, lse = -inf.
  *   n_src >= 1; head_dim a multiple of 8 in [8, 1024]; rows == 0 is a no-op.
- *   fp32 arithmetic.  Asynchronous on `stream`; no allocation.  out must not
- *   overlap outs.
+ *   fp32 arithmetic.  Runs on the calling thread's current CUDA device (all
+ *   pointers must be device memory of that device), asynchronously on `stream`
+ *   (NULL = legacy default stream); no allocation.  out must not overlap outs.
  */
 kv_status paged_merge_attention_states(const void* outs, const float* lses, int n_src,
                                        long long rows, int head_dim, void* out, float* lse_out,
