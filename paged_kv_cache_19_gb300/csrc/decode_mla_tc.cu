@@ -223,7 +223,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         // ------------------------------------------------------------ partition, items, loads
         // Units: (half dq, head tile ht, sequence b, block) in that order (outer index
         // dq * head_tiles + ht), cut into equal contiguous ranges (mla_partition.cuh).
-        MlaPartition<TC_TOK> part;
+        MlaPartition<TC_TOK, MLA_SEG_PAD_WIDE> part;
         part.init(p, p.head_tiles * 2, lane);
         if (lane == 0) {
             prefetch_tensormap(&tmp);

@@ -272,7 +272,7 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 
     if (warp == 4) {
         // ------------------------------------------------------------ segments and loads
-        MlaPartition<TN_TOK> part;
+        MlaPartition<TN_TOK, MLA_SEG_PAD_NARROW> part;
         part.init(p, p.head_tiles, lane);
         if (lane == 0) {
             prefetch_tensormap(&tmp);

@@ -156,6 +156,11 @@ cudaError_t launch_mla_decode(int block_size, bool prod, dim3 grid, const CUtens
 // pieces of sequences cut by a range boundary are merged by a second kernel, launched
 // by launch_mla_decode_tc when max_splits > 1.
 constexpr int MLA_TC_HEADS = 128;
+// Positions the tcgen05 forms' partition adds before each sequence's blocks: the cost of
+// starting a segment (the queries' load and the epilogue), in blocks (mla_partition.cuh);
+// the values timed best on GB300.
+constexpr int MLA_SEG_PAD_WIDE = 4;
+constexpr int MLA_SEG_PAD_NARROW = 2;
 constexpr int MLA_TC_BLOCK = 64;
 cudaError_t prepare_mla_decode_tc();
 cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,

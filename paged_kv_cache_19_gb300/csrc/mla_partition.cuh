@@ -1,15 +1,21 @@
 // mla_partition.cuh -- the balanced static partition of the latent-attention
 // work shared by the tcgen05 MLA kernels.
 //
-// Units are (outer, sequence b, block) in that order, T = S * nouter of them, S
-// being the blocks of the whole batch (a sequence of ctx tokens has
-// ceil(ctx / tok) blocks) and `outer` whatever the kernel splits the heads into
-// (head tiles, times the latent halves for the wide form).  CTA c of the G that
-// have work takes the contiguous range [c T / G, (c + 1) T / G), with G chosen
-// so that a range holds at least split_blocks units; every CTA derives the same
-// partition from the context lengths, so no CTA waits for another.  A sequence
+// Units are (outer, sequence b, position) in that order, T = S * nouter of them,
+// `outer` being whatever the kernel splits the heads into (head tiles, times the
+// latent halves for the wide form).  A sequence of ctx tokens has nb =
+// ceil(ctx / tok) blocks and occupies PAD + nb positions (none when it is empty):
+// a pad, then its blocks.  The pad is no work; it stands for what starting a
+// segment costs a CTA (the queries' load, the epilogue), so that ranges holding
+// many sequence starts get fewer blocks (measured best on GB300: 2 positions for
+// the narrow form, 4 for the wide one).  S is the
+// positions of the whole batch.  CTA c of the G that have work takes the
+// contiguous range [c T / G, (c + 1) T / G), with G chosen so that a range holds
+// at least split_blocks positions; every CTA derives the same partition from the
+// context lengths, so no CTA waits for another.  A sequence
 // cut by range boundaries leaves one piece per CTA that holds some of its
-// units: piece `split` of `nsplit`, merged afterwards by log-sum-exp.
+// blocks: piece `split` of `nsplit`, merged afterwards by log-sum-exp.  A range
+// that holds only pad positions has no work.
 //
 // A CTA walks its range as segments (runs of blocks of one sequence and one
 // outer index), the last segment first: a sequence cut between CTA c and c + 1
@@ -28,7 +34,7 @@ struct MlaSegment {
     int outer, b, blk0, n, ctx, split, nsplit;
 };
 
-template <int TOK>
+template <int TOK, int PAD>
 struct MlaPartition {
     const MlaParams* p;
     long long S, T, gact, u0, u1, c;
@@ -75,20 +81,21 @@ struct MlaPartition {
                     x = x < 0 ? 0 : cap;
                 }
                 const int nb = (x + TOK - 1) / TOK;
+                const int wv = nb > 0 ? nb + PAD : 0;   // positions of the sequence
                 if (bb < p->batch && nb == 0 && bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
                     uint4* dst = reinterpret_cast<uint4*>(p->out + static_cast<size_t>(bb) * p->q_heads * MLA_DV);
                     for (int v = 0; v < p->q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
                     if (p->lse != nullptr)
                         for (int hh = 0; hh < p->q_heads; ++hh) p->lse[static_cast<size_t>(bb) * p->q_heads + hh] = -INFINITY;
                 }
-                int in = nb;
+                int in = wv;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int y = __shfl_up_sync(FULL_MASK, in, o);
                     if (lane >= o) in += y;
                 }
                 ctxv[i] = x;
-                nbv[i] = nb;
+                nbv[i] = wv;
                 incl[i] = in;
                 S += __shfl_sync(FULL_MASK, in, 31);
             }
@@ -153,8 +160,8 @@ struct MlaPartition {
         blk = u0 < u1 ? static_cast<int>(u0 % S - pre_first) : 0;
     }
 
-    // Warp-wide: the sequence holding unit x < T, and the number of blocks before it
-    // (prefix sums of the block counts, 32 sequences at a time).
+    // Warp-wide: the sequence holding position x < T, and the number of positions before
+    // it (prefix sums, 32 sequences at a time).
     __device__ void locate(long long x, int& b_at, long long& pre_at, int lane) const
     {
         const long long v = x % S;
@@ -163,7 +170,8 @@ struct MlaPartition {
         pre_at = 0;
         for (int b0 = 0; b0 < p->batch; b0 += 32) {
             const int bb = b0 + lane;
-            const int nb = bb < p->batch ? (seq_ctx(bb) + TOK - 1) / TOK : 0;
+            const int nbr = bb < p->batch ? (seq_ctx(bb) + TOK - 1) / TOK : 0;
+            const int nb = nbr > 0 ? nbr + PAD : 0;       // positions
             int in = nb;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -181,17 +189,20 @@ struct MlaPartition {
         }
     }
 
+    // A segment of blocks blk0 .. blk0 + n - 1 of a sequence whose positions start at ub
+    // (its pad): the pieces are the ranges holding its blocks.
     __device__ __forceinline__ MlaSegment make(int o, int bb, long long ub, int blk0, int n, int x, int nb) const
     {
         MlaSegment it;
-        const int cf = cta_of(ub);
+        const long long first = ub + PAD;   // position of block 0
+        const int cf = cta_of(first);
         it.outer = o;
         it.b = bb;
         it.blk0 = blk0;
         it.n = n;
         it.ctx = x;
         it.split = static_cast<int>(c) - cf;
-        it.nsplit = cta_of(ub + nb - 1) - cf + 1;
+        it.nsplit = cta_of(first + nb - 1) - cf + 1;
         return it;
     }
 
@@ -202,13 +213,18 @@ struct MlaPartition {
         it.n = -1;
         if (!last_done) {
             last_done = true;
-            return make(outer_l, b_last, ub_l, static_cast<int>(ls - ub_l), static_cast<int>(u1 - ls), ctx_l, nb_l);
+            // positions [ls, u1) of the last sequence; its blocks among them, if any
+            const long long r0 = ls - ub_l - PAD > 0 ? ls - ub_l - PAD : 0;
+            const long long r1 = u1 - ub_l - PAD;
+            if (r1 > r0)
+                return make(outer_l, b_last, ub_l, static_cast<int>(r0), static_cast<int>(r1 - r0), ctx_l, nb_l);
         }
         while (u < ls) {
             const int x = seq_ctx(b);
             const int nb = (x + TOK - 1) / TOK;
-            if (blk >= nb) {                        // next sequence (or next outer index)
-                pre += nb;
+            const int wv = nb > 0 ? nb + PAD : 0;
+            if (blk >= wv) {                        // next sequence (or next outer index)
+                pre += wv;
                 blk = 0;
                 if (++b == p->batch) {
                     b = 0;
@@ -217,11 +233,14 @@ struct MlaPartition {
                 }
                 continue;
             }
-            const int n = static_cast<int>(nb - blk < ls - u ? nb - blk : ls - u);
-            it = make(outer, b, static_cast<long long>(outer) * S + pre, blk, n, x, nb);
+            const int n = static_cast<int>(wv - blk < ls - u ? wv - blk : ls - u);
+            const int r0 = blk - PAD > 0 ? blk - PAD : 0;
+            const int r1 = blk + n - PAD;
+            const long long ub = static_cast<long long>(outer) * S + pre;
             u += n;
             blk += n;
-            return it;
+            if (r1 > r0) return make(outer, b, ub, r0, r1 - r0, x, nb);
+            // only pad positions of this sequence: no work, walk on
         }
         return it;
     }

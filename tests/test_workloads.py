@@ -66,10 +66,14 @@ def test_decode_bytes_counts_kv_and_partials():
     assert many["partials"] == 4 * 8 * (64 + 2) * 4 * 2
 
 
-def _brute_force_pieces(nb, tiles, split_blocks, grid, halves=2):
-    """Assign every unit (latent half / head tile, sequence, block) to its range by
-    scanning the range starts, then count the distinct ranges each sequence touches."""
-    units = [(outer, b) for outer in range(tiles * halves) for b, n in enumerate(nb) for _ in range(n)]
+def _brute_force_pieces(nb, tiles, split_blocks, grid, halves=2, pad=None):
+    """Assign every position (latent half / head tile, sequence, position) to its range by
+    scanning the range starts, then count the distinct ranges holding each sequence's
+    blocks (a sequence's first `pad` positions hold none; by default the form's pad)."""
+    if pad is None:
+        pad = accounting.MLA_SEG_PAD_WIDE if halves == 2 else accounting.MLA_SEG_PAD_NARROW
+    units = [(outer, b, j >= pad) for outer in range(tiles * halves) for b, n in enumerate(nb)
+             for j in range(n + pad if n else 0)]
     T = len(units)
     g = max(1, min(grid, T // split_blocks))
     starts = [c * T // g for c in range(g + 1)]
@@ -81,8 +85,9 @@ def _brute_force_pieces(nb, tiles, split_blocks, grid, halves=2):
         owner.append(c)
     sizes = [starts[c + 1] - starts[c] for c in range(g)]
     seen = {}
-    for (key, c) in zip(units, owner):
-        seen.setdefault(key, set()).add(c)
+    for ((outer, b, real), c) in zip(units, owner):
+        if real:
+            seen.setdefault((outer, b), set()).add(c)
     pieces = [len(seen[(outer, b)]) for outer in range(tiles * halves) for b, n in enumerate(nb) if n > 0]
     return pieces, sizes, g
 
@@ -122,3 +127,92 @@ def test_mla_narrow_pieces_match_a_brute_force_partition(ctx, heads, split_block
     if g > 1:
         assert min(sizes) >= split_blocks
     assert max(want) <= (max(nb) - 1 + split_blocks - 1) // split_blocks + 1
+
+
+def _walk_partition(nb, nouter, split_blocks, grid, pad):
+    """The tensor-core MLA kernels' partition walk restated on the host: per CTA, the
+    segments (outer, sequence, first block, blocks, split, nsplit) it hands on, the last
+    one first, from the same integer arithmetic as the device code."""
+    wv = [n + pad if n else 0 for n in nb]
+    S = sum(wv)
+    T = S * nouter
+    gact = min(grid, max(1, T // split_blocks))
+    pre = [sum(wv[:i]) for i in range(len(nb))]
+
+    def cta_of(x):
+        return ((x + 1) * gact - 1) // T
+
+    def locate(v):
+        for b in range(len(nb)):
+            if wv[b] and pre[b] <= v < pre[b] + wv[b]:
+                return b, pre[b]
+        raise AssertionError("position outside the batch")
+
+    def make(c, o, bb, ub, blk0, n):
+        first = ub + pad
+        cf = cta_of(first)
+        return (o, bb, blk0, n, c - cf, cta_of(first + nb[bb] - 1) - cf + 1)
+
+    segs = {}
+    for c in range(grid):
+        u0 = c * T // gact if c < gact else T
+        u1 = (c + 1) * T // gact if c < gact else T
+        out = []
+        if u0 < u1:
+            b_first, pre_first = locate(u0 % S)
+            b_last, pre_last = locate((u1 - 1) % S)
+            outer_l = (u1 - 1) // S
+            ub_l = outer_l * S + pre_last
+            ls = max(ub_l, u0)
+            r0, r1 = max(ls - ub_l - pad, 0), u1 - ub_l - pad
+            if r1 > r0:
+                out.append(make(c, outer_l, b_last, ub_l, r0, r1 - r0))
+            u, outer, b, p_, blk = u0, u0 // S, b_first, pre_first, u0 % S - pre_first
+            while u < ls:
+                if blk >= wv[b]:
+                    p_ += wv[b]
+                    blk = 0
+                    b += 1
+                    if b == len(nb):
+                        b, p_, outer = 0, 0, outer + 1
+                    continue
+                n = min(wv[b] - blk, ls - u)
+                r0, r1 = max(blk - pad, 0), blk + n - pad
+                ub = outer * S + p_
+                u += n
+                blk += n
+                if r1 > r0:
+                    out.append(make(c, outer, b, ub, r0, r1 - r0))
+        segs[c] = out
+    return segs
+
+
+@pytest.mark.parametrize("pad", [0, accounting.MLA_SEG_PAD_NARROW, accounting.MLA_SEG_PAD_WIDE, 7])
+def test_mla_partition_walk_covers_every_block_once(pad):
+    rng = np.random.default_rng(17)
+    for trial in range(300):
+        batch = int(rng.integers(1, 40))
+        nb = [int(x) if rng.random() > 0.15 else 0 for x in rng.integers(1, 70, size=batch)]
+        if sum(nb) == 0:
+            nb[0] = 1
+        nouter = int(rng.choice([1, 2, 3, 4, 6]))
+        split_blocks = int(rng.choice([1, 2, 4, 13]))
+        grid = int(rng.choice([1, 7, 33, 152]))
+        segs = _walk_partition(nb, nouter, split_blocks, grid, pad)
+        covered = {}
+        for c, lst in segs.items():
+            keys = [(o, b) for (o, b, *_rest) in lst]
+            assert len(keys) == len(set(keys)), "two segments of one sequence in one CTA"
+            for (o, b, blk0, n, split, nsplit) in lst:
+                assert n >= 1 and 0 <= blk0 and blk0 + n <= nb[b]
+                assert 0 <= split < nsplit
+                covered.setdefault((o, b), []).append((blk0, n, split, nsplit))
+        want_pieces, _, _ = _brute_force_pieces(nb, nouter, split_blocks, grid, halves=1, pad=pad)
+        keys = [(o, b) for o in range(nouter) for b in range(batch) if nb[b]]
+        assert sorted(covered) == sorted(keys)
+        for key, want in zip(keys, want_pieces):
+            parts = sorted(covered[key])
+            blocks = [j for (blk0, n, _, _) in parts for j in range(blk0, blk0 + n)]
+            assert blocks == list(range(nb[key[1]])), (trial, key)
+            assert {s for (_, _, s, _) in parts} == set(range(want))
+            assert all(ns == want for (_, _, _, ns) in parts)

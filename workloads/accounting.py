@@ -82,24 +82,35 @@ def decode_flops(w) -> int:
     return int(4 * w.context_lens.astype(np.int64).sum() * s.head_dim * s.q_heads * s.q_len)
 
 
-def mla_tc_pieces(w, split_blocks: int, grid: int, head_tile: int = 128, halves: int = 2) -> np.ndarray:
+# Positions the tensor-core MLA partition puts before each sequence's blocks (the cost of
+# starting a segment, in blocks): the wide form's and the narrow form's.
+MLA_SEG_PAD_WIDE = 4
+MLA_SEG_PAD_NARROW = 2
+
+
+def mla_tc_pieces(w, split_blocks: int, grid: int, head_tile: int = 128, halves: int = 2,
+                  pad: int | None = None) -> np.ndarray:
     """Pieces each (outer, sequence) is cut into by a tensor-core MLA decode's partition:
-    its units (outer, sequence, block) -- outer = (latent half, head tile) for the wide
-    form (tiles of 128 heads, two halves), the head tile for the narrow one (tiles of 16,
-    halves=1) -- T in all, are cut into G = min(grid, T // split_blocks) (at least 1) equal
-    contiguous ranges, range c = [c T / G, (c + 1) T / G); a sequence with blocks is cut at
-    every range boundary inside it.  Same integer arithmetic as the kernels."""
+    its positions (outer, sequence, position) -- outer = (latent half, head tile) for the
+    wide form (tiles of 128 heads, two halves), the head tile for the narrow one (tiles of
+    16, halves=1); a sequence with nb blocks has pad + nb positions, the pad first (none
+    when empty) -- T in all, are cut into G = min(grid, T // split_blocks) (at least 1)
+    equal contiguous ranges, range c = [c T / G, (c + 1) T / G); a sequence is cut at every
+    range boundary among its blocks.  Same integer arithmetic as the kernels."""
+    if pad is None:
+        pad = MLA_SEG_PAD_WIDE if halves == 2 else MLA_SEG_PAD_NARROW
     nb = _nb(w)
     tiles = -(-w.spec.q_heads // head_tile)
-    S = int(nb.sum())
+    wv = np.where(nb > 0, nb + pad, 0).astype(np.int64)
+    S = int(wv.sum())
     T = S * tiles * halves
     if T == 0:
         return np.zeros(0, dtype=np.int64)
     g = max(1, min(grid, T // max(1, split_blocks)))
-    pre = np.concatenate([[0], np.cumsum(nb)[:-1]]).astype(np.int64)
+    pre = np.concatenate([[0], np.cumsum(wv)[:-1]]).astype(np.int64)
     out = []
     for outer in range(tiles * halves):
-        ub = outer * S + pre
+        ub = outer * S + pre + pad                # position of each sequence's block 0
         for u, n in zip(ub, nb):
             if n == 0:
                 continue
