@@ -61,6 +61,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="measure only --config (no other workloads in the same run)")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=3.0,
+                    help="target CPU time of the oracle baseline of each other workload")
     return ap.parse_args()
 
 
@@ -492,6 +496,275 @@ def stage(w, device):
     return pool, tables, ctx, step
 
 
+NOMINAL_HBM_GBS = 8000.0          # GB300 HBM3e, nominal (about 8 TB/s)
+# The workloads measured in the same run after the headline one (one GPU only): the other
+# bench configurations, the multi-token verify pass and both latent-attention layers.
+EXTRA_CONFIGS = ["long_context", "ragged_prefix", "mha_fp8", "llama3_8b_verify4",
+                 "deepseek_mla", "deepseek_mla_tp8"]
+
+
+class Staged:
+    """One workload resident on the GPU and the library calls the bench times."""
+
+    def __init__(self, w, device, split_override):
+        import torch
+        import paged_kv_cache_19_gb300 as kp
+        self.kp = kp
+        self.w = w
+        s = self.s = w.spec
+        self.device = device
+        self.split_req = s.split_tokens if split_override is None else split_override
+        self.pool, self.tables, self.ctx, self.stp = stage(w, device)
+        self.q = self.stp["q"]
+        if s.mla:
+            self.split_tokens, self.max_splits = kp.paged_mla_decode_plan(
+                self.pool, s.batch, s.q_heads, w.max_blocks, self.split_req)
+            ws_bytes = kp.paged_mla_workspace_size(self.pool, s.batch, s.q_heads, w.max_blocks,
+                                                   self.split_req)
+            self.out = torch.empty(s.batch, s.q_heads, s.latent_dim, dtype=torch.bfloat16,
+                                   device=device)
+        else:
+            self.split_tokens, self.max_splits = kp.paged_decode_plan(
+                self.pool, s.batch, s.q_heads, w.max_blocks, self.split_req)
+            ws_bytes = kp.paged_multi_query_workspace_size(self.pool, s.batch, s.q_heads, s.q_len,
+                                                           w.max_blocks, self.split_req)
+            self.out = torch.empty_like(self.q)
+        self.workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.lse = torch.empty(self.q.shape[:-1], dtype=torch.float32, device=device)
+        self.stream = torch.cuda.current_stream()
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.dec_bytes = decode_bytes(w, self.split_tokens, sms)
+        self.app_bytes = accounting.mla_append_bytes(w) if s.mla else accounting.append_bytes(w)
+        self.step_bytes = self.dec_bytes["total"] + self.app_bytes
+        # append + decode; the tensor-core MLA forms add their merge kernel when sequences
+        # can be cut into pieces (the other kernels merge inside the decode kernel)
+        self.two_kernels = kernel_kind(s) in ("mla_tc", "mla_tcn") and self.max_splits > 1
+        self.launches_per_step = 3 if self.two_kernels else 2
+
+    def attend(self, out=None):
+        kp, s, w = self.kp, self.s, self.w
+        out = self.out if out is None else out
+        if s.mla:
+            kp.paged_mla_decode_attention(self.pool, self.q, self.tables, self.ctx, w.scale,
+                                          kv_split_tokens=self.split_req, workspace=self.workspace,
+                                          out=out, lse=self.lse, stream=self.stream,
+                                          latent_dim=s.latent_dim)
+        elif s.q_len == 1:
+            kp.paged_decode_attention(self.pool, self.q, self.tables, self.ctx, w.scale,
+                                      kv_split_tokens=self.split_req, workspace=self.workspace,
+                                      out=out, lse=self.lse, stream=self.stream)
+        else:
+            kp.paged_attention_multi_query(self.pool, self.q, self.tables, self.ctx, w.scale,
+                                           kv_split_tokens=self.split_req,
+                                           workspace=self.workspace, out=out, lse=self.lse,
+                                           stream=self.stream)
+
+    def run_step(self, kk, vv, qq, tt, cc, out=None):
+        """One decode step through the public API: append + attention in one call, the
+        attention overlapping the append -- paged_decode_step for K/V caches,
+        paged_mla_decode_step for latent pools.  The step's tokens are the last q_len of
+        every sequence, in sequence order, which is the layout both calls take."""
+        kp, s, w = self.kp, self.s, self.w
+        out = self.out if out is None else out
+        if s.mla:
+            kp.paged_mla_decode_step(self.pool, kk, qq, tt, cc, w.scale,
+                                     kv_split_tokens=self.split_req, workspace=self.workspace,
+                                     out=out, lse=self.lse, stream=self.stream,
+                                     latent_dim=s.latent_dim)
+        else:
+            kp.paged_decode_step(self.pool, kk, vv, qq, tt, cc, w.scale,
+                                 kv_split_tokens=self.split_req, workspace=self.workspace,
+                                 out=out, lse=self.lse, stream=self.stream)
+
+    def step(self):
+        self.run_step(self.stp["k"], self.stp["v"], self.q, self.tables, self.ctx)
+
+    def _loop_ms(self, fn, n):
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(self.stream)
+        for _ in range(n):
+            fn()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def decode_ms(self, n):
+        """The decode kernel alone: n launches back to back; mean ms per call."""
+        return self._loop_ms(self.attend, n) / n
+
+    def append_ms(self, n):
+        """The append kernel alone: n launches back to back (rewriting the same slots)."""
+        kp, stp = self.kp, self.stp
+
+        def app():
+            kp.paged_kv_append(self.pool, stp["k"], stp["v"], self.tables, self.ctx,
+                               token_seq=stp["seq"], token_pos=stp["pos"], stream=self.stream)
+
+        return self._loop_ms(app, n) / n
+
+    def per_call_us(self, n):
+        """The decode kernel per call, L2 flushed before each (a read of twice the L2 size
+        between the calls, outside the event pair: it evicts every earlier line and, unlike
+        a write, leaves no dirty lines for the timed kernel to write back)."""
+        import torch
+        flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=self.device)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n)]
+        for e0, e1 in pairs:
+            flush.sum()
+            e0.record(self.stream)
+            self.attend()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        del flush
+        return sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in pairs)
+
+    def e2e(self, steps, warmup, world, all_bytes):
+        """The step end to end: every step copies its inputs from pinned host memory and
+        reads its output back.  Two device input buffers and two outputs let step i + 1's
+        host-to-device copy and step i's device-to-host copy run on a copy stream while
+        step i + 1 / step i computes; every step still moves its own bytes both ways."""
+        import torch
+        stp = self.stp
+        inputs = [("q", self.q), ("k", stp["k"]), ("tables", self.tables), ("ctx", self.ctx)]
+        if stp["v"] is not None:
+            inputs.append(("v", stp["v"]))
+        if stp["seq"] is not None:
+            inputs += [("seq", stp["seq"]), ("pos", stp["pos"])]
+        # the step's inputs packed into one pinned host buffer (16-byte aligned pieces) and
+        # copied with one host-to-device copy per step into a device buffer whose views the
+        # call takes
+        offs, total = {}, 0
+        for name, t in inputs:
+            offs[name] = total
+            total += -(-t.numel() * t.element_size() // 16) * 16
+        h_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        d_bufs = [torch.empty(total, dtype=torch.uint8, device=self.device) for _ in range(2)]
+
+        def view(buf, name, t):
+            n = t.numel() * t.element_size()
+            return buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+
+        for name, t in inputs:
+            view(h_buf, name, t).copy_(t.cpu())
+        views = [{name: view(b, name, t) for name, t in inputs} for b in d_bufs]
+        outs = [self.out, torch.empty_like(self.out)]
+        h_outs = [torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+                  for _ in range(2)]
+        comp = self.stream
+        copy = torch.cuda.Stream(device=self.device)
+        ev = lambda: torch.cuda.Event()                                  # noqa: E731
+        in_ready, done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        for e in done + out_read:
+            e.record(comp)
+
+        def h2d(i):
+            j = i % 2
+            copy.wait_event(done[j])               # step i - 2 has finished reading d_bufs[j]
+            with torch.cuda.stream(copy):
+                d_bufs[j].copy_(h_buf, non_blocking=True)
+            in_ready[j].record(copy)
+
+        def run(n):
+            h2d(0)
+            for i in range(n):
+                j = i % 2
+                if i + 1 < n:
+                    h2d(i + 1)                     # overlaps step i
+                comp.wait_event(in_ready[j])
+                comp.wait_event(out_read[j])       # step i - 2's output has been read
+                d = views[j]
+                self.run_step(d["k"], d.get("v"), d["q"], d["tables"], d["ctx"], out=outs[j])
+                done[j].record(comp)
+                copy.wait_event(done[j])
+                with torch.cuda.stream(copy):
+                    h_outs[j].copy_(outs[j], non_blocking=True)
+                out_read[j].record(copy)
+
+        run(max(3, warmup))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(copy)
+        run(steps)
+        e1.record(copy)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        bo = h_outs[0].numel() * h_outs[0].element_size()
+        return {"value": round(all_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": total, "d2h_bytes_per_step": bo,
+                "ms_per_step": round(e2e_ms / steps, 5),
+                "overlap": "double-buffered inputs and outputs; copies on a second stream "
+                           "overlap the neighbouring steps' compute"}
+
+    def destroy(self):
+        self.pool.destroy()
+
+
+def roofline_obj(st, dec_ms, peak, peak_kind, config_name):
+    """The roofline figures of a workload's decode kernel: algorithmic bytes per launch over
+    the back-to-back launch time, against the measured copy bandwidth and the nominal HBM
+    bandwidth, with the DRAM traffic of an ncu capture of the same sources."""
+    s = st.s
+    achieved = st.dec_bytes["total"] / (dec_ms / 1e3) / 1e9
+    traffic, traffic_src = profiled_traffic(config_name)
+    kind = kernel_kind(s)
+    return {"kernel": KERNEL_NAMES[kind]
+                      + ((" + paged_mla_merge_tc" + ("n" if kind == "mla_tcn" else "")
+                          + " (the decode call's two launches; ") if st.two_kernels else
+                         " (one launch per decode call, in-kernel split-KV merge; ")
+                      + "K calls timed back to back)",
+            "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic, "traffic_source": traffic_src,
+            "algorithmic_bytes_per_launch": st.dec_bytes["total"],
+            "algorithmic_bytes_unique_per_launch": st.dec_bytes["total_unique"],
+            **(mla_roofline(st.w, st.dec_bytes, dec_ms, peak) if s.mla else {})}
+
+
+def measure_extra(name, args, device, peak, peak_kind):
+    """One more workload in the same run: the step and the decode kernel back to back, the
+    decode per call with L2 flushed, and the oracle on a short sample of host work."""
+    import torch
+    w = workloads.make(workloads.CONFIGS[name])
+    st = Staged(w, device, None)
+    steps = 200
+    for _ in range(max(3, args.warmup)):
+        st.step()
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() == 0, f"device-side error during warm-up ({name})"
+    step_ms = st._loop_ms(st.step, steps) / steps
+    dec_ms = st.decode_ms(steps)
+    per_call = st.per_call_us(20)
+    assert st.pool.device_errors() == 0, f"device-side error during the timed calls ({name})"
+    res = {
+        "workload": name, "steps": steps,
+        "config": workload_config(w, st.split_tokens, st.max_splits, 1),
+        "step_ms": round(step_ms, 5),
+        "step_gbs": round(st.step_bytes / (step_ms / 1e3) / 1e9, 2),
+        "kv_tokens_per_s": round(w.total_tokens / (step_ms / 1e3), 1),
+        "decode_us_back_to_back": round(dec_ms * 1e3, 2),
+        "decode_per_call": {"calls": len(per_call), "median_us": round(statistics.median(per_call), 2),
+                            "min_us": round(per_call[0], 2),
+                            "l2": "flushed before each call (a read of twice the L2 size)",
+                            "median_gbs": round(st.dec_bytes["total"]
+                                                / (statistics.median(per_call) * 1e-6) / 1e9, 2)},
+        "roofline": roofline_obj(st, dec_ms, peak, peak_kind, name),
+    }
+    out = st.out
+    st.destroy()
+    if not args.no_cpu_baseline and w.spec.q_len == 1:
+        res["cpu_baseline"] = cpu_baseline(w, args.extra_cpu_seconds, gpu_out=out)
+    del out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local):
     import torch
     import paged_kv_cache_19_gb300 as kp
@@ -502,66 +775,13 @@ def run_ours(args, rank, world, local):
     kp.load_library()
     w = workloads.make(rank_spec(args.config, rank))
     s = w.spec
-    split_req = s.split_tokens if args.split_tokens is None else args.split_tokens
-    pool, tables, ctx, stp = stage(w, device)
-    q = stp["q"]
-    if s.mla:
-        split_tokens, max_splits = kp.paged_mla_decode_plan(pool, s.batch, s.q_heads, w.max_blocks,
-                                                            split_req)
-        ws_bytes = kp.paged_mla_workspace_size(pool, s.batch, s.q_heads, w.max_blocks, split_req)
-        out = torch.empty(s.batch, s.q_heads, s.latent_dim, dtype=torch.bfloat16, device=device)
-    else:
-        split_tokens, max_splits = kp.paged_decode_plan(pool, s.batch, s.q_heads, w.max_blocks,
-                                                        split_req)
-        ws_bytes = kp.paged_multi_query_workspace_size(pool, s.batch, s.q_heads, s.q_len,
-                                                       w.max_blocks, split_req)
-        out = torch.empty_like(q)
-    workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream()
-
-    def attend(qq, tt, cc):
-        if s.mla:
-            kp.paged_mla_decode_attention(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
-                                          workspace=workspace, out=out, lse=lse, stream=stream,
-                                          latent_dim=s.latent_dim)
-        elif s.q_len == 1:
-            kp.paged_decode_attention(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
-                                      workspace=workspace, out=out, lse=lse, stream=stream)
-        else:
-            kp.paged_attention_multi_query(pool, qq, tt, cc, w.scale, kv_split_tokens=split_req,
-                                           workspace=workspace, out=out, lse=lse, stream=stream)
-
-    def run_step(kk, vv, qq, tt, cc, sq, ps):
-        """One decode step through the public API: append + attention in one call, the
-        attention overlapping the append -- paged_decode_step for K/V caches,
-        paged_mla_decode_step for latent pools.  The step's tokens are the last q_len of
-        every sequence, in sequence order, which is the layout both calls take."""
-        if s.mla:
-            kp.paged_mla_decode_step(pool, kk, qq, tt, cc, w.scale, kv_split_tokens=split_req,
-                                     workspace=workspace, out=out, lse=lse, stream=stream,
-                                     latent_dim=s.latent_dim)
-        else:
-            kp.paged_decode_step(pool, kk, vv, qq, tt, cc, w.scale, kv_split_tokens=split_req,
-                                 workspace=workspace, out=out, lse=lse, stream=stream)
-
-    def step():
-        run_step(stp["k"], stp["v"], q, tables, ctx, stp["seq"], stp["pos"])
-
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    dec_bytes = decode_bytes(w, split_tokens, sms)
-    app_bytes = accounting.mla_append_bytes(w) if s.mla else accounting.append_bytes(w)
-    step_bytes = dec_bytes["total"] + app_bytes
-    # append + decode; the tensor-core MLA forms add their merge kernel when sequences can
-    # be cut into pieces (the other kernels merge inside the decode kernel)
-    two_kernels = kernel_kind(s) in ("mla_tc", "mla_tcn") and max_splits > 1
-    launches_per_step = 3 if two_kernels else 2
-    # (the decode-only roofline loop after the timed region launches K more decode kernels)
+    st = Staged(w, device, args.split_tokens)
+    stream = st.stream
 
     for _ in range(max(3, args.warmup)):
-        step()
+        st.step()
     torch.cuda.synchronize()
-    assert pool.device_errors() == 0, "device-side error during warm-up"
+    assert st.pool.device_errors() == 0, "device-side error during warm-up"
 
     gpu_uuid = None
     try:
@@ -582,7 +802,7 @@ def run_ours(args, rank, world, local):
     host0 = time.time()
     t_start.record(stream)
     for _ in range(args.steps):
-        step()
+        st.step()
     t_end.record(stream)
     torch.cuda.synchronize()
     host1 = time.time()
@@ -590,43 +810,13 @@ def run_ours(args, rank, world, local):
     total_ms = t_start.elapsed_time(t_end)
     total_ms_max = max_over_ranks(total_ms, world)
 
-    # ---- the decode kernel alone: K launches back to back (roofline of the kernel)
-    d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    d_start.record(stream)
-    for _ in range(args.steps):
-        attend(q, tables, ctx)
-    d_end.record(stream)
-    torch.cuda.synchronize()
-    dec_avg_ms = d_start.elapsed_time(d_end) / args.steps
-
-    # ---- the decode kernel per call, L2 flushed before each (a read of twice the L2 size
-    # between the calls, outside the event pair: it evicts every earlier line and, unlike a
-    # write, leaves no dirty lines for the timed kernel to write back): median and minimum
-    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    # ---- the decode kernel alone (roofline of the kernel), per call with L2 flushed, and
+    # the append kernel alone
+    dec_avg_ms = st.decode_ms(args.steps)
     n_calls = min(50, max(5, args.steps))
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(n_calls)]
-    for e0, e1 in pairs:
-        flush.sum()
-        e0.record(stream)
-        attend(q, tables, ctx)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    per_call_us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in pairs)
-    del flush
-
-    # ---- the append kernel alone: K launches back to back (rewriting the same slots)
-    a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    a_start.record(stream)
-    for _ in range(args.steps):
-        kp.paged_kv_append(pool, stp["k"], stp["v"], tables, ctx, token_seq=stp["seq"],
-                           token_pos=stp["pos"], stream=stream)
-    a_end.record(stream)
-    torch.cuda.synchronize()
-    app_avg_ms = a_start.elapsed_time(a_end) / args.steps
-    assert pool.device_errors() == 0, "device-side error during the timed region"
+    per_call_us = st.per_call_us(n_calls)
+    app_avg_ms = st.append_ms(args.steps)
+    assert st.pool.device_errors() == 0, "device-side error during the timed region"
     if sampler is not None:
         time.sleep(0.2)
         sampler.stop()
@@ -634,66 +824,33 @@ def run_ours(args, rank, world, local):
     else:
         clocks = None
 
-    all_bytes = sum_over_ranks(step_bytes * args.steps, world)
+    all_bytes = sum_over_ranks(st.step_bytes * args.steps, world)
     value = all_bytes / (total_ms_max / 1e3) / 1e9
     kv_tok = sum_over_ranks(w.total_tokens * args.steps, world) / (total_ms_max / 1e3)
     peak, peak_kind = measured_peaks()
-    achieved = dec_bytes["total"] / (dec_avg_ms / 1e3) / 1e9
-    traffic, traffic_src = profiled_traffic(args.config)
 
     # ---- end to end: host (pinned) inputs copied in and the output copied out every step
-    e2e = None
-    if not args.no_e2e:
-        inputs = [("q", q), ("k", stp["k"]), ("tables", tables), ("ctx", ctx)]
-        if stp["v"] is not None:
-            inputs.append(("v", stp["v"]))
-        if stp["seq"] is not None:
-            inputs += [("seq", stp["seq"]), ("pos", stp["pos"])]
-        # the step's inputs packed into one pinned host buffer (16-byte aligned pieces) and
-        # copied with one host-to-device copy per step into one device buffer whose views
-        # the call takes
-        offs, total = {}, 0
-        for name, t in inputs:
-            offs[name] = total
-            total += -(-t.numel() * t.element_size() // 16) * 16
-        h_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-        d_buf = torch.empty(total, dtype=torch.uint8, device=device)
-
-        def view(buf, name, t):
-            n = t.numel() * t.element_size()
-            return buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
-
-        for name, t in inputs:
-            view(h_buf, name, t).copy_(t.cpu())
-        d = {name: view(d_buf, name, t) for name, t in inputs}
-        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        bi = total
-        bo = h_out.numel() * h_out.element_size()
-
-        def e2e_step():
-            d_buf.copy_(h_buf, non_blocking=True)
-            run_step(d["k"], d.get("v"), d["q"], d["tables"], d["ctx"], d.get("seq"), d.get("pos"))
-            h_out.copy_(out, non_blocking=True)
-
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
-        barrier(world)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-        e2e = {"value": round(all_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": round(e2e_ms / args.steps, 5)}
+    e2e = None if args.no_e2e else st.e2e(args.steps, args.warmup, world, all_bytes)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and s.q_len == 1:
-        cpu = cpu_baseline(w, args.cpu_seconds, gpu_out=out)
+        cpu = cpu_baseline(w, args.cpu_seconds, gpu_out=st.out)
+    line_cfg = workload_config(w, st.split_tokens, st.max_splits, world)
+    app_bytes = st.app_bytes
+    launches = st.launches_per_step * args.steps
+    roof = roofline_obj(st, dec_avg_ms, peak, peak_kind, args.config)
+    st.destroy()
+    del st
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, in the same run (one GPU only)
+    extra = None
+    if world == 1 and not args.no_extra:
+        extra = {}
+        for name in EXTRA_CONFIGS:
+            if name == args.config:
+                continue
+            extra[name] = measure_extra(name, args, device, peak, peak_kind)
 
     if rank == 0:
         line = {
@@ -703,40 +860,30 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if s.cache_dtype == "bf16" else "fp8_e4m3 cache, bf16 q/out",
             "data": "synthetic (seeded N(0,1) bf16, no trained weights)",
-            "config": workload_config(w, split_tokens, max_splits, world),
+            "config": line_cfg,
             "pct_of_peak": round(100 * value / peak, 2),
+            "pct_of_nominal_peak": round(100 * value / NOMINAL_HBM_GBS, 2),
             "kv_tokens_per_s": round(kv_tok, 1),
             "decode_ms_per_call": round(dec_avg_ms, 5),
             "decode_per_call": {"calls": n_calls, "median_us": round(statistics.median(per_call_us), 2),
                                 "min_us": round(per_call_us[0], 2),
                                 "l2": "flushed before each call (a read of twice the L2 size)",
-                                "median_gbs": round(dec_bytes["total"] / (statistics.median(per_call_us) * 1e-6) / 1e9, 2)},
+                                "median_gbs": round(roof["algorithmic_bytes_per_launch"]
+                                                    / (statistics.median(per_call_us) * 1e-6) / 1e9, 2)},
             "append": {"kernel": "paged_kv_append_kernel (K launches back to back after the timed "
                                  "steps)",
                        "ms_per_call": round(app_avg_ms, 5), "bytes_per_call": app_bytes,
                        "achieved_gbs": round(app_bytes / (app_avg_ms / 1e3) / 1e9, 2),
                        "frac": round(app_bytes / (app_avg_ms / 1e3) / 1e9 / peak, 4),
                        "bound": "launch latency (a few hundred KB per call)"},
-            "roofline": {"kernel": KERNEL_NAMES[kernel_kind(s)]
-                                   + ((" + paged_mla_merge_tc" + ("n" if kernel_kind(s) == "mla_tcn" else "")
-                                       + " (the decode call's two launches; ")
-                                      if two_kernels else
-                                      " (one launch per decode call, in-kernel split-KV merge; ")
-                                   + "K calls timed back to back after the timed steps)",
-                         "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                         "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                         "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "traffic_source": traffic_src,
-                         "algorithmic_bytes_per_launch": dec_bytes["total"],
-                         "algorithmic_bytes_unique_per_launch": dec_bytes["total_unique"],
-                         **(mla_roofline(w, dec_bytes, dec_avg_ms, peak) if s.mla else {})},
+            "roofline": roof,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks,
+            "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)
-    pool.destroy()
 
 
 def main():

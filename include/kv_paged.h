@@ -335,7 +335,11 @@ kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new,
  *     paged_decode_attention with your own workspace.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process, so a
+ *     cudaDeviceReset after that first call is not supported: the array is
+ *     created again at a new address that this call would not see.
+ *   - Arguments are validated before the array is touched: a rejected call
+ *     writes nothing to it and launches nothing.
  *   - All calls on a device share the one array, which keeps what the last
  *     call left.  The chunk counters that must start at zero are cleared by
  *     each call on its stream before its kernel; the partial results need no

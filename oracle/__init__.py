@@ -255,28 +255,43 @@ def decode_workload(w, seqs=None, threads: int = 1, cache_dtype: str | None = No
                   v_scale=w.v_scale, seqs=seqs, threads=threads)
 
 
-def pool_image(w, after_step: bool) -> tuple[np.ndarray, np.ndarray]:
+def pool_image(w, after_step: bool, threads: int = 1) -> tuple[np.ndarray, np.ndarray]:
     """Expected raw bytes of the K and V pools of a workload.
 
     Poisoned with 0xFF, then every prefilled token written; with after_step the
     token appended in this step as well.  Shape [num_blocks, bs, Hkv, d * elem].
+    threads > 1 writes disjoint sets of tokens in concurrent calls of the C routine:
+    every token has its own slot, so the image is the same whatever the order.
     """
     s = w.spec
     eb = w.elem_bytes
     shape = (w.num_blocks, s.block_size, s.kv_heads, s.head_dim * eb)
     kp = np.full(shape, 0xFF, dtype=np.uint8)
     vp = np.full(shape, 0xFF, dtype=np.uint8)
+
+    def write(rows, seq, pos):
+        n = rows.size
+        parts = max(1, min(threads, n // 4096))
+        cuts = [(i * n // parts, (i + 1) * n // parts) for i in range(parts)]
+
+        def one(c):
+            a, b = c
+            return append(kp, vp, s.cache_dtype, s.block_size, w.k[rows[a:b]], w.v[rows[a:b]],
+                          w.block_tables, w.context_lens, token_seq=seq[a:b], token_pos=pos[a:b],
+                          k_scale=w.k_scale, v_scale=w.v_scale)
+
+        if parts == 1:
+            bad = one(cuts[0])
+        else:
+            from concurrent.futures import ThreadPoolExecutor
+            with ThreadPoolExecutor(parts) as ex:
+                bad = sum(ex.map(one, cuts))
+        assert bad == 0
+
     if w.prefill_seq.size:
-        bad = append(kp, vp, s.cache_dtype, s.block_size, w.k[w.prefill_row], w.v[w.prefill_row],
-                     w.block_tables, w.context_lens, token_seq=w.prefill_seq,
-                     token_pos=w.prefill_pos, k_scale=w.k_scale, v_scale=w.v_scale)
-        assert bad == 0
+        write(w.prefill_row, w.prefill_seq, w.prefill_pos)
     if after_step:
-        rows = w.step_rows
-        bad = append(kp, vp, s.cache_dtype, s.block_size, w.k[rows], w.v[rows], w.block_tables,
-                     w.context_lens, token_seq=w.step_seq, token_pos=w.step_pos,
-                     k_scale=w.k_scale, v_scale=w.v_scale)
-        assert bad == 0
+        write(np.asarray(w.step_rows), np.asarray(w.step_seq), np.asarray(w.step_pos))
     return kp, vp
 
 
@@ -355,8 +370,27 @@ def mla_decode(q, cache, seq_start, context_lens, *, latent_dim: int, scale: flo
     return out, lse
 
 
-def mla_decode_workload(w, seqs=None):
-    """Oracle absorbed-MLA decode of a workload whose cache holds one vector per token."""
+def mla_decode_workload(w, seqs=None, threads: int = 1):
+    """Oracle absorbed-MLA decode of a workload whose cache holds one vector per token.
+
+    threads > 1 runs disjoint sets of sequences in concurrent calls of the C routine
+    (ctypes releases the interpreter lock); each sequence's arithmetic is unchanged."""
     s = w.spec
-    return mla_decode(w.q, w.k[:, 0, :], w.seq_start, w.context_lens, latent_dim=s.latent_dim,
-                      scale=w.scale, seqs=seqs)
+    seq_list = list(range(w.batch)) if seqs is None else [int(b) for b in seqs]
+
+    def run(part):
+        return mla_decode(w.q, w.k[:, 0, :], w.seq_start, w.context_lens, latent_dim=s.latent_dim,
+                          scale=w.scale, seqs=part)
+
+    if threads <= 1 or len(seq_list) <= 1:
+        return run(seq_list)
+    from concurrent.futures import ThreadPoolExecutor
+    parts = [seq_list[i::threads] for i in range(min(threads, len(seq_list)))]
+    with ThreadPoolExecutor(len(parts)) as ex:
+        res = list(ex.map(run, parts))
+    out = np.zeros((len(seq_list), s.q_heads, s.latent_dim), dtype=np.float64)
+    lse = np.zeros((len(seq_list), s.q_heads), dtype=np.float64)
+    for i, (o, l) in enumerate(res):
+        out[i::len(parts)] = o
+        lse[i::len(parts)] = l
+    return out, lse

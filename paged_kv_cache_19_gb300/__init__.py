@@ -9,7 +9,6 @@ CPU path, and importing a function without the built library raises.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -278,7 +277,7 @@ def paged_decode_workspace_size(pool: Pool, batch: int, q_heads: int, max_blocks
     return n.value
 
 
-def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: float | None = None,
+def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: float,
                            kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
                            stream=None):
     """Decode attention; q bf16 [B, Hq, 1, d] or [B, Hq, d].  Returns out (shape of q)."""
@@ -293,8 +292,6 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     _need(lse, torch.float32, "lse")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         need = paged_decode_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
         # zero-filled: it holds the per-sequence chunk counters of the in-kernel merge
@@ -310,7 +307,7 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
 
 
 def paged_decode_attention_split_merge(pool: Pool, q, block_tables, context_lens,
-                                       scale: float | None = None, kv_split_tokens: int = 0,
+                                       scale: float, kv_split_tokens: int = 0,
                                        workspace=None, out=None, lse=None, stream=None):
     """paged_decode_attention as two kernels: the split-KV grid, then a separate
     log-sum-exp merge kernel (same bits).  Returns out (shape of q)."""
@@ -325,8 +322,6 @@ def paged_decode_attention_split_merge(pool: Pool, q, block_tables, context_lens
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     _need(lse, torch.float32, "lse")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         need = paged_decode_workspace_size(pool, batch, q_heads, max_blocks, kv_split_tokens)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device) if need else None
@@ -374,7 +369,7 @@ def paged_multi_query_workspace_size(pool: Pool, batch: int, q_heads: int, q_len
     return n.value
 
 
-def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale: float | None = None,
+def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale: float,
                                 kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
                                 stream=None):
     """Attention of q_len new tokens per sequence; q bf16 [B, Hq, q_len, d].  Returns out."""
@@ -390,8 +385,6 @@ def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     _need(lse, torch.float32, "lse")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         need = paged_multi_query_workspace_size(pool, batch, q_heads, q_len, max_blocks,
                                                 kv_split_tokens)
@@ -408,7 +401,7 @@ def paged_attention_multi_query(pool: Pool, q, block_tables, context_lens, scale
 
 
 def paged_decode_step(pool: Pool, k_new, v_new, q, block_tables, context_lens,
-                      scale: float | None = None, kv_split_tokens: int = 0, workspace=None,
+                      scale: float, kv_split_tokens: int = 0, workspace=None,
                       out=None, lse=None, stream=None):
     """One decode step: append k_new / v_new (bf16 [B * q_len, Hkv, d]; row i is token i %
     q_len of sequence i / q_len, at position ctx - q_len + i % q_len), then the attention of
@@ -434,8 +427,6 @@ def paged_decode_step(pool: Pool, k_new, v_new, q, block_tables, context_lens,
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     _need(lse, torch.float32, "lse")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     if workspace is None:
         need = paged_multi_query_workspace_size(pool, batch, q_heads, q_len, max_blocks,
                                                 kv_split_tokens)

@@ -1057,6 +1057,15 @@ extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const v
     if (need > 0) {
         st = scratch_address(pool->device, &scratch);
         if (st != KV_OK) return st;
+    }
+    // Every argument is checked before the shared array is touched: a call that is
+    // rejected writes nothing to it and launches nothing.
+    kvp::DecodeParams p;
+    dim3 grid;
+    st = make_decode_launch(pool, q, q_heads, 1, block_tables, max_blocks, context_lens, batch,
+                            scale, kv_split_tokens, scratch, need, out, lse_out, &plan, &p, &grid);
+    if (st != KV_OK) return st;
+    if (need > 0) {
         // The per-unit chunk counts in the scratch must start at zero, whatever
         // an earlier (possibly failed) call left there.
         const WorkspaceLayout wl = workspace_layout(pool, batch, plan);
@@ -1067,6 +1076,5 @@ extern "C" kv_status paged_decode_attention_noalloc(const kv_pool* pool, const v
             return KV_ERR_CUDA;
         }
     }
-    return paged_decode_attention(pool, q, q_heads, block_tables, max_blocks, context_lens, batch,
-                                  scale, kv_split_tokens, scratch, need, out, lse_out, stream);
+    return launch_decode(pool, plan, grid, p, stream);
 }

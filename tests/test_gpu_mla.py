@@ -6,6 +6,8 @@ and averages its latent part (xuewyang.github.io/posts/kv, "MLA: how does decode
 get full-size keys and values back?").  Outputs within max |err| <= 2e-2 and
 relative L2 <= 5e-3, LSE within 2e-3; the latent pool's bytes bit for bit.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -56,8 +58,8 @@ def staged(request):
     st.destroy()
 
 
-def check(out, lse, w, seqs=None):
-    ref, ref_lse = oracle.mla_decode_workload(w, seqs=seqs)
+def check(out, lse, w, seqs=None, threads=1):
+    ref, ref_lse = oracle.mla_decode_workload(w, seqs=seqs, threads=threads)
     got = out if seqs is None else out[torch.as_tensor(seqs, device=out.device).long()]
     max_abs, rel, _ = compare(got, ref)
     assert max_abs <= MAX_ABS and rel <= REL_L2, (max_abs, rel)
@@ -155,16 +157,51 @@ def test_api_rejects_mismatched_pools():
 
 
 @pytest.mark.parametrize("config", ["deepseek_mla", "deepseek_mla_tp8"])
-def test_full_size_sampled(config):
+def test_full_size_parity(config):
+    """At the benchmark's sizes and in its launch configuration (append + attention in one
+    paged_mla_decode_step call): the whole latent pool bit for bit against the oracle's
+    image, and every sequence's output and LSE against the oracle."""
     w = workloads.make(workloads.CONFIGS[config])
+    st = Staged(w, step_append=False)
+    s = w.spec
+    out = torch.empty(w.batch, s.q_heads, s.latent_dim, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.batch, s.q_heads, dtype=torch.float32, device="cuda")
+    kp.paged_mla_decode_step(st.pool, st.k_new, st.q, st.tables, st.ctx, w.scale,
+                             kv_split_tokens=s.split_tokens, out=out, lse=lse,
+                             latent_dim=s.latent_dim)
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() == 0
+    threads = os.cpu_count() or 1
+    kimg, _ = oracle.pool_image(w, after_step=True, threads=threads)
+    kr, vr = st.pool.raw_bytes()
+    assert vr is None and tuple(kr.shape) == kimg.shape
+    for a in range(0, kimg.shape[0], 4096):
+        assert np.array_equal(kr[a:a + 4096].cpu().numpy(), kimg[a:a + 4096]), a
+    del kimg
+    check(out, lse, w, threads=threads)
+    out1, lse1 = st.mla()                        # the attention alone: the same bits
+    assert torch.equal(out.view(torch.int16), out1.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse1.view(torch.int32))
+    assert st.pool.device_errors() == 0
+    st.destroy()
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_tcgen05_batches_over_256_sequences(heads):
+    """Batches above 256 sequences take the tensor-core forms' prefix search over the
+    segment-padded positions (a different path from smaller batches); short ragged
+    sequences and small ranges give many segments per CTA."""
+    w = workloads.make(M(batch=300, q_heads=heads, block_size=64, ctx_uniform=(1, 400),
+                         seed=218, split_tokens=64))
     st = Staged(w)
     out, lse = st.mla()
     torch.cuda.synchronize()
-    rng = np.random.default_rng(11)
-    seqs = sorted(rng.choice(w.batch, size=3, replace=False).tolist())
-    seqs.append(int(np.argmax(w.context_lens)))
-    check(out, lse, w, seqs=seqs)
     assert st.pool.device_errors() == 0
+    check(out, lse, w, threads=os.cpu_count() or 1)
+    out2, lse2 = st.mla(split_tokens=0)
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() == 0
+    check(out2, lse2, w, threads=os.cpu_count() or 1)
     st.destroy()
 
 

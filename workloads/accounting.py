@@ -53,10 +53,10 @@ def decode_bytes(w, split_tokens: int) -> dict:
     row = 2 * s.kv_heads * s.head_dim * e                      # K and V of one token
     kv_logical = int(ctx.sum()) * row
     kv_unique = unique_kv_tokens(w) * row
+    # Each K/V element counts once, whatever the kernel does: a kernel that tiles a GQA
+    # group's query rows and reads a block once per tile shows the extra reads as DRAM
+    # traffic above these bytes, not as work of the method.
     rows = s.q_heads * s.q_len                                  # query rows per sequence
-    tiles = -(-(s.q_heads // s.kv_heads * s.q_len) // 16) if s.q_heads // s.kv_heads * s.q_len > 8 else 1
-    kv_logical *= tiles                                         # each row tile reads the K/V once
-    kv_unique *= tiles
     qo = 2 * w.batch * rows * s.head_dim * 2                    # q read + out written (bf16)
     meta = 4 * int(nb.sum()) + 4 * w.batch + 4 * w.batch * rows  # tables, ctx, lse
     sb = max(1, split_tokens // s.block_size)
