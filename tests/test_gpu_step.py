@@ -129,7 +129,7 @@ def test_step_rejects_bad_arguments_before_launching():
                              torch.zeros(1, 576, dtype=torch.bfloat16, device="cuda"),
                              torch.zeros(1, 16, 576, dtype=torch.bfloat16, device="cuda"),
                              torch.zeros(1, 1, dtype=torch.int32, device="cuda"),
-                             torch.ones(1, dtype=torch.int32, device="cuda"))
+                             torch.ones(1, dtype=torch.int32, device="cuda"), 0.1)
     lat.destroy()
 
 
