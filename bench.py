@@ -72,6 +72,7 @@ def parse_args():
 KERNEL_SOURCES = {
     "gqa": ["decode_kernel.cuh", "decode_common.cuh", "decode_bf16.cu", "decode_fp8.cu",
             "device_common.cuh"],
+    "gqa_heads": ["decode_heads.cuh", "decode_heads.cu", "decode_common.cuh", "device_common.cuh"],
     "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
     "mla_tc": ["decode_mla_tc.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
                "device_common.cuh"],
@@ -80,18 +81,20 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_kind(spec) -> str:
-    """Which decode kernel a workload runs: the GQA kernel, or a form of the latent decode
-    (tcgen05 for blocks of 64: the wide form for at least 64 query heads, the narrow one
-    below; mma.sync for other block sizes)."""
+def kernel_kind(spec, cta_heads: int = 1) -> str:
+    """Which decode kernel a workload runs: the GQA kernel with one CTA per kv head or per
+    group of cta_heads kv heads (the library's plan, paged_decode_cta_heads), or a form of
+    the latent decode (tcgen05 for blocks of 64: the wide form for at least 64 query heads,
+    the narrow one below; mma.sync for other block sizes)."""
     if not spec.mla:
-        return "gqa"
+        return "gqa" if cta_heads == 1 else "gqa_heads"
     if spec.block_size != 64:
         return "mla"
     return "mla_tc" if spec.q_heads >= 64 else "mla_tcn"
 
 
-KERNEL_NAMES = {"gqa": "paged_decode_main", "mla": "paged_mla_decode_main (mma.sync)",
+KERNEL_NAMES = {"gqa": "paged_decode_main", "gqa_heads": "paged_decode_heads (a CTA per group of kv heads)",
+                "mla": "paged_mla_decode_main (mma.sync)",
                 "mla_tc": "paged_mla_decode_tc (tcgen05)",
                 "mla_tcn": "paged_mla_decode_tcn (tcgen05, 16-head tiles)"}
 
@@ -106,13 +109,13 @@ def kernel_source_sha(kind: str = "gqa") -> str:
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(config: str):
+def profiled_traffic(config: str, kind: str):
     """DRAM bytes per decode launch recorded by an ncu capture of the current kernels.
 
     A profile summary under profiles/ states `kernel_source_sha:` and
     `dram_bytes_per_launch:` for a workload; it counts only while the sources
     are unchanged."""
-    sha = kernel_source_sha(kernel_kind(workloads.CONFIGS[config]))
+    sha = kernel_source_sha(kind)
     for path in glob.glob(os.path.join(PROFILES, "*.md")) + glob.glob(os.path.join(PROFILES, "*.txt")):
         text = open(path).read()
         m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
@@ -538,7 +541,10 @@ class Staged:
         self.step_bytes = self.dec_bytes["total"] + self.app_bytes
         # append + decode; the tensor-core MLA forms add their merge kernel when sequences
         # can be cut into pieces (the other kernels merge inside the decode kernel)
-        self.two_kernels = kernel_kind(s) in ("mla_tc", "mla_tcn") and self.max_splits > 1
+        self.cta_heads = 1 if s.mla else kp.paged_decode_cta_heads(
+            self.pool, s.batch, s.q_heads, s.q_len, w.max_blocks, self.split_req)
+        self.kind = kernel_kind(s, self.cta_heads)
+        self.two_kernels = self.kind in ("mla_tc", "mla_tcn") and self.max_splits > 1
         self.launches_per_step = 3 if self.two_kernels else 2
 
     def attend(self, out=None):
@@ -710,8 +716,8 @@ def roofline_obj(st, dec_ms, peak, peak_kind, config_name):
     bandwidth, with the DRAM traffic of an ncu capture of the same sources."""
     s = st.s
     achieved = st.dec_bytes["total"] / (dec_ms / 1e3) / 1e9
-    traffic, traffic_src = profiled_traffic(config_name)
-    kind = kernel_kind(s)
+    kind = st.kind
+    traffic, traffic_src = profiled_traffic(config_name, kind)
     return {"kernel": KERNEL_NAMES[kind]
                       + ((" + paged_mla_merge_tc" + ("n" if kind == "mla_tcn" else "")
                           + " (the decode call's two launches; ") if st.two_kernels else

@@ -163,12 +163,25 @@ kv_status paged_kv_append(kv_pool* pool, const void* k_new, const void* v_new, i
  * sizes: *split_tokens (a multiple of block_size) and *max_splits (the most
  * chunks any sequence can have, ceil(max_blocks * block_size / split_tokens)).
  * kv_split_tokens: 0 = automatic (from batch, heads, max_blocks and the SM
- * count; between 64 and 192 blocks), else a positive multiple of block_size.
+ * count; between 64 and 192 blocks, 128 at most where one CTA covers two kv
+ * heads), else a positive multiple of block_size.
  * KV_ERR_UNSUPPORTED when max_splits would exceed 65535.  Either output may
  * be NULL.
  */
 kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max_blocks,
                             int kv_split_tokens, int* split_tokens, int* max_splits);
+
+/*
+ * The CTA layout paged_decode_attention (q_len = 1), paged_attention_multi_query and
+ * paged_decode_step use for these sizes: *cta_heads = the kv heads one CTA covers --
+ * 1 (one CTA per kv head and query-row tile) or 2 / 4 (one CTA per group of kv heads,
+ * chosen with the automatic chunk for the pool layouts it is built for: bf16, head_dim
+ * 128, blocks of 16 -> 2; fp8, head_dim 128, blocks of 32 -> 4; rows of a kv head <= 8).
+ * Diagnostic only: both layouts compute the same attention.  Same errors as
+ * paged_decode_plan.
+ */
+kv_status paged_decode_cta_heads(const kv_pool* pool, int batch, int q_heads, int q_len,
+                                 int max_blocks, int kv_split_tokens, int* cta_heads);
 
 /*
  * Bytes of device workspace paged_decode_attention needs for these sizes

@@ -16,6 +16,7 @@ import torch
 
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
+    "paged_decode_cta_heads",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_decode_attention_split_merge",
     "paged_merge_attention_states",
     "paged_attention_multi_query",
@@ -89,6 +90,7 @@ def load_library():
             "kv_pool_device_errors": ([P, ctypes.POINTER(ctypes.c_uint32), I], I),
             "paged_kv_append": ([P, P, P, I, P, P, P, I, P, I, P], I),
             "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
+            "paged_decode_cta_heads": ([P, I, I, I, I, I, ctypes.POINTER(I)], I),
             "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
             "paged_merge_attention_states": ([P, P, I, L, I, P, P, P], I),
@@ -265,6 +267,17 @@ def paged_decode_plan(pool: Pool, batch: int, q_heads: int, max_blocks: int,
                                  int(kv_split_tokens), ctypes.byref(a), ctypes.byref(b)),
            "paged_decode_plan")
     return a.value, b.value
+
+
+def paged_decode_cta_heads(pool: Pool, batch: int, q_heads: int, q_len: int, max_blocks: int,
+                           kv_split_tokens: int = 0) -> int:
+    """kv heads one CTA of the decode covers for these sizes (1, 2 or 4)."""
+    lib = load_library()
+    n = ctypes.c_int()
+    _check(lib.paged_decode_cta_heads(pool.handle, int(batch), int(q_heads), int(q_len),
+                                      int(max_blocks), int(kv_split_tokens), ctypes.byref(n)),
+           "paged_decode_cta_heads")
+    return n.value
 
 
 def paged_decode_workspace_size(pool: Pool, batch: int, q_heads: int, max_blocks: int,

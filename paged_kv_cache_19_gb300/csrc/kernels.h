@@ -134,6 +134,14 @@ cudaError_t launch_decode_bf16(int head_dim, int block_size, int head_tile, dim3
 cudaError_t launch_decode_fp8(int head_dim, int block_size, int head_tile, dim3 grid,
                               const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, cudaStream_t s);
+// The decode kernel with one CTA per group of `heads` kv heads (decode_heads.cuh), `ctas`
+// CTAs per SM; the variants built are listed in decode_heads.cu.
+bool decode_heads_supported(bool fp8, int head_dim, int block_size, int head_tile, int heads,
+                            int ctas);
+cudaError_t prepare_decode_heads(bool fp8, int head_dim, int block_size);
+cudaError_t launch_decode_heads(bool fp8, int head_dim, int block_size, int head_tile, int heads,
+                                int ctas, dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const DecodeParams& p, cudaStream_t s);
 // The separate log-sum-exp merge of the chunk partials that paged_decode_main leaves
 // with merge_kernel = 1: one thread per 4 numbers of a query row, sequences of one
 // chunk skipped (their chunk wrote the output).

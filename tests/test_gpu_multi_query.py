@@ -26,6 +26,8 @@ CASES = {
                            ctx=[16, 77], q_len=16, seed=205),
     "fp8_g1_t3": C(batch=3, q_heads=4, kv_heads=4, head_dim=128, block_size=32, ctx=[3, 64, 200],
                    q_len=3, seed=206, cache_dtype="fp8_e4m3"),
+    "hkv8_g4_t4_verify": C(batch=3, q_heads=32, kv_heads=8, head_dim=128, block_size=16,
+                           ctx=[4, 300, 1100], q_len=4, seed=207, split_tokens=256),
 }
 
 

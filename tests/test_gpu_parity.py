@@ -48,6 +48,18 @@ SMALL = {
                  ctx=[64, 300], seed=111, cache_dtype="fp8_e4m3"),
     "long_ragged_auto_split": C(batch=3, q_heads=16, kv_heads=2, head_dim=128, block_size=16,
                                 ctx=[5000, 17, 2500], seed=112),
+    # eight kv heads: the layouts whose CTA covers a group of kv heads
+    "hkv8_g4_split256": C(batch=3, q_heads=32, kv_heads=8, head_dim=128, block_size=16,
+                          ctx=[1, 300, 1900], seed=113, split_tokens=256),
+    "hkv8_g2_auto": C(batch=5, q_heads=16, kv_heads=8, head_dim=128, block_size=16,
+                      ctx=[17, 64, 700, 2500, 33], seed=114),
+    "hkv8_g16_nt16": C(batch=2, q_heads=128, kv_heads=8, head_dim=128, block_size=16,
+                       ctx=[100, 1000], seed=116, split_tokens=512),
+    "hkv8_prefix_shared": C(batch=8, q_heads=32, kv_heads=8, head_dim=128, block_size=16,
+                            ctx=[20, 70, 64, 129, 65, 200, 16, 90], seed=117, prefix_group=4,
+                            prefix_tokens=64, split_tokens=32),
+    "fp8_hkv8_split256": C(batch=3, q_heads=8, kv_heads=8, head_dim=128, block_size=32,
+                           ctx=[5, 700, 1500], seed=115, cache_dtype="fp8_e4m3", split_tokens=256),
 }
 
 
