@@ -330,6 +330,24 @@ kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new,
                             void* out, float* lse_out, void* stream);
 
 /*
+ * Test hook of the failure path of the decode kernels; the pages have no
+ * counterpart (their engines raise on the host; this library's kernels bound
+ * every pipeline wait instead, see KV_DEVERR_TIMEOUT).  Process-wide, read by
+ * every later paged_decode_attention / paged_attention_multi_query /
+ * paged_decode_step / split-merge / no-alloc launch:
+ *   stop_stage: the producer of each CTA issues no load for the stages of its
+ *     chunk from this index on (-1, the default: off), so the consumers' wait
+ *     for that stage can only run out: they set KV_DEVERR_TIMEOUT, leave their
+ *     loop and write what they have (the outputs are then meaningless), while
+ *     every load that was issued lands before the CTA exits;
+ *   consumer_wait_ns: the consumers' limit for a stage wait (0: the default,
+ *     two seconds); the producer's waits keep the default.
+ * KV_ERR_INVALID_ARG for stop_stage < -1.  Not for production use: call
+ * kv_debug_decode_stall(-1, 0) to restore normal operation.
+ */
+kv_status kv_debug_decode_stall(int stop_stage, unsigned long long consumer_wait_ns);
+
+/*
  * Allocation-free decode attention.  The paper has no counterpart to this call;
  * it exists for users of this library who cannot allocate device memory at the
  * call site: plug-in hosts that give a kernel only its input and output

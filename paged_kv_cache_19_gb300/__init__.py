@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "KVError", "Pool", "kv_pool_create", "kv_pool_destroy", "paged_kv_append", "paged_decode_plan",
-    "paged_decode_cta_heads",
+    "paged_decode_cta_heads", "kv_debug_decode_stall",
     "paged_decode_workspace_size", "paged_decode_attention", "paged_decode_attention_split_merge",
     "paged_merge_attention_states",
     "paged_attention_multi_query",
@@ -91,6 +91,7 @@ def load_library():
             "paged_kv_append": ([P, P, P, I, P, P, P, I, P, I, P], I),
             "paged_decode_plan": ([P, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)], I),
             "paged_decode_cta_heads": ([P, I, I, I, I, I, ctypes.POINTER(I)], I),
+            "kv_debug_decode_stall": ([I, ctypes.c_ulonglong], I),
             "paged_decode_workspace_size": ([P, I, I, I, I, ctypes.POINTER(S)], I),
             "paged_decode_attention": ([P, P, I, P, I, P, I, ctypes.c_float, I, P, S, P, P, P], I),
             "paged_merge_attention_states": ([P, P, I, L, I, P, P, P], I),
@@ -267,6 +268,13 @@ def paged_decode_plan(pool: Pool, batch: int, q_heads: int, max_blocks: int,
                                  int(kv_split_tokens), ctypes.byref(a), ctypes.byref(b)),
            "paged_decode_plan")
     return a.value, b.value
+
+
+def kv_debug_decode_stall(stop_stage: int = -1, consumer_wait_ns: int = 0) -> None:
+    """Failure-path test hook (see include/kv_paged.h); (-1, 0) restores normal operation."""
+    lib = load_library()
+    _check(lib.kv_debug_decode_stall(int(stop_stage), int(consumer_wait_ns)),
+           "kv_debug_decode_stall")
 
 
 def paged_decode_cta_heads(pool: Pool, batch: int, q_heads: int, q_len: int, max_blocks: int,

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -63,6 +64,10 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Failure-path test hook of the decode kernels (kv_debug_decode_stall).
+std::atomic<int> g_stop_stage{-1};
+std::atomic<unsigned long long> g_consumer_wait_ns{0};
 
 // Restores the caller's current device on scope exit.
 struct DeviceGuard {
@@ -454,6 +459,14 @@ kv_status paged_decode_plan(const kv_pool* pool, int batch, int q_heads, int max
     return KV_OK;
 }
 
+kv_status kv_debug_decode_stall(int stop_stage, unsigned long long consumer_wait_ns)
+{
+    if (stop_stage < -1) return KV_ERR_INVALID_ARG;
+    g_stop_stage.store(stop_stage, std::memory_order_relaxed);
+    g_consumer_wait_ns.store(consumer_wait_ns, std::memory_order_relaxed);
+    return KV_OK;
+}
+
 kv_status paged_decode_cta_heads(const kv_pool* pool, int batch, int q_heads, int q_len,
                                  int max_blocks, int kv_split_tokens, int* cta_heads)
 {
@@ -542,6 +555,8 @@ kv_status make_decode_launch(const kv_pool* pool, const void* q, int q_heads, in
     p.scale_log2 = scale * 1.4426950408889634f;
     p.dep_tail = 0;
     p.merge_kernel = 0;
+    p.stop_stage = g_stop_stage.load(std::memory_order_relaxed);
+    p.consumer_wait_ns = g_consumer_wait_ns.load(std::memory_order_relaxed);
     // chunk-major grid: x = (kv head group, row tile), y = sequence, z = chunk
     *grid = dim3(static_cast<unsigned>(pool->kv_heads / plan.cta_heads * plan.head_groups),
                  static_cast<unsigned>(batch), static_cast<unsigned>(plan.max_splits));

@@ -183,6 +183,10 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
             for (int k = 0; k < cnt; ++k) {
                 const int blk = __shfl_sync(FULL_MASK, id, k);
                 const int it = base + k;
+                if (it == p.stop_stage) {                // test hook: the rest never lands
+                    ok = false;
+                    break;
+                }
                 const int st = it % H::NST;
                 const uint32_t ph = static_cast<uint32_t>(it / H::NST) & 1u;
                 int good = 1;
@@ -230,10 +234,11 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     // ------------------------------------------------------------ consumer warps
     WarpState<C> st;
     reset_state(st);
+    const unsigned long long wait_ns = p.consumer_wait_ns ? p.consumer_wait_ns : WAIT_LIMIT_NS;
     for (int it = 0; it < nb; ++it) {
         const int s = it % H::NST;
         const uint32_t ph = static_cast<uint32_t>(it / H::NST) & 1u;
-        const bool arrived = mbar_wait_bounded(smem_u32(full + s), ph);
+        const bool arrived = mbar_wait_bounded(smem_u32(full + s), ph, wait_ns);
         if (!__all_sync(FULL_MASK, arrived)) {
             if (lane == 0) atomicOr(p.err, KV_DEVERR_TIMEOUT);
             break;

@@ -126,6 +126,10 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int k = 0; k < cnt; ++k) {
                 const int blk = __shfl_sync(FULL_MASK, id, k);
                 const int it = base + k;
+                if (it == p.stop_stage) {                // test hook: the rest never lands
+                    ok = false;
+                    break;
+                }
                 const int st = it % C::NSTAGE;
                 const uint32_t ph = static_cast<uint32_t>(it / C::NSTAGE) & 1u;
                 int good = 1;
@@ -176,11 +180,11 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // ------------------------------------------------------------ consumer warps
     WarpState<C> st;
     reset_state(st);
-
+    const unsigned long long wait_ns = p.consumer_wait_ns ? p.consumer_wait_ns : WAIT_LIMIT_NS;
     for (int it = warp; it < nb; it += C::NCW) {
         const int s = it % C::NSTAGE;
         const uint32_t ph = static_cast<uint32_t>(it / C::NSTAGE) & 1u;
-        const bool arrived = mbar_wait_bounded(smem_u32(full + s), ph);
+        const bool arrived = mbar_wait_bounded(smem_u32(full + s), ph, wait_ns);
         if (!__all_sync(FULL_MASK, arrived)) {
             if (lane == 0) atomicOr(p.err, KV_DEVERR_TIMEOUT);
             break;

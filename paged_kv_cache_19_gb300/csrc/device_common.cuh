@@ -68,14 +68,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false (without having observed completion) once WAIT_LIMIT_NS has passed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+// false (without having observed completion) once limit_ns has passed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_timer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

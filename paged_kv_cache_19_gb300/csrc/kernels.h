@@ -43,6 +43,11 @@ struct DecodeParams {
     // 0: the last chunk CTA of a cut sequence merges the chunks (tickets).  1: chunk CTAs
     // only leave their partials, and paged_decode_merge (launch_decode_merge) merges them.
     int merge_kernel;
+    // Failure-path test hook (kv_debug_decode_stall): the producer issues no load for a
+    // chunk's stages from stop_stage on (-1: all), and the consumers give up a stage wait
+    // after consumer_wait_ns instead of WAIT_LIMIT_NS (0: the default).
+    int stop_stage;
+    unsigned long long consumer_wait_ns;
 };
 
 struct AppendParams {

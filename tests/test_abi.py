@@ -119,3 +119,8 @@ def test_product_package_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_decode_stall_hook_validates_on_the_host(lib):
+    assert lib.kv_debug_decode_stall(-2, ctypes.c_ulonglong(0)) == kp.KV_ERR_INVALID_ARG
+    assert lib.kv_debug_decode_stall(-1, ctypes.c_ulonglong(0)) == kp.KV_OK
