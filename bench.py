@@ -501,8 +501,9 @@ def stage(w, device):
 
 NOMINAL_HBM_GBS = 8000.0          # GB300 HBM3e, nominal (about 8 TB/s)
 # The workloads measured in the same run after the headline one (one GPU only): the other
-# bench configurations, the multi-token verify pass and both latent-attention layers.
-EXTRA_CONFIGS = ["long_context", "ragged_prefix", "mha_fp8", "llama3_8b_verify4",
+# bench configurations (the tiny one is launch-bound: reported, not a roofline claim), the
+# multi-token verify pass and both latent-attention layers.
+EXTRA_CONFIGS = ["tiny", "long_context", "ragged_prefix", "mha_fp8", "llama3_8b_verify4",
                  "deepseek_mla", "deepseek_mla_tp8"]
 
 
