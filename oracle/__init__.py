@@ -323,13 +323,33 @@ def decode_multi(q, k, v, seq_start, context_lens, *, q_heads: int, q_len: int, 
     return out, lse
 
 
-def decode_multi_workload(w, q_multi, q_len: int, seqs=None, cache_dtype: str | None = None):
-    """Oracle attention of q_len new tokens per sequence of a workload (q_multi [B, Hq, q_len, d])."""
+def decode_multi_workload(w, q_multi, q_len: int, seqs=None, cache_dtype: str | None = None,
+                          threads: int = 1):
+    """Oracle attention of q_len new tokens per sequence of a workload (q_multi [B, Hq, q_len, d]).
+
+    threads > 1 runs disjoint sets of sequences in concurrent calls of the C routine
+    (ctypes releases the interpreter lock); each sequence's arithmetic is unchanged."""
     s = w.spec
-    return decode_multi(q_multi, w.k, w.v, w.seq_start, w.context_lens, q_heads=s.q_heads,
-                        q_len=q_len, kv_heads=s.kv_heads, head_dim=s.head_dim, scale=w.scale,
-                        cache_dtype=cache_dtype or s.cache_dtype, k_scale=w.k_scale,
-                        v_scale=w.v_scale, seqs=seqs)
+    seq_list = list(range(w.batch)) if seqs is None else [int(b) for b in seqs]
+
+    def run(part):
+        return decode_multi(q_multi, w.k, w.v, w.seq_start, w.context_lens, q_heads=s.q_heads,
+                            q_len=q_len, kv_heads=s.kv_heads, head_dim=s.head_dim, scale=w.scale,
+                            cache_dtype=cache_dtype or s.cache_dtype, k_scale=w.k_scale,
+                            v_scale=w.v_scale, seqs=part)
+
+    if threads <= 1 or len(seq_list) <= 1:
+        return run(seq_list)
+    from concurrent.futures import ThreadPoolExecutor
+    parts = [seq_list[i::threads] for i in range(min(threads, len(seq_list)))]
+    with ThreadPoolExecutor(len(parts)) as ex:
+        res = list(ex.map(run, parts))
+    out = np.zeros((len(seq_list), s.q_heads, q_len, s.head_dim), dtype=np.float64)
+    lse = np.zeros((len(seq_list), s.q_heads, q_len), dtype=np.float64)
+    for i, (o, l) in enumerate(res):
+        out[i::len(parts)] = o
+        lse[i::len(parts)] = l
+    return out, lse
 
 
 def mla_attend(q, cache, latent_dim: int, scale: float):
