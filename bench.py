@@ -71,8 +71,9 @@ def parse_args():
 # --------------------------------------------------------------------------- helpers
 KERNEL_SOURCES = {
     "gqa": ["decode_kernel.cuh", "decode_common.cuh", "decode_bf16.cu", "decode_fp8.cu",
-            "device_common.cuh"],
-    "gqa_heads": ["decode_heads.cuh", "decode_heads.cu", "decode_common.cuh", "device_common.cuh"],
+            "device_common.cuh", "append_row.cuh"],
+    "gqa_heads": ["decode_heads.cuh", "decode_heads.cu", "decode_common.cuh", "device_common.cuh",
+                  "append_row.cuh"],
     "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
     "mla_tc": ["decode_mla_tc.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
                "device_common.cuh"],
@@ -546,7 +547,15 @@ class Staged:
             self.pool, s.batch, s.q_heads, s.q_len, w.max_blocks, self.split_req)
         self.kind = kernel_kind(s, self.cta_heads)
         self.two_kernels = self.kind in ("mla_tc", "mla_tcn") and self.max_splits > 1
-        self.launches_per_step = 3 if self.two_kernels else 2
+        # paged_decode_step on a K/V pool whose kv heads have at most 8 query rows is one
+        # kernel (its CTAs write the new rows before loading their blocks), else the append
+        # kernel then the attention; on a latent pool the append kernel, then the attention
+        # (and the merge kernel of the tensor-core forms when sequences can be cut)
+        rows = s.q_heads // s.kv_heads * s.q_len
+        if s.mla:
+            self.launches_per_step = 3 if self.two_kernels else 2
+        else:
+            self.launches_per_step = 1 if rows <= 8 else 2
 
     def attend(self, out=None):
         kp, s, w = self.kp, self.s, self.w

@@ -318,10 +318,14 @@ kv_status paged_multi_query_workspace_size(const kv_pool* pool, int batch, int q
  *   error bits -- as in paged_attention_multi_query; all arguments are checked
  *   before anything is launched, so an error leaves the pool untouched.
  *   The result equals paged_kv_append (with those positions) followed by
- *   paged_attention_multi_query.  Because the attention kernel knows that the
- *   preceding append writes only those last q_len positions, it reads every
- *   other block of the cache while the append runs and waits for the append
- *   only before loading a block that holds a new token.
+ *   paged_attention_multi_query: the same pool bytes, the same output bits.
+ *   Where a kv head's query rows (q_heads / kv_heads * q_len) fit one 8-row
+ *   tile it is one kernel launch: the CTA that reads a block holding one of
+ *   the new tokens writes that token's rows of its kv heads into the pool
+ *   first (bf16 copied, fp8 quantised exactly as paged_kv_append does), then
+ *   loads the block; new tokens whose position lies outside the block table
+ *   are not written and set KV_DEVERR_POSITION, as the append would.  With
+ *   more rows it is paged_kv_append's kernel followed by the attention's.
  */
 kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new, const void* q,
                             int q_heads, int q_len, const int32_t* block_tables, int max_blocks,

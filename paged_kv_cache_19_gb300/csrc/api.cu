@@ -553,7 +553,10 @@ kv_status make_decode_launch(const kv_pool* pool, const void* q, int q_heads, in
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.dep_tail = 0;
+    p.k_new = nullptr;
+    p.v_new = nullptr;
+    p.k_pool = nullptr;
+    p.v_pool = nullptr;
     p.merge_kernel = 0;
     p.stop_stage = g_stop_stage.load(std::memory_order_relaxed);
     p.consumer_wait_ns = g_consumer_wait_ns.load(std::memory_order_relaxed);
@@ -623,6 +626,18 @@ kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new,
         return KV_ERR_INVALID_ARG;
     if (static_cast<long long>(batch) * q_len > std::numeric_limits<int>::max())
         return KV_ERR_UNSUPPORTED;
+    if (plan.head_tile == 8) {
+        // One kernel: the CTA that reads a block holding one of the step's new tokens writes
+        // that token's rows of its kv heads into the pool first (the append's arithmetic, the
+        // same bytes), so no append kernel has to finish before the attention starts.
+        p.k_new = static_cast<const uint16_t*>(k_new);
+        p.v_new = static_cast<const uint16_t*>(v_new);
+        p.k_pool = pool->k;
+        p.v_pool = pool->v;
+        return launch_decode(pool, plan, grid, p, stream);
+    }
+    // 16-row tiles: the append kernel, then the attention (the kernel's step form is not
+    // built for them)
     kvp::AppendParams a;
     a.k_new = static_cast<const uint16_t*>(k_new);
     a.v_new = static_cast<const uint16_t*>(v_new);
@@ -645,8 +660,6 @@ kv_status paged_decode_step(kv_pool* pool, const void* k_new, const void* v_new,
     a.fp8 = pool->dtype == KV_DTYPE_FP8_E4M3;
     a.q_len = q_len;
     if (kvp::launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
-    // the append wrote only the last q_len positions of each sequence
-    p.dep_tail = q_len;
     return launch_decode(pool, plan, grid, p, stream);
 }
 

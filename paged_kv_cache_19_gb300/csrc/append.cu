@@ -1,4 +1,5 @@
 // append.cu -- the paged KV append.
+#include "append_row.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 #include "kv_block_manager.h"
@@ -12,7 +13,7 @@ namespace kvp {
 // write_kv; brunomaga.github.io, PagedKVCache.append).  One CTA per token;
 // each thread moves 8 elements (16 bytes of bf16 input) per step.
 // fp8: code = e4m3fn(x / scale[head]) with the quotient rounded to binary32
-// and the conversion rounding to nearest even, saturating at +-448.
+// and the conversion rounding to nearest even, saturating at +-448 (e4m3_codes8).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams p)
 {
@@ -58,26 +59,8 @@ __global__ void __launch_bounds__(128) paged_kv_append_kernel(const AppendParams
     uint2* vd = reinterpret_cast<uint2*>(p.v_pool + dst);
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
         const int h = (v * 8) / p.head_dim;
-        const float sk = __ldg(p.k_scale + h);
-        const float sv = __ldg(p.v_scale + h);
-        const uint4 kx = __ldg(ks + v);
-        const uint4 vx = __ldg(vs + v);
-        const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
-        const uint32_t vw[4] = {vx.x, vx.y, vx.z, vx.w};
-        uint32_t kc[2] = {0u, 0u}, vc[2] = {0u, 0u};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float k0 = __fdiv_rn(__uint_as_float(kw[e] << 16), sk);
-            const float k1 = __fdiv_rn(__uint_as_float(kw[e] & 0xffff0000u), sk);
-            const float v0 = __fdiv_rn(__uint_as_float(vw[e] << 16), sv);
-            const float v1 = __fdiv_rn(__uint_as_float(vw[e] & 0xffff0000u), sv);
-            const uint32_t k2 = __nv_cvt_float2_to_fp8x2(make_float2(k0, k1), __NV_SATFINITE, __NV_E4M3);
-            const uint32_t v2 = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
-            kc[e >> 1] |= (k2 & 0xffffu) << (16 * (e & 1));
-            vc[e >> 1] |= (v2 & 0xffffu) << (16 * (e & 1));
-        }
-        kd[v] = make_uint2(kc[0], kc[1]);
-        vd[v] = make_uint2(vc[0], vc[1]);
+        kd[v] = e4m3_codes8(__ldg(ks + v), __ldg(p.k_scale + h));
+        vd[v] = e4m3_codes8(__ldg(vs + v), __ldg(p.v_scale + h));
     }
 }
 

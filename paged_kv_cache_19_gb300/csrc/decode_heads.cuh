@@ -26,6 +26,7 @@
 //     KV_DEVERR_TIMEOUT and the CTA drains its copies and returns.
 #pragma once
 
+#include "append_row.cuh"
 #include "decode_common.cuh"
 
 namespace kvp {
@@ -93,7 +94,8 @@ __device__ __forceinline__ void write_warp_rows(const WarpState<C>& st, const De
         }
 }
 
-template <bool FP8, int D, int BS, int NT, int HC, int CTAS>
+// STEP: paged_decode_step's form (writes the step's new rows before loading their blocks).
+template <bool FP8, int D, int BS, int NT, int HC, int CTAS, bool STEP>
 __global__ void __launch_bounds__(HeadsCfg<FP8, D, BS, NT, HC, CTAS>::THREADS, CTAS)
 paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const DecodeParams p)
@@ -124,7 +126,7 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
         fence_mbar_init();
     }
-    if (p.dep_tail == 0) grid_dependency_wait();
+    grid_dependency_wait();                                  // inputs of the preceding kernel
 
     const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
     int id_first = -1;
@@ -142,6 +144,7 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     }
     int ctx = __ldg(p.ctx + b);
     const int cap = p.max_blocks * BS;
+
     if (ctx < 0 || ctx > cap || (ctx > 0 && ctx < p.q_len)) {
         if (threadIdx.x == 0 && split == 0 && blockIdx.x == 0) atomicOr(p.err, KV_DEVERR_CONTEXT);
         ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
@@ -163,8 +166,19 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
         }
         int issued = 0;
         bool ok = true;
-        bool waited = p.dep_tail == 0;
-        const int tail_blk = (ctx - p.dep_tail) / BS;
+        // paged_decode_step: the length as given (re-read here rather than kept live across
+        // the roles: the consumers' registers are the kernel's peak)
+        const int ctx_raw = STEP ? __ldg(p.ctx + b) : 0;
+        if (STEP && lane == 0 && split == 0 && blockIdx.x == 0) {
+            // paged_decode_step: a new token whose position is not in the table is not written
+            for (int t = 0; t < p.q_len; ++t) {
+                const int pos = ctx_raw - p.q_len + t;
+                if (pos < 0 || pos / BS >= p.max_blocks) atomicOr(p.err, KV_DEVERR_POSITION);
+            }
+        }
+        // paged_decode_step: the first block that holds one of the step's new tokens
+        const int new_blk = STEP ? max(0, ctx_raw - p.q_len) / BS : p.max_blocks;
+        bool wrote = blk0 + nb <= new_blk;                    // nothing of the step in this chunk
         // lane i < 2 HC loads the K (i < HC) or V tile of kv head kg * HC + i % HC
         const int my_h = lane % HC;
         const CUtensorMap* my_map = lane < HC ? &tmk : &tmv;
@@ -187,14 +201,19 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                     ok = false;
                     break;
                 }
+                if (STEP && !wrote && (blk0 + it >= new_blk || it == H::NST)) {
+                    // the step's new rows go into their blocks once the ring is full (the
+                    // producer would wait for a slot anyway), or before the first block that
+                    // holds one is loaded, whichever comes first
+                    write_step_rows<FP8, D, BS, HC>(p, b, ctx_raw, max(blk0, new_blk), blk0 + nb, kg * HC, lane);
+                    fence_proxy_async_all();
+                    __syncwarp();
+                    wrote = true;
+                }
                 const int st = it % H::NST;
                 const uint32_t ph = static_cast<uint32_t>(it / H::NST) & 1u;
                 int good = 1;
                 if (lane == 0) {
-                    if (!waited && blk0 + it >= tail_blk) {
-                        grid_dependency_wait();
-                        waited = true;
-                    }
                     if (!mbar_wait_bounded(smem_u32(empty + st), ph ^ 1u)) {
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         good = 0;
@@ -316,7 +335,11 @@ paged_decode_heads(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 template <bool FP8, int D, int BS, int NT, int HC, int CTAS>
 cudaError_t prepare_heads_variant()
 {
-    return cudaFuncSetAttribute(paged_decode_heads<FP8, D, BS, NT, HC, CTAS>,
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_heads<FP8, D, BS, NT, HC, CTAS, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         HeadsCfg<FP8, D, BS, NT, HC, CTAS>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_decode_heads<FP8, D, BS, NT, HC, CTAS, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 HeadsCfg<FP8, D, BS, NT, HC, CTAS>::SMEM);
 }
@@ -325,7 +348,11 @@ template <bool FP8, int D, int BS, int NT, int HC, int CTAS>
 cudaError_t launch_heads_variant(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const DecodeParams& p, cudaStream_t s)
 {
-    return launch_dependent(paged_decode_heads<FP8, D, BS, NT, HC, CTAS>, grid,
+    if (p.k_new != nullptr)
+        return launch_dependent(paged_decode_heads<FP8, D, BS, NT, HC, CTAS, true>, grid,
+                                dim3(HeadsCfg<FP8, D, BS, NT, HC, CTAS>::THREADS),
+                                HeadsCfg<FP8, D, BS, NT, HC, CTAS>::SMEM, s, tk, tv, p);
+    return launch_dependent(paged_decode_heads<FP8, D, BS, NT, HC, CTAS, false>, grid,
                             dim3(HeadsCfg<FP8, D, BS, NT, HC, CTAS>::THREADS),
                             HeadsCfg<FP8, D, BS, NT, HC, CTAS>::SMEM, s, tk, tv, p);
 }

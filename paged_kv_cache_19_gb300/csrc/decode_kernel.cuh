@@ -23,6 +23,7 @@
 //     KV_DEVERR_TIMEOUT and the CTA drains its copies and returns.
 #pragma once
 
+#include "append_row.cuh"
 #include "decode_common.cuh"
 
 namespace kvp {
@@ -35,7 +36,10 @@ struct GridCfg : DecodeCfg<FP8, D, BS, NT> {
     static_assert(C::RED_BYTES <= C::NSTAGE * C::STAGE, "epilogue buffer reuses the stages");
 };
 
-template <bool FP8, int D, int BS, int NT>
+// STEP: paged_decode_step's form, which writes the step's new rows of each block into the
+// pool before loading it (a separate instantiation, so that the attention-only kernel keeps
+// its registers).
+template <bool FP8, int D, int BS, int NT, bool STEP>
 __global__ void __launch_bounds__(DecodeCfg<FP8, D, BS, NT>::THREADS, GridCfg<FP8, D, BS, NT>::MINB)
 paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p)
@@ -67,10 +71,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         fence_mbar_init();
     }
-    // Inputs of the preceding kernel are ready -- unless it only appended the last
-    // dep_tail positions of each sequence: then only the producer waits, before the first
-    // load of a block that holds one of them.
-    if (p.dep_tail == 0) grid_dependency_wait();
+    grid_dependency_wait();                          // inputs of the preceding kernel are ready
 
     // Independent loads in flight together: the context length, the chunk's
     // first 32 table entries (producer) and the query fragments (consumers).
@@ -87,6 +88,7 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     int ctx = __ldg(p.ctx + b);
     const int cap = p.max_blocks * BS;
+
     if (ctx < 0 || ctx > cap || (ctx > 0 && ctx < p.q_len)) {
         // out of range (clamped), or fewer cached tokens than new queries (kept:
         // the queries at negative positions attend to nothing)
@@ -110,8 +112,19 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         int issued = 0;
         bool ok = true;
-        bool waited = p.dep_tail == 0;
-        const int tail_blk = (ctx - p.dep_tail) / BS;    // first block written by the append
+        // paged_decode_step: the length as given (re-read here rather than kept live across
+        // the roles: the consumers' registers are the kernel's peak)
+        const int ctx_raw = STEP ? __ldg(p.ctx + b) : 0;
+        if (STEP && lane == 0 && split == 0 && blockIdx.x == 0) {
+            // paged_decode_step: a new token whose position is not in the table is not written
+            for (int t = 0; t < p.q_len; ++t) {
+                const int pos = ctx_raw - p.q_len + t;
+                if (pos < 0 || pos / BS >= p.max_blocks) atomicOr(p.err, KV_DEVERR_POSITION);
+            }
+        }
+        // paged_decode_step: the first block that holds one of the step's new tokens
+        const int new_blk = STEP ? max(0, ctx_raw - p.q_len) / BS : p.max_blocks;
+        bool wrote = blk0 + nb <= new_blk;                    // nothing of the step in this chunk
         for (int base = 0; base < nb && ok; base += 32) {
             const int j = base + lane;
             int id = -1;
@@ -130,14 +143,19 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     ok = false;
                     break;
                 }
+                if (STEP && !wrote && (blk0 + it >= new_blk || it == C::NSTAGE)) {
+                    // the step's new rows go into their blocks once the ring is full (the
+                    // producer would wait for a slot anyway), or before the first block that
+                    // holds one is loaded, whichever comes first
+                    write_step_rows<FP8, D, BS, 1>(p, b, ctx_raw, max(blk0, new_blk), blk0 + nb, kvh, lane);
+                    fence_proxy_async_all();
+                    __syncwarp();
+                    wrote = true;
+                }
                 const int st = it % C::NSTAGE;
                 const uint32_t ph = static_cast<uint32_t>(it / C::NSTAGE) & 1u;
                 int good = 1;
                 if (lane == 0) {
-                    if (!waited && blk0 + it >= tail_blk) {
-                        grid_dependency_wait();
-                        waited = true;
-                    }
                     if (!mbar_wait_bounded(smem_u32(empty + st), ph ^ 1u)) {
                         atomicOr(p.err, KV_DEVERR_TIMEOUT);
                         good = 0;
@@ -277,19 +295,39 @@ paged_decode_main(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (t == 0) *ticket = 0;                        // ready for the next call
 }
 
+// The step form is built for 8-row tiles only: with 16-row tiles the consumers' state
+// leaves no registers for it (measured: 134 us for the 4-token verify step against 125 us
+// for its attention), so paged_decode_step runs the append kernel first there.
+template <int NT>
+constexpr bool step_form_built() { return NT == 8; }
+
 template <bool FP8, int D, int BS, int NT>
 cudaError_t prepare_variant()
 {
-    return cudaFuncSetAttribute(paged_decode_main<FP8, D, BS, NT>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GridCfg<FP8, D, BS, NT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_main<FP8, D, BS, NT, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GridCfg<FP8, D, BS, NT>::SMEM);
+    if constexpr (step_form_built<NT>()) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(paged_decode_main<FP8, D, BS, NT, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GridCfg<FP8, D, BS, NT>::SMEM);
+    }
+    return e;
 }
 
 template <bool FP8, int D, int BS, int NT>
 cudaError_t launch_variant(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv,
                            const DecodeParams& p, cudaStream_t s)
 {
-    return launch_dependent(paged_decode_main<FP8, D, BS, NT>, grid,
+    if (p.k_new != nullptr) {
+        if constexpr (step_form_built<NT>())
+            return launch_dependent(paged_decode_main<FP8, D, BS, NT, true>, grid,
+                                    dim3(DecodeCfg<FP8, D, BS, NT>::THREADS),
+                                    GridCfg<FP8, D, BS, NT>::SMEM, s, tk, tv, p);
+        return cudaErrorInvalidValue;
+    }
+    return launch_dependent(paged_decode_main<FP8, D, BS, NT, false>, grid,
                             dim3(DecodeCfg<FP8, D, BS, NT>::THREADS),
                             GridCfg<FP8, D, BS, NT>::SMEM, s, tk, tv, p);
 }

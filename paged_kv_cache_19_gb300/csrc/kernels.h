@@ -35,11 +35,14 @@ struct DecodeParams {
     int max_blocks, num_blocks;
     int split_blocks, max_splits;   // chunk length in blocks; most chunks a sequence can have
     float scale_log2;         // softmax scale * log2(e)
-    // 0: the preceding kernel on the stream may have written anything this one reads, so
-    // wait for it before the first read.  n > 0: it wrote only the last n positions of
-    // each sequence in the pool (the step's append), so blocks holding none of them are
-    // read at once and only the loads of the others wait for it.
-    int dep_tail;
+    // paged_decode_step: the step's new tokens (bf16 [batch * q_len, kv_heads, head_dim],
+    // token t of sequence b at row b * q_len + t, position ctx - q_len + t), which the CTA
+    // reading a block writes into the pool halves before it loads that block; null for the
+    // attention alone.
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint8_t* k_pool;
+    uint8_t* v_pool;
     // 0: the last chunk CTA of a cut sequence merges the chunks (tickets).  1: chunk CTAs
     // only leave their partials, and paged_decode_merge (launch_decode_merge) merges them.
     int merge_kernel;

@@ -1,9 +1,11 @@
 """GPU parity of paged_decode_step: the append of the step's new tokens and their attention
-in one call, the attention streaming the blocks the append does not touch while it runs.
+in one call (for K/V pools one kernel, whose CTAs write the new rows of the blocks they read
+before loading them; for latent pools the append kernel, then the attention streaming the
+blocks the append does not touch while it runs).
 
 The pool after the step must equal the oracle's append image bit for bit, the outputs the
 oracle within the attention tolerances, and both must be bit-identical to the separate
-paged_kv_append + attention calls (the same kernels; only the dependency differs).
+paged_kv_append + attention calls.
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ import torch
 import oracle
 import paged_kv_cache_19_gb300 as kp
 import workloads
-from gpu_util import LSE_ABS, MAX_ABS, REL_L2, Staged, compare
+from gpu_util import LSE_ABS, MAX_ABS, REL_L2, Staged, compare, i32
 
 pytestmark = pytest.mark.gpu
 
@@ -109,6 +111,38 @@ def test_repeated_steps_on_one_stream_stay_exact():
         assert torch.equal(out, outs[0])
     assert st.pool.device_errors() == 0
     st.destroy()
+
+
+def test_step_writes_and_flags_what_the_separate_append_does():
+    """Context lengths that put a new token outside its block table (an empty sequence, one
+    longer than the table): the step writes the same pool bytes as paged_kv_append followed
+    by the attention, sets the same device error bits and gives the same output bits."""
+    w = workloads.make(C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=16,
+                         ctx=[10, 40, 33], seed=310))
+    bad_ctx = np.array([0, 40, w.max_blocks * 16 + 5], dtype=np.int32)
+    results = []
+    for fused in (True, False):
+        st = Staged(w, step_append=False)
+        ctx = i32(bad_ctx)
+        out = torch.empty_like(st.q)
+        lse = torch.empty(st.q.shape[:2], dtype=torch.float32, device="cuda")
+        if fused:
+            kp.paged_decode_step(st.pool, st.k_new, st.v_new, st.q, st.tables, ctx, w.scale,
+                                 out=out, lse=lse)
+        else:
+            kp.paged_kv_append(st.pool, st.k_new, st.v_new, st.tables, ctx)
+            kp.paged_decode_attention(st.pool, st.q, st.tables, ctx, w.scale, out=out, lse=lse)
+        torch.cuda.synchronize()
+        bits = st.pool.device_errors()
+        kr, vr = st.pool.raw_bytes()
+        results.append((bits, kr.clone(), vr.clone(), out.clone(), lse.clone()))
+        st.destroy()
+    (b1, k1, v1, o1, l1), (b2, k2, v2, o2, l2) = results
+    assert b1 == b2, (hex(b1), hex(b2))
+    assert b1 & kp.DEVERR_POSITION and b1 & kp.DEVERR_CONTEXT
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
 
 
 def test_step_rejects_bad_arguments_before_launching():
