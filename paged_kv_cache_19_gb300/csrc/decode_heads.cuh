@@ -18,10 +18,14 @@
 //     decode_common.cuh), so it holds the whole chunk's state for its rows and no
 //     warp states are merged; a stage is free once the HC warps have read it.
 //   * Each warp writes its rows: bf16 output and LSE for a sequence of one chunk,
-//     else an fp32 partial; the CTA then takes a
-//     ticket and the last chunk CTA of the (sequence, head group, row tile) merges
-//     every chunk by log-sum-exp (learn.mohebi.ai lesson 12, section 6: split-KV
-//     decoding), unless the separate merge kernel is asked for.
+//     else an fp32 partial; the CTA then takes a ticket and the last chunk CTA of
+//     the (sequence, head group, row tile) merges every chunk by log-sum-exp
+//     (learn.mohebi.ai lesson 12, section 6: split-KV decoding), unless the
+//     separate merge kernel is asked for.
+//   * The step form (STEP, paged_decode_step) also appends: the producer writes the
+//     step's new K/V rows of the group's kv heads into the chunk's blocks
+//     (append_row.cuh) once the ring is full or before the first block holding
+//     one is loaded, and orders the writes before its TMA loads.
 //   * Every wait is bounded (WAIT_LIMIT_NS); a late barrier sets
 //     KV_DEVERR_TIMEOUT and the CTA drains its copies and returns.
 #pragma once

@@ -19,6 +19,10 @@
 //     so each warp owns NSTAGE / 4 stages and waits on them in order), each
 //     with its own online-softmax state (decode_common.cuh); the four states
 //     are merged in shared memory at the end.
+//   * The step form (STEP, paged_decode_step with 8-row tiles) also appends: the
+//     producer writes the step's new K/V rows of its kv head into the chunk's
+//     blocks (append_row.cuh) once the ring is full or before the first block
+//     holding one is loaded, and orders the writes before its TMA loads.
 //   * Every wait is bounded (WAIT_LIMIT_NS); a late barrier sets
 //     KV_DEVERR_TIMEOUT and the CTA drains its copies and returns.
 #pragma once

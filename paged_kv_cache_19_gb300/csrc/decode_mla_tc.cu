@@ -730,6 +730,9 @@ __global__ void __launch_bounds__(TC_M, 4)
 paged_mla_merge_tc(const MlaParams p)
 {
     __shared__ uint32_t tile[TC_M][17];             // bf16 pairs, padded rows
+    // The next kernel may start launching now (its CTAs set up beside this grid's small
+    // CTAs); it reads nothing before waiting for this grid to complete.
+    grid_dependents_launch();
     grid_dependency_wait();
     const int cg = blockIdx.x;                      // 32-number chunk of the half
     const int ht = blockIdx.y >> 1, dq = blockIdx.y & 1;
@@ -798,7 +801,6 @@ paged_mla_merge_tc(const MlaParams p)
                     make_uint4(tile[rr][4 * qd], tile[rr][4 * qd + 1], tile[rr][4 * qd + 2], tile[rr][4 * qd + 3]);
         }
     }
-    grid_dependents_launch();
 }
 
 cudaError_t prepare_mla_decode_tc()

@@ -668,6 +668,9 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 __global__ void __launch_bounds__(256)
 paged_mla_merge_tcn(const MlaParams p)
 {
+    // The next kernel may start launching now (its CTAs set up beside this grid's small
+    // CTAs); it reads nothing before waiting for this grid to complete.
+    grid_dependents_launch();
     grid_dependency_wait();
     const int b = blockIdx.x, ht = blockIdx.y, qd = blockIdx.z;
     const int h = threadIdx.x >> 4, cg = threadIdx.x & 15;
@@ -718,7 +721,6 @@ paged_mla_merge_tcn(const MlaParams p)
         if (p.lse != nullptr && qd == 0 && cg == 0)
             p.lse[static_cast<size_t>(b) * p.q_heads + ht * TN_H + h] = lse_from(M, W);
     }
-    grid_dependents_launch();
 }
 
 cudaError_t prepare_mla_decode_tcn()
