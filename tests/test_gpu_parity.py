@@ -60,6 +60,14 @@ SMALL = {
                             prefix_tokens=64, split_tokens=32),
     "fp8_hkv8_split256": C(batch=3, q_heads=8, kv_heads=8, head_dim=128, block_size=32,
                            ctx=[5, 700, 1500], seed=115, cache_dtype="fp8_e4m3", split_tokens=256),
+    # the automatic chunk on kv-head counts the group layouts divide (6 -> pairs, 12 -> fours)
+    # or do not (fp8 with 2 kv heads keeps one CTA per kv head)
+    "hkv6_g3_pairs": C(batch=4, q_heads=18, kv_heads=6, head_dim=128, block_size=16,
+                       ctx=[2, 160, 1300, 47], seed=118),
+    "fp8_hkv12_fours": C(batch=3, q_heads=12, kv_heads=12, head_dim=128, block_size=32,
+                         ctx=[33, 900, 2100], seed=119, cache_dtype="fp8_e4m3"),
+    "fp8_hkv2_per_head": C(batch=3, q_heads=8, kv_heads=2, head_dim=128, block_size=32,
+                           ctx=[64, 250, 3000], seed=120, cache_dtype="fp8_e4m3"),
 }
 
 
