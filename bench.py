@@ -24,7 +24,6 @@ import argparse
 import glob
 import hashlib
 import json
-import math
 import os
 import re
 import statistics

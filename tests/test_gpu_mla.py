@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_kv_cache_19_gb300 as kp
 import workloads
-from gpu_util import LSE_ABS, MAX_ABS, REL_L2, Staged, bf16_tensor, compare, i32
+from gpu_util import LSE_ABS, MAX_ABS, REL_L2, Staged, compare, i32
 
 pytestmark = pytest.mark.gpu
 

@@ -10,7 +10,7 @@ import oracle
 import paged_kv_cache_19_gb300 as kp
 import workloads
 from gpu_util import (FP8_GATE_MIN_CTX, FP8_VS_UNQUANTISED_MAX_ABS, LSE_ABS, MAX_ABS, REL_L2,
-                      Staged, bf16_tensor, compare, i32)
+                      Staged, compare, i32)
 
 pytestmark = pytest.mark.gpu
 

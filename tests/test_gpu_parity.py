@@ -5,7 +5,6 @@ within max |err| <= 2e-2 and relative L2 <= 5e-3 (bf16 storage, fp32
 accumulation); for the fp8 cache also within 6e-2 of the oracle on the
 unquantised values.
 """
-import math
 import os
 
 import numpy as np
