@@ -73,11 +73,11 @@ KERNEL_SOURCES = {
             "device_common.cuh", "append_row.cuh"],
     "gqa_heads": ["decode_heads.cuh", "decode_heads.cu", "decode_common.cuh", "device_common.cuh",
                   "append_row.cuh"],
-    "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh"],
+    "mla": ["decode_mla.cu", "decode_common.cuh", "device_common.cuh", "append_row.cuh"],
     "mla_tc": ["decode_mla_tc.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
-               "device_common.cuh"],
+               "device_common.cuh", "append_row.cuh"],
     "mla_tcn": ["decode_mla_tcn.cu", "mla_partition.cuh", "tcgen05.cuh", "decode_common.cuh",
-                "device_common.cuh"],
+                "device_common.cuh", "append_row.cuh"],
 }
 
 
@@ -548,11 +548,12 @@ class Staged:
         self.two_kernels = self.kind in ("mla_tc", "mla_tcn") and self.max_splits > 1
         # paged_decode_step on a K/V pool whose kv heads have at most 8 query rows is one
         # kernel (its CTAs write the new rows before loading their blocks), else the append
-        # kernel then the attention; on a latent pool the append kernel, then the attention
-        # (and the merge kernel of the tensor-core forms when sequences can be cut)
+        # kernel then the attention; on a latent pool the attention kernel writes the new
+        # vectors itself (plus the merge kernel of the tensor-core forms when sequences can
+        # be cut)
         rows = s.q_heads // s.kv_heads * s.q_len
         if s.mla:
-            self.launches_per_step = 3 if self.two_kernels else 2
+            self.launches_per_step = 2 if self.two_kernels else 1
         else:
             self.launches_per_step = 1 if rows <= 8 else 2
 
@@ -575,9 +576,8 @@ class Staged:
                                            stream=self.stream)
 
     def run_step(self, kk, vv, qq, tt, cc, out=None):
-        """One decode step through the public API: append + attention in one call, the
-        attention overlapping the append -- paged_decode_step for K/V caches,
-        paged_mla_decode_step for latent pools.  The step's tokens are the last q_len of
+        """One decode step through the public API: append + attention in one call --
+        paged_decode_step for K/V caches, paged_mla_decode_step for latent pools.  The step's tokens are the last q_len of
         every sequence, in sequence order, which is the layout both calls take."""
         kp, s, w = self.kp, self.s, self.w
         out = self.out if out is None else out

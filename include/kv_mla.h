@@ -99,9 +99,12 @@ kv_status paged_mla_decode_attention(const kv_pool* pool, const void* q, int q_h
 /*
  * One decode step over a latent pool in one call: append each sequence's new cached
  * vector at position context_lens[b] - 1 (as paged_kv_append with token i = sequence i
- * and no V half), then paged_mla_decode_attention.  The attention kernel starts while
- * the append runs and waits for it only before loading the block that holds the new
- * vector.  Results are bit-identical to the two separate calls.
+ * and no V half), then paged_mla_decode_attention.  No separate append kernel runs:
+ * each CTA that loads the block holding a sequence's new vector writes the vector into it
+ * before that load (several CTAs may write the same bytes).  Pool bytes, outputs and device
+ * error bits are identical to the two separate calls: a position outside the table
+ * (context_lens[b] < 1 or beyond max_blocks * block_size) is flagged
+ * KV_DEVERR_POSITION and not written, a bad block id KV_DEVERR_BLOCK_ID.
  *   kv_new: bf16 [batch, 576], 16-byte aligned (512 latent + 64 rotary-key numbers).
  *   Every other argument as for paged_mla_decode_attention.  All arguments are checked
  *   before anything is launched; on an error nothing is appended.

@@ -638,8 +638,9 @@ def paged_mla_decode_step(pool: Pool, kv_new, q, block_tables, context_lens, sca
                           kv_split_tokens: int = 0, workspace=None, out=None, lse=None,
                           stream=None, latent_dim: int = 512):
     """One step over a latent pool: append kv_new bf16 [B, latent + rope] at position
-    context_lens[b] - 1 of each sequence, then the absorbed MLA decode (one call, the
-    attention overlapping the append).  Returns out bf16 [B, Hq, latent]."""
+    context_lens[b] - 1 of each sequence, then the absorbed MLA decode (one call: the
+    attention kernel writes the new vectors before it loads their blocks).  Returns out
+    bf16 [B, Hq, latent]."""
     lib = load_library()
     _need(kv_new, torch.bfloat16, "kv_new")
     _need(q, torch.bfloat16, "q")

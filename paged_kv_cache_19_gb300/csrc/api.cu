@@ -974,7 +974,8 @@ kv_status make_mla_launch(const kv_pool* pool, const void* q, int q_heads, const
     p.split_blocks = plan.split_blocks;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.dep_tail = 0;
+    p.kv_new = nullptr;
+    p.pool = nullptr;
     *plan_out = plan;
     return KV_OK;
 }
@@ -1041,30 +1042,10 @@ kv_status paged_mla_decode_step(kv_pool* pool, const void* kv_new, const void* q
                                    kv_split_tokens, workspace, workspace_bytes, out, lse_out, &plan, &p);
     if (st != KV_OK || batch == 0) return st;
     if (kv_new == nullptr || !aligned(kv_new, 16)) return KV_ERR_INVALID_ARG;
-    kvp::AppendParams a;
-    a.k_new = static_cast<const uint16_t*>(kv_new);
-    a.v_new = nullptr;
-    a.token_seq = nullptr;
-    a.token_pos = nullptr;
-    a.tables = block_tables;
-    a.ctx = context_lens;
-    a.k_pool = pool->k;
-    a.v_pool = nullptr;
-    a.k_scale = pool->k_scale;
-    a.v_scale = pool->v_scale;
-    a.err = pool->err;
-    a.num_tokens = batch;
-    a.batch = batch;
-    a.max_blocks = max_blocks;
-    a.num_blocks = pool->num_blocks;
-    a.block_size = pool->block_size;
-    a.kv_heads = pool->kv_heads;
-    a.head_dim = pool->head_dim;
-    a.fp8 = false;
-    a.q_len = 1;
-    if (kvp::launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KV_ERR_CUDA;
-    // the append wrote only the last position of each sequence
-    p.dep_tail = 1;
+    // One attention launch (plus the merge of cut sequences): the CTA that reads the block
+    // holding a sequence's new vector writes it into the pool first (the append's bytes).
+    p.kv_new = static_cast<const uint16_t*>(kv_new);
+    p.pool = pool->k;
     return launch_mla(pool, plan, p, stream);
 }
 

@@ -78,4 +78,47 @@ __device__ __forceinline__ void fence_proxy_async_all()
     asm volatile("fence.proxy.async;" ::: "memory");
 }
 
+// paged_mla_decode_step: the logical block that holds sequence b's new vector (position
+// ctx - 1), or -1 when the call appends nothing or the position is outside the table
+// (flagged KV_DEVERR_POSITION elsewhere, as the append would).
+__device__ __forceinline__ int mla_step_block(const MlaParams& p, int b, int bs)
+{
+    if (p.kv_new == nullptr) return -1;
+    const int raw = __ldg(p.ctx + b);
+    if (raw < 1 || raw > p.max_blocks * bs) return -1;
+    return (raw - 1) / bs;
+}
+
+// paged_mla_decode_step: thread t of nth (nth >= 24) copies its share of sequence b's new
+// vector (row b of kv_new, MLA_DK bf16 numbers = 72 vectors of 16 bytes) into slot `slot`
+// of pool block blk: vectors t, t + nth, t + 2 nth, all loaded before any is stored.  The
+// caller orders the writes before the TMA loads of the block (fence_proxy_async_all, then a
+// barrier the loading thread waits on).
+__device__ __forceinline__ void load_latent_share(const MlaParams& p, int b, int t, int nth, uint4 (&x)[3])
+{
+    constexpr int NV = MLA_DK / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(p.kv_new + static_cast<size_t>(b) * MLA_DK);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (t + i * nth < NV) x[i] = __ldg(src + t + i * nth);
+}
+
+__device__ __forceinline__ void store_latent_share(const MlaParams& p, int blk, int bs, int slot, int t,
+                                                   int nth, const uint4 (&x)[3])
+{
+    constexpr int NV = MLA_DK / 8;
+    uint4* dst = reinterpret_cast<uint4*>(p.pool + (static_cast<size_t>(blk) * bs + slot) * MLA_DK * 2);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (t + i * nth < NV) dst[t + i * nth] = x[i];
+}
+
+__device__ __forceinline__ void write_latent_share(const MlaParams& p, int b, int blk, int bs, int slot,
+                                                   int t, int nth)
+{
+    uint4 x[3];
+    load_latent_share(p, b, t, nth, x);
+    store_latent_share(p, blk, bs, slot, t, nth, x);
+}
+
 }  // namespace kvp

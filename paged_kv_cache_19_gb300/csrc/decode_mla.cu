@@ -31,9 +31,13 @@
 //     computed once, before the loop.
 //   * split chunks leave fp32 partials and the last one to finish merges them by
 //     log-sum-exp (ticket in the workspace), as in the GQA decode kernel.
+//   * paged_mla_decode_step: the CTA whose chunk holds the block with the sequence's
+//     new vector writes it there (72 threads, 16 bytes each) before the barrier that
+//     precedes every load.
 // Every wait is bounded; a stage that does not arrive sets KV_DEVERR_TIMEOUT and
 // all consumer warps leave the loop together (the decision is shared across the
 // exchange barrier), after the loads in flight have landed (bounded waits).
+#include "append_row.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
 
@@ -48,6 +52,7 @@ struct MlaCfg {
     static constexpr int SPB = BS / SUB;            // stages per block
     static constexpr int NCW = 4;
     static constexpr int THREADS = (NCW + (PROD ? 1 : 0)) * 32;
+    static_assert(NCW * 32 >= MLA_DK / 8, "the step's new vector: one 16-byte vector a thread");
     static constexpr int NT = 16;                   // heads per CTA
     static constexpr int NTT = NT / 8;
     static constexpr int MT = SUB / 16;             // 16-token slices per stage
@@ -91,15 +96,10 @@ __device__ __forceinline__ uint32_t swz_off(int tok, int ch)
 template <class C, int SUB, int NSTAGE>
 __device__ __forceinline__ void issue_stage(int it, const int32_t* trow, int num_blocks,
                                             uint8_t* smem, uint64_t* full, int* stage_blk,
-                                            const CUtensorMap* tmc, uint32_t* err, int tail_j,
-                                            bool& waited)
+                                            const CUtensorMap* tmc, uint32_t* err)
 {
     const int j = it / C::SPB;
     const int sub = it - j * C::SPB;
-    if (!waited && j >= tail_j) {                  // a block the preceding append wrote to
-        grid_dependency_wait();
-        waited = true;
-    }
     int blk = __ldg(trow + j);
     if (blk < 0 || blk >= num_blocks) {
         atomicOr(err, KV_DEVERR_BLOCK_ID);
@@ -150,9 +150,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         flags[0] = 0;
         fence_mbar_init();
     }
-    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
-    // positions of each sequence: then the loads of the blocks that hold them wait.
-    if (p.dep_tail == 0) grid_dependency_wait();
+    grid_dependency_wait();                          // inputs of the preceding kernel are ready
 
     const int32_t* trow = p.tables + static_cast<size_t>(b) * p.max_blocks + blk0;
     int id_first = -1;
@@ -180,10 +178,26 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         ctx = ctx < 0 ? 0 : cap;
     }
     const int nblk = (ctx + BS - 1) / BS;
-    const int tail_blk = (ctx - p.dep_tail) / BS;   // first block the preceding append wrote
     const int nsplit = nblk > 0 ? (nblk + p.split_blocks - 1) / p.split_blocks : 1;
     const int nb = max(0, min(nblk - blk0, p.split_blocks));
     const int nstages = nb * C::SPB;
+    // paged_mla_decode_step: a position outside the table is flagged once per sequence (as
+    // the append would) and not written; a CTA whose chunk holds the block with the new
+    // vector writes it there first (its first 72 threads, one 16-byte vector each), before
+    // the barrier that precedes every load.  Several head tiles write the same bytes.
+    if (p.kv_new != nullptr) {
+        const int raw = __ldg(p.ctx + b);
+        if (threadIdx.x == 0 && split == 0 && ht == 0 && (raw < 1 || raw > cap))
+            atomicOr(p.err, KV_DEVERR_POSITION);
+        const int step_j = mla_step_block(p, b, BS) - blk0;
+        if (step_j >= 0 && step_j < nb && threadIdx.x < MLA_DK / 8) {
+            const int bid = __ldg(trow + step_j);
+            if (bid >= 0 && bid < p.num_blocks) {   // a bad id is flagged by the load path
+                write_latent_share(p, b, bid, BS, (raw - 1) % BS, threadIdx.x, MLA_DK / 8);
+                fence_proxy_async_all();
+            }
+        }
+    }
     __syncthreads();                                 // barriers initialised
     if (split >= nsplit) {
         grid_dependents_launch();
@@ -195,7 +209,6 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         if (lane == 0) prefetch_tensormap(&tmc);
         int issued = 0;
         bool ok = true;
-        bool waited = p.dep_tail == 0;
         for (int base = 0; base < nb && ok; base += 32) {
             const int j = base + lane;
             int id = -1;
@@ -216,10 +229,6 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
                     const uint32_t ph = static_cast<uint32_t>(it / NSTAGE) & 1u;
                     int good = 1;
                     if (lane == 0) {
-                        if (!waited && blk0 + base + k >= tail_blk) {
-                            grid_dependency_wait();
-                            waited = true;
-                        }
                         if (!mbar_wait_bounded(smem_u32(empty + st), ph ^ 1u)) {
                             atomicOr(p.err, KV_DEVERR_TIMEOUT);
                             good = 0;
@@ -259,12 +268,11 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
 
     // ------------------------------------------------------------ consumer warps
     int issued = 0;                                  // thread 0 (not PROD): loads issued
-    bool dep_waited = p.dep_tail == 0;               // thread 0 (not PROD): waited for the append
     if (!PROD && threadIdx.x == 0) {
         prefetch_tensormap(&tmc);
         for (; issued < min(NSTAGE, nstages); ++issued)
             issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
-                                        p.err, tail_blk - blk0, dep_waited);
+                                        p.err);
     }
 
     MlaState st;
@@ -342,7 +350,7 @@ paged_mla_decode_main(const __grid_constant__ CUtensorMap tmc, const MlaParams p
         if (flags[0]) break;                        // a stage never arrived: all warps leave
         if (!PROD && threadIdx.x == 0 && it >= 1 && issued < nstages) {
             issue_stage<C, SUB, NSTAGE>(issued, trow, p.num_blocks, smem, full, stage_blk, &tmc,
-                                        p.err, tail_blk - blk0, dep_waited);   // into the slot of stage it - 1
+                                        p.err);   // into the slot of stage it - 1
             ++issued;
         }
         if (blk < 0) {                              // skipped (bad id): nothing to fold in

@@ -46,9 +46,14 @@
 //   * tensor memory: queries [0, 160), scores [160, 224), probabilities
 //     [224, 256), output [256, 512).  Shared memory: 2 stages (144 KB), the
 //     queries' other 256 numbers (64 KB, K-major, 128-byte swizzle), control.
+//   * paged_mla_decode_step: lanes 1-31 of the producer warp walk the same partition and
+//     write the new vector of each sequence whose last block lies in the range into that
+//     block; the producer lane waits on an mbarrier for those writes before it loads such
+//     a block.
 // Every wait is bounded; a late barrier sets KV_DEVERR_TIMEOUT and every role
 // leaves its loop, waits (bounded) for its copies and MMAs in flight, and the CTA
 // frees its tensor memory before it exits.
+#include "append_row.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
 #include "mla_partition.cuh"
@@ -110,6 +115,7 @@ struct TcCtl {
     TcItem items[TC_NITEM];
     float xmax[2][2][TC_M];                         // [stage parity][token half][head]
     float xl[2][TC_M];                              // [token half][head]
+    uint64_t step_done;                             // paged_mla_decode_step: new vectors written
 };
 static_assert(sizeof(TcCtl) <= TC_CTL, "control block");
 
@@ -206,14 +212,12 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         mbar_init(smem_u32(&ctl->p_free), 1);
         mbar_init(smem_u32(&ctl->q_ready), 8);
         mbar_init(smem_u32(&ctl->mma_done), 1);
+        mbar_init(smem_u32(&ctl->step_done), 31);   // lanes 1-31 of the producer warp
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 9) tc_alloc(smem_u32(&ctl->tmem_base), TM_COLS);
-    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
-    // positions of each sequence: then the producer waits, before the first load of a block
-    // that holds one of them.
-    if (p.dep_tail == 0) grid_dependency_wait();
+    grid_dependency_wait();                     // inputs of the preceding kernel are ready
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -231,7 +235,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             int g = 0;                              // stages issued (all items)
             int ge = 0, gl = 0;                     // stages with score-only / output loads issued
             bool ok = true;
-            bool waited = p.dep_tail == 0;
+            bool step_written = false;              // paged_mla_decode_step: waited for lanes 1-31
             for (;;) {
                 TcItem it{};
                 it.n = -1;
@@ -268,6 +272,8 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 if (last) break;
                 const int32_t* trow = p.tables + static_cast<size_t>(it.b) * p.max_blocks + it.blk0;
                 int next_blk = __ldg(trow);         // block id read one stage ahead
+                // paged_mla_decode_step: the segment's stage whose block holds the new vector
+                const int step_s = mla_step_block(p, it.b, TC_TOK) - it.blk0;
                 for (int s = 0; s < it.n; ++s, ++g) {
                     const int st = g % TC_NSTAGE;
                     const uint32_t ph = (static_cast<uint32_t>(g / TC_NSTAGE) & 1u) ^ 1u;
@@ -277,15 +283,18 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         atomicOr(p.err, KV_DEVERR_BLOCK_ID);
                         bid = -1;
                     }
+                    if (s == step_s && bid >= 0 && !step_written) {   // holds a new vector
+                        if (!mbar_wait_bounded(smem_u32(&ctl->step_done), 0u)) {
+                            ok = false;
+                            break;
+                        }
+                        step_written = true;
+                    }
                     const uint32_t dst = smem_u32(smem + st * TC_STAGE);
                     // score-only pieces: free once the scores of the stage two back are done
                     if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty_e[st]), ph) || *abort_flag) {
                         ok = false;
                         break;
-                    }
-                    if (!waited && it.blk0 + s >= (it.ctx - p.dep_tail) / TC_TOK) {
-                        grid_dependency_wait();
-                        waited = true;
                     }
                     const uint32_t fe = smem_u32(&ctl->kv_full_e[st]);
                     if (bid >= 0) {
@@ -333,6 +342,11 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 if (!mbar_wait_bounded(smem_u32(&ctl->kv_full_l[j % TC_NSTAGE]),
                                        static_cast<uint32_t>(j / TC_NSTAGE) & 1u))
                     break;
+        } else {
+            // the next kernel may start launching (it waits for this grid's completion
+            // before reading anything); lanes 1-31 write the step's new vectors, if any
+            grid_dependents_launch();
+            if (p.kv_new != nullptr) part.write_step_rows(smem_u32(&ctl->step_done), lane - 1, 31);
         }
         grid_dependents_launch();
     } else if (warp == 9) {

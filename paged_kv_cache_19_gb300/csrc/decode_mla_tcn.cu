@@ -48,9 +48,14 @@
 //   * tensor memory: the queries' latent numbers [0, 256), two score buffers [256,
 //     384), output tiles at 384, 416, 448, 480 (16 columns each); the queries' 64
 //     rotary numbers sit in shared memory.
+//   * paged_mla_decode_step (the STEP instantiation, 224 threads): warp 6 walks the
+//     same partition and writes the new vector of each sequence whose last block lies in
+//     the range into that block; warp 4 waits on an mbarrier for those writes before it
+//     loads such a block.
 // Every wait is bounded; a late barrier sets KV_DEVERR_TIMEOUT and every role leaves
 // its loop, waits (bounded) for its copies and MMAs in flight, and the CTA frees its
 // tensor memory before it exits.
+#include "append_row.cuh"
 #include "decode_common.cuh"
 #include "kernels.h"
 #include "mla_partition.cuh"
@@ -68,6 +73,7 @@ constexpr int TN_NPIECE = MLA_DK / 64;          // 9
 constexpr int TN_STAGE = TN_NPIECE * TN_PIECE;  // 73,728 bytes
 constexpr int TN_PBUF = TN_H * 128;             // P^T: a 128-byte row of 64 bf16 per head
 constexpr int TN_THREADS = 192;                 // warps 0-3 softmax / epilogue, 4 loads, 5 MMA
+constexpr int TN_THREADS_STEP = 224;            // + warp 6: the step's new vectors
 constexpr int TN_EPI = 128;                     // threads of warps 0-3
 // tensor memory: the queries' 512 latent numbers [0, 256), two score buffers [256, 320)
 // and [320, 384), output tiles at 384, 416, 448, 480 (16 columns each)
@@ -103,6 +109,7 @@ struct TnCtl {
     MlaSegment items[TN_NITEM];
     float fac[TN_H];                                // per-head factors of a rescale
     float lsum[TN_H], mref[TN_H];                   // per-head (sum, max) at a segment's end
+    uint64_t step_done;                             // paged_mla_decode_step: new vectors written
 };
 static_assert(sizeof(TnCtl) <= TN_CTL, "control block");
 
@@ -223,7 +230,9 @@ __device__ __forceinline__ void load_queries(const MlaParams& p, int b, int ht, 
 
 }  // namespace
 
-__global__ void __launch_bounds__(TN_THREADS, 1)
+// STEP: paged_mla_decode_step (p.kv_new set), whose new vectors a seventh warp writes.
+template <bool STEP>
+__global__ void __launch_bounds__(STEP ? TN_THREADS_STEP : TN_THREADS, 1)
 paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -257,14 +266,12 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         mbar_init(smem_u32(&ctl->o_full), 1);
         mbar_init(smem_u32(&ctl->o_free), 4);
         mbar_init(smem_u32(&ctl->mma_done), 1);
+        mbar_init(smem_u32(&ctl->step_done), 32);   // the lanes of warp 6 (STEP)
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 5) tc_alloc(smem_u32(&ctl->tmem_base), TN_COLS);
-    // Inputs of the preceding kernel are ready -- unless it only appended the last dep_tail
-    // positions of each sequence: then the producer waits, before the first load of a block
-    // that holds one of them.
-    if (p.dep_tail == 0) grid_dependency_wait();
+    grid_dependency_wait();                     // inputs of the preceding kernel are ready
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -279,7 +286,7 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             int k = 0;                              // segments handed on
             int g = 0;                              // stages issued (all segments)
             bool ok = true;
-            bool waited = p.dep_tail == 0;
+            bool step_written = false;              // paged_mla_decode_step: waited for lanes 1-31
             for (;;) {
                 const MlaSegment it = *abort_flag ? MlaSegment{0, 0, 0, -1, 0, 0, 0} : part.next();
                 const bool last = it.n < 0;
@@ -300,6 +307,8 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 if (last) break;
                 const int32_t* trow = p.tables + static_cast<size_t>(it.b) * p.max_blocks + it.blk0;
                 int next_blk = __ldg(trow);         // block id read one stage ahead
+                // paged_mla_decode_step: the segment's stage whose block holds the new vector
+                const int step_s = STEP ? mla_step_block(p, it.b, TN_TOK) - it.blk0 : -1;
                 for (int s = 0; s < it.n; ++s, ++g) {
                     const int st = g % TN_NSTAGE;
                     int bid = next_blk;
@@ -308,6 +317,13 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         atomicOr(p.err, KV_DEVERR_BLOCK_ID);
                         bid = -1;
                     }
+                    if (STEP && s == step_s && bid >= 0 && !step_written) {   // warp 6 wrote it?
+                        if (!mbar_wait_bounded(smem_u32(&ctl->step_done), 0u)) {
+                            ok = false;
+                            break;
+                        }
+                        step_written = true;
+                    }
                     if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty[st]),
                                            (static_cast<uint32_t>(g / TN_NSTAGE) & 1u) ^ 1u) ||
                         *abort_flag) {
@@ -315,10 +331,6 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         break;
                     }
                     ctl->stage_blk[st] = bid;
-                    if (!waited && it.blk0 + s >= (it.ctx - p.dep_tail) / TN_TOK) {
-                        grid_dependency_wait();
-                        waited = true;
-                    }
                     const uint32_t fb = smem_u32(&ctl->kv_full[st]);
                     if (bid >= 0) {
                         const uint32_t dst = smem_u32(stages + st * TN_STAGE);
@@ -342,6 +354,13 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     break;
         }
         grid_dependents_launch();
+    } else if (STEP && warp == 6) {
+        // ------------------------------------------------------------ the step's new vectors
+        // The same partition, walked beside the producer: every block of the range that holds
+        // a sequence's new vector gets it before the producer loads that block.
+        MlaPartition<TN_TOK, MLA_SEG_PAD_NARROW> part;
+        part.init(p, p.head_tiles, lane, false);
+        part.write_step_rows(smem_u32(&ctl->step_done), lane, 32);
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
@@ -725,14 +744,19 @@ paged_mla_merge_tcn(const MlaParams p)
 
 cudaError_t prepare_mla_decode_tcn()
 {
-    return cudaFuncSetAttribute(paged_mla_decode_tcn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(paged_mla_decode_tcn<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TN_SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(paged_mla_decode_tcn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 TN_SMEM);
 }
 
 cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
                                   cudaStream_t s)
 {
-    cudaError_t e = launch_dependent(paged_mla_decode_tcn, grid, dim3(TN_THREADS), TN_SMEM, s, tm, p);
+    cudaError_t e = p.kv_new != nullptr
+                        ? launch_dependent(paged_mla_decode_tcn<true>, grid, dim3(TN_THREADS_STEP), TN_SMEM, s, tm, p)
+                        : launch_dependent(paged_mla_decode_tcn<false>, grid, dim3(TN_THREADS), TN_SMEM, s, tm, p);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     return launch_dependent(paged_mla_merge_tcn, dim3(p.batch, p.head_tiles, MLA_DV / 128), dim3(256), 0, s, p);
 }

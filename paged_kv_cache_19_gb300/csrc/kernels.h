@@ -98,9 +98,11 @@ struct MlaParams {
     int split_blocks, max_splits;   // chunk length in blocks (tcgen05 form: least blocks per CTA
                                     // range); most chunks (pieces) a sequence can have
     float scale_log2;
-    int dep_tail;             // 0: wait for the preceding kernel before reading anything; n > 0:
-                              // it wrote only the last n positions of each sequence (the step's
-                              // append), and only the loads of the blocks holding them wait
+    // paged_mla_decode_step: the step's new vectors (bf16 [batch, MLA_DK], sequence b's at
+    // position ctx - 1), which the CTA reading the block that holds one writes into the
+    // latent pool first; null for the attention alone.
+    const uint16_t* kv_new;
+    uint8_t* pool;
 };
 
 // Launch with programmatic stream serialisation: the kernel may begin launching

@@ -23,6 +23,7 @@
 // the end of either range.
 #pragma once
 
+#include "append_row.cuh"
 #include "device_common.cuh"
 #include "kernels.h"
 
@@ -39,7 +40,7 @@ struct MlaPartition {
     const MlaParams* p;
     long long S, T, gact, u0, u1, c;
     int cap;
-    // the cursor (lane 0 only after init)
+    // the cursor (each lane walks its own copy after init)
     long long u, ls, ub_l, pre;
     int outer, b, blk, outer_l, b_last, ctx_l, nb_l;
     bool last_done;
@@ -56,10 +57,11 @@ struct MlaPartition {
     // Warp-wide (all 32 lanes): block count of the batch, the range of this CTA and the
     // sequences at its ends.  Out-of-range context lengths are flagged and clamped; an
     // empty sequence has no units, so its output (0) and LSE (-inf) are written here, by
-    // CTA b mod gridDim.x.  Batches of up to 256 sequences keep their lengths and block
+    // CTA b mod gridDim.x (all of this only when `outputs`; a second warp walking the same
+    // partition passes false).  Batches of up to 256 sequences keep their lengths and block
     // prefix sums in registers (sequence 32 i + lane in slot i), so that the range ends
     // are located without loading the lengths again.
-    __device__ void init(const MlaParams& params, int nouter, int lane)
+    __device__ void init(const MlaParams& params, int nouter, int lane, bool outputs = true)
     {
         p = &params;
         cap = p->max_blocks * TOK;
@@ -77,12 +79,13 @@ struct MlaPartition {
                 const int bb = b0 + i * 32 + lane;
                 int x = raw[i];
                 if (bb < p->batch && (x < 0 || x > cap)) {
-                    if (blockIdx.x == 0) atomicOr(p->err, KV_DEVERR_CONTEXT);
+                    if (blockIdx.x == 0 && outputs) atomicOr(p->err, KV_DEVERR_CONTEXT);
                     x = x < 0 ? 0 : cap;
                 }
                 const int nb = (x + TOK - 1) / TOK;
                 const int wv = nb > 0 ? nb + PAD : 0;   // positions of the sequence
-                if (bb < p->batch && nb == 0 && bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+                if (outputs && bb < p->batch && nb == 0 &&
+                    bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
                     uint4* dst = reinterpret_cast<uint4*>(p->out + static_cast<size_t>(bb) * p->q_heads * MLA_DV);
                     for (int v = 0; v < p->q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
                     if (p->lse != nullptr)
@@ -204,6 +207,40 @@ struct MlaPartition {
         it.split = static_cast<int>(c) - cf;
         it.nsplit = cta_of(first + nb - 1) - cf + 1;
         return it;
+    }
+
+    // paged_mla_decode_step, thread t of the nth (>= 24) lanes that walk the partition after
+    // init, each on its own cursor: every segment of the range that holds the block with a
+    // sequence's new vector (position ctx - 1) gets the vector written into that block, the
+    // lanes sharing each copy; then each lane orders its writes before later TMA loads and
+    // arrives once on `done` (expected count nth).  The thread that loads the blocks waits on
+    // `done` before it loads such a block.  Blocks with a bad id are skipped (the loading
+    // thread flags them when it reaches them); a position outside the table is not written
+    // and is flagged KV_DEVERR_POSITION by CTA 0, as the append would flag it.  Several CTAs,
+    // or both halves of one, may write the same bytes.
+    __device__ void write_step_rows(uint32_t done, int t, int nth)
+    {
+        if (blockIdx.x == 0)
+            for (int bb = t; bb < p->batch; bb += nth) {
+                const int x = __ldg(p->ctx + bb);
+                if (x < 1 || x > cap) atomicOr(p->err, KV_DEVERR_POSITION);
+            }
+        for (;;) {
+            const MlaSegment sg = next();
+            if (sg.n < 0) break;
+            const int raw = __ldg(p->ctx + sg.b);
+            if (raw < 1 || raw > cap) continue;
+            const int j = (raw - 1) / TOK;
+            if (j < sg.blk0 || j >= sg.blk0 + sg.n) continue;
+            // the block id and the new vector are loaded together
+            const int bid = __ldg(p->tables + static_cast<size_t>(sg.b) * p->max_blocks + j);
+            uint4 x[3];
+            load_latent_share(*p, sg.b, t, nth, x);
+            if (bid < 0 || bid >= p->num_blocks) continue;
+            store_latent_share(*p, bid, TOK, (raw - 1) % TOK, t, nth, x);
+        }
+        fence_proxy_async_all();
+        mbar_arrive(done);
     }
 
     // One thread: the next segment of the range (n < 0: none left).

@@ -178,7 +178,7 @@ MLA_STEP = {
     "wide_bs64_h128": M(batch=3, q_heads=128, block_size=64, ctx=[1, 70, 900], seed=314,
                         split_tokens=64),
     # a grid of more than three CTAs per SM: the mma.sync form without a producer warp, whose
-    # loads are issued by a consumer thread (the one that waits for the append)
+    # loads (and the write of the new vector before them) are issued by a consumer thread
     "mma_bs16_h128_many_ctas": M(batch=24, q_heads=128, block_size=16, ctx_uniform=(1, 300),
                                  seed=316, split_tokens=64),
 }
@@ -217,6 +217,56 @@ def test_mla_step_matches_the_oracle_and_the_separate_calls(name):
     fused.destroy()
 
 
+MLA_EDGE = {
+    "mma_bs16_h16": (M(batch=4, q_heads=16, block_size=16, ctx=[10, 40, 33, 50], seed=318), 16),
+    "narrow_bs64_h16": (M(batch=4, q_heads=16, block_size=64, ctx=[10, 140, 70, 200], seed=319),
+                        64),
+    "wide_bs64_h128": (M(batch=4, q_heads=128, block_size=64, ctx=[10, 140, 70, 200], seed=320),
+                       64),
+    "mma_bs16_h128_many_ctas": (M(batch=24, q_heads=128, block_size=16, ctx_uniform=(20, 300),
+                                  seed=321), 16),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MLA_EDGE))
+def test_mla_step_writes_and_flags_what_the_separate_append_does(name):
+    """A latent step whose new vectors fall outside the block table (an empty sequence, one
+    longer than the table) or into a block with a bad id: the same pool bytes, device error
+    bits and output bits as paged_kv_append followed by the attention."""
+    spec, bs = MLA_EDGE[name]
+    w = workloads.make(spec)
+    bad_ctx = w.context_lens.astype(np.int32)
+    bad_ctx[0] = 0
+    bad_ctx[2] = w.max_blocks * bs + 5
+    bad_tables = w.block_tables.copy()
+    bad_tables[3, (bad_ctx[3] - 1) // bs] = -7        # the block that would hold the new vector
+    results = []
+    for fused in (True, False):
+        st = Staged(w, step_append=False)
+        ctx, tables = i32(bad_ctx), i32(bad_tables)
+        out = torch.empty(w.batch, spec.q_heads, spec.latent_dim, dtype=torch.bfloat16,
+                          device="cuda")
+        lse = torch.empty(w.batch, spec.q_heads, dtype=torch.float32, device="cuda")
+        if fused:
+            kp.paged_mla_decode_step(st.pool, st.k_new, st.q, tables, ctx, w.scale, out=out,
+                                     lse=lse, latent_dim=spec.latent_dim)
+        else:
+            kp.paged_kv_append(st.pool, st.k_new, None, tables, ctx)
+            kp.paged_mla_decode_attention(st.pool, st.q, tables, ctx, w.scale, out=out, lse=lse,
+                                          latent_dim=spec.latent_dim)
+        torch.cuda.synchronize()
+        bits = st.pool.device_errors()
+        kr = st.pool.raw_bytes()[0]
+        results.append((bits, kr.clone(), out.clone(), lse.clone()))
+        st.destroy()
+    (b1, k1, o1, l1), (b2, k2, o2, l2) = results
+    assert b1 == b2, (hex(b1), hex(b2))
+    assert b1 & kp.DEVERR_POSITION and b1 & kp.DEVERR_CONTEXT and b1 & kp.DEVERR_BLOCK_ID
+    assert torch.equal(k1, k2)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
 def test_mla_step_rejects_bad_arguments_before_launching():
     w = workloads.make(M(batch=2, q_heads=16, block_size=64, ctx=[10, 100], seed=315))
     st = Staged(w, step_append=False)
@@ -239,8 +289,8 @@ def test_mla_step_rejects_bad_arguments_before_launching():
 
 
 def test_repeated_mla_steps_on_one_stream_stay_exact():
-    """Several latent steps back to back on one stream, each attention overlapping the append
-    before it (the same step repeated: same bits each time)."""
+    """Several latent steps back to back on one stream, each kernel starting while the one
+    before it finishes (the same step repeated: same bits each time)."""
     w = workloads.make(M(batch=4, q_heads=16, block_size=64, ctx=[15, 64, 65, 600], seed=317,
                          split_tokens=64))
     st = Staged(w, step_append=False)
