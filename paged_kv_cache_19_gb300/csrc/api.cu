@@ -32,7 +32,9 @@ struct kv_pool {
                             // with the stage box of the producer-warp decode (tmk) and of
                             // the three-CTA decode (tmv)
     CUtensorMap tmt;        // latent pools with blocks of 64: one 128-byte piece of a block
-                            // per box (the tcgen05 decode)
+                            // per box (the wide tcgen05 decode)
+    CUtensorMap tmh;        // latent pools with blocks of 64: one 128-byte piece of 32 slots
+                            // per box (the narrow tcgen05 decode)
     int has_tc;
     int num_sms;
     int mla;                // 1: latent pool (one cached vector per token, no V half)
@@ -117,6 +119,27 @@ kv_status encode_pool_map(const kv_pool* p, uint8_t* base, CUtensorMap* map, int
     CUresult r = fn(map, dt, 5, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
+}
+
+// Tile map of the absorbed queries [batch, q_heads, MLA_DK] (bf16) for the narrow
+// tcgen05 decode: dims (innermost first) = number, head, sequence; a box is one 64-number
+// piece of min(16, q_heads) heads, written to shared memory with the 128-byte swizzle
+// (heads past q_heads read as zeros).
+kv_status encode_query_map(const uint16_t* q, int q_heads, int batch, CUtensorMap* map)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return KV_ERR_CUDA;
+    const cuuint64_t row = static_cast<cuuint64_t>(kvp::MLA_DK) * 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kvp::MLA_DK), static_cast<cuuint64_t>(q_heads),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {row, row * static_cast<cuuint64_t>(q_heads)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(q_heads < kvp::MLA_TCN_HEADS ? q_heads
+                                                                                       : kvp::MLA_TCN_HEADS), 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(q), dims, strides, box,
+                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? KV_OK : KV_ERR_CUDA;
 }
 
@@ -891,6 +914,7 @@ kv_status kv_mla_pool_create(int num_blocks, int block_size, int latent_dim, int
         st = encode_pool_map(p, p->k, &p->tmv, kvp::mla_stage_tokens(block_size, false));
     if (st == KV_OK && block_size == kvp::MLA_TC_BLOCK) {
         st = encode_pool_map(p, p->k, &p->tmt, block_size, 1);
+        if (st == KV_OK) st = encode_pool_map(p, p->k, &p->tmh, kvp::MLA_TCN_STAGE_TOKENS, 1);
         if (st == KV_OK && kvp::prepare_mla_decode_tc() != cudaSuccess) st = KV_ERR_CUDA;
         if (st == KV_OK && kvp::prepare_mla_decode_tcn() != cudaSuccess) st = KV_ERR_CUDA;
         p->has_tc = 1;
@@ -991,11 +1015,16 @@ kv_status launch_mla(const kv_pool* pool, const MlaPlan& plan, const kvp::MlaPar
         const long long ranges = units_max / plan.split_blocks > 0 ? units_max / plan.split_blocks : 1;
         const int sms = pool->num_sms > 0 ? pool->num_sms : 148;
         const dim3 grid(static_cast<unsigned>(ranges < sms ? ranges : sms));
-        const cudaError_t e =
-            plan.form == kMlaWide
-                ? kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream))
-                : kvp::launch_mla_decode_tcn(grid, pool->tmt, p, static_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+        if (plan.form == kMlaWide)
+            return kvp::launch_mla_decode_tc(grid, pool->tmt, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                       ? KV_OK
+                       : KV_ERR_CUDA;
+        CUtensorMap tq;
+        const kv_status st = encode_query_map(p.q, p.q_heads, p.batch, &tq);
+        if (st != KV_OK) return st;
+        return kvp::launch_mla_decode_tcn(grid, pool->tmh, tq, p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? KV_OK
+                   : KV_ERR_CUDA;
     }
     // chunk-major grid: x = head tile, y = sequence, z = chunk.  Grids of up to
     // three CTAs per SM run the producer-warp variant (32-token stages, two CTAs

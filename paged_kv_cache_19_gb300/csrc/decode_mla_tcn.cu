@@ -6,49 +6,52 @@
 // latent part).
 //
 // With 16 heads the work per cached byte is small (about 30 flop/byte), so the
-// kernel is meant to stream the cache at HBM speed; a tcgen05 MMA costs a fixed
-// ~50 cycles whatever its shape up to N = 64 (measured on GB300), so the shapes
-// are chosen for few instructions per token:
-//   * scores S[16 heads x 64 tokens] = Q . C^T: an M = 128 MMA whose rows 0-15
-//     (tensor-memory lanes 0-15) are the tile's heads, the other rows never read --
-//     A = the queries (latent part in tensor memory, rotary part in shared memory),
-//     B = the stage's nine K-major pieces -- 36
-//     MMAs of K = 16 per block.  (An M = 64 form costs the same per MMA, but
-//     alternating it with the M = 128 output MMAs left ~700 idle cycles at every
-//     switch in a trace of this kernel on GB300.)
+// kernel is meant to stream the cache at HBM speed.  A tcgen05 MMA costs a fixed
+// ~50 cycles of issue whatever its shape up to N = 64 (measured on GB300), so the
+// shapes are chosen for few MMAs per token, with the tokens on the M dimension:
+//   * a stage is 32 tokens (half a 64-token pool block) as nine 4 KB pieces, piece
+//     j = numbers 64 j .. 64 j + 63 of every token (K-major, 128-byte swizzle);
+//   * scores S^T = C . Q^T with M = 128 rows that stack four K-groups of the same 32
+//     tokens: rows 32 w .. 32 w + 31 are piece 4 G + w of the stage (consecutive
+//     pieces are 4 KB apart, the stride of 8-row groups times four), and the N = 64
+//     columns stack the 16 heads four times, column group w holding the queries'
+//     piece 4 G + w.  The diagonal blocks (rows 32 w.., columns 16 w..) are the
+//     products wanted; the others are computed and never read.  Two such MMAs (G =
+//     0, 1) per 16-number slice cover the eight latent pieces: 8 MMAs; the rotary
+//     piece takes 4 more (N = 16, rows 96-127 = piece 8 are the ones read);
 //   * output O^T[512 latent x 16 heads] += C^T . P^T: four M = 128 tiles of the
-//     latent numbers, A = two pieces of the stage read MN-major (a token's latent
-//     numbers are contiguous), B = the probabilities P^T[16 x 64] in shared
-//     memory -- 16 MMAs of K = 16 per block.
-// About 3,100 cycles of MMA issue per 72 KB block: below the ~3,400 cycles an SM's
-// share of the HBM bandwidth needs for it.
+//     latent numbers, A = two pieces read MN-major, B = P^T[16 x 32] -- 8 MMAs;
+//   so 20 MMAs per 32 tokens.
+//   The four K-group partial scores of a token sit in four lane quarters of tensor
+//   memory: the softmax warps add them through shared memory.
 //
-// Persistent, one CTA per SM (224 KB of shared memory, all 512 tensor-memory columns);
-// the units (head tile, sequence, block) are cut into one equal contiguous range
-// per CTA (mla_partition.cuh), a sequence cut by a range boundary leaving fp32
-// partials merged by paged_mla_merge_tcn.  192 threads:
+// Persistent, one CTA per SM (224 KB of shared memory, 512 tensor-memory columns);
+// the units (head tile, sequence, 64-token block) are cut into one equal contiguous
+// range per CTA (mla_partition.cuh), a sequence cut by a range boundary leaving fp16
+// partials merged by paged_mla_merge_tcn.  352 threads:
 //   * warp 4 walks the range's segments, hands each to the other roles through a
-//     4-slot ring, prefetches its queries into L2 and streams its 64-token blocks
-//     with nine TMA loads each (one per 128-byte piece, 128-byte swizzle) into 3
-//     stages of 72 KB;
-//   * warp 5 (one thread) issues the MMAs in a fixed order -- the scores of block g
-//     (two score buffers in tensor memory), then the output update of block g - 1 --
-//     so that the scores of a block run while the softmax of the one before does;
-//   * warp 0, lanes 0-15 (head h = lane h): the online softmax
-//     over each stage's 64 scores in registers, P^T row h written to shared memory
-//     (two buffers); the whole warp loads the next segment's queries into tensor
-//     memory (lanes 16-31 fetch the second half of each row and pass it down);
-//   * warps 0-3: each stage, a barrier at which warp 0 publishes whether the output
-//     is to be rescaled (the running max grew by more than 2^8 -- until then the
-//     older max stays the reference, exact since the final division uses the sum
-//     taken against the same reference) and whether the block has tokens past the
-//     cache (their value rows are zeroed: 0 * NaN must not reach the sums); at the
-//     end of a segment each warp normalises and writes its quarter of the latent
-//     rows.
-//   * tensor memory: the queries' latent numbers [0, 256), two score buffers [256,
-//     384), output tiles at 384, 416, 448, 480 (16 columns each); the queries' 64
-//     rotary numbers sit in shared memory.
-//   * paged_mla_decode_step (the STEP instantiation, 224 threads): warp 6 walks the
+//     4-slot ring, loads each segment's queries by TMA into one of two query buffers
+//     (as soon as the scores of the segment two back are done, so a new segment never
+//     waits for its queries) and streams the 32-token stages, nine TMA loads each,
+//     into a ring of 5 stages;
+//   * warp 5 (one thread) issues the score MMAs of each stage as soon as it has landed
+//     (two score buffers in tensor memory), warp 10 (one thread) the output update of
+//     each stage as soon as its probabilities are written, so neither waits behind the
+//     other;
+//   * warps 0-3 (the softmax): each reads its quarter's diagonal block of the scores,
+//     the four partials are added through shared memory in two rounds so that warp 0
+//     holds heads 0-7 and warp 1 heads 8-15 (lane = token); those two warps take the
+//     maxima with shuffles, decide a lazy rescale (the running max grew by more than
+//     2^8; until then the older max stays the reference, exact since the final
+//     division uses the sum taken against the same reference) and write the bf16
+//     probabilities P^T; all four zero the value rows of tokens past the cache (0 *
+//     NaN must not reach the sums) and apply a rescale to the output;
+//   * warps 6-9 (the epilogue): two output buffers in tensor memory alternate between
+//     segments, so a segment's output is normalised and written while the next one
+//     accumulates;
+//   * tensor memory: score buffers at columns 0 and 128 (64 columns + 16 for the
+//     rotary part), output buffers at 256 and 384 (four 16-column tiles 32 apart).
+//   * paged_mla_decode_step (the STEP instantiation, 384 threads): warp 11 walks the
 //     same partition and writes the new vector of each sequence whose last block lies in
 //     the range into that block; warp 4 waits on an mbarrier for those writes before it
 //     loads such a block.
@@ -66,186 +69,166 @@ namespace kvp {
 namespace {
 
 constexpr int TN_H = MLA_TCN_HEADS;             // heads per tile
-constexpr int TN_TOK = 64;                      // tokens per stage (one block)
-constexpr int TN_NSTAGE = 3;
-constexpr int TN_PIECE = TN_TOK * 128;          // one 64-number piece of 64 tokens
+constexpr int TN_BLK = MLA_TC_BLOCK;            // tokens per pool block (the partition's unit)
+constexpr int TN_TOK = 32;                      // tokens per stage
+constexpr int TN_NSTAGE = 5;
+constexpr int TN_PIECE = TN_TOK * 128;          // one 64-number piece of 32 tokens
 constexpr int TN_NPIECE = MLA_DK / 64;          // 9
-constexpr int TN_STAGE = TN_NPIECE * TN_PIECE;  // 73,728 bytes
-constexpr int TN_PBUF = TN_H * 128;             // P^T: a 128-byte row of 64 bf16 per head
-constexpr int TN_THREADS = 192;                 // warps 0-3 softmax / epilogue, 4 loads, 5 MMA
-constexpr int TN_THREADS_STEP = 224;            // + warp 6: the step's new vectors
-constexpr int TN_EPI = 128;                     // threads of warps 0-3
-// tensor memory: the queries' 512 latent numbers [0, 256), two score buffers [256, 320)
-// and [320, 384), output tiles at 384, 416, 448, 480 (16 columns each)
-constexpr uint32_t TN_Q = 0, TN_S = 256, TN_O = 384, TN_COLS = 512;
-// shared memory: the queries' 64 rotary numbers (16 rows of 128 bytes, K-major,
-// 128-byte swizzle) lead, the A operand of the rotary score MMAs, whose rows 16-127 fall
-// on the first stage (read, never used)
-constexpr int TN_QR = 2048;
-constexpr uint32_t IDESC_S = tc_idesc_bf16(128, TN_TOK, 0, 0);
+constexpr int TN_STAGE = TN_NPIECE * TN_PIECE;  // 36,864 bytes
+constexpr int TN_QPIECE = TN_H * 128;           // one 64-number piece of the 16 query rows
+constexpr int TN_QBUF = TN_NPIECE * TN_QPIECE;  // 18,432 bytes
+constexpr int TN_PBUF = TN_H * 128;             // P^T: 128-byte rows, stage parity b in bytes [64 b, 64 b + 64)
+constexpr int TN_XBUF = 12 * 32 * 16;           // the score partials exchanged between warps
+constexpr int TN_CTL = 1024;
+constexpr int TN_THREADS = 352;                 // warps 0-3 softmax, 4 loads, 5 and 10 MMA, 6-9 epilogue
+constexpr int TN_THREADS_STEP = 384;            // + warp 11: the step's new vectors
+constexpr int TN_SOFT = 128;                    // threads of warps 0-3
+constexpr int TN_NITEM = 4;
+constexpr int TN_ITEM_READERS = 10;             // the two MMA threads, warps 0-3, warps 6-9
+// shared memory: two query buffers, the stages, P^T, the exchange buffer, the control block
+constexpr int TN_OFF_Q = 0;
+constexpr int TN_OFF_ST = TN_OFF_Q + 2 * TN_QBUF;
+constexpr int TN_OFF_P = TN_OFF_ST + TN_NSTAGE * TN_STAGE;
+constexpr int TN_OFF_X = TN_OFF_P + TN_PBUF;
+constexpr int TN_OFF_CTL = TN_OFF_X + TN_XBUF;
+constexpr int TN_SMEM = 1024 + TN_OFF_CTL + TN_CTL;
+static_assert(TN_SMEM <= 227 * 1024, "one CTA per SM");
+static_assert(TN_OFF_ST % 1024 == 0 && TN_STAGE % 1024 == 0 && TN_OFF_P % 1024 == 0 && TN_QBUF % 1024 == 0,
+              "128-byte-swizzled operands start on 1 KB boundaries");
+// tensor memory
+constexpr uint32_t TN_S = 0, TN_S_STRIDE = 128, TN_ROPE = 64, TN_O = 256, TN_O_STRIDE = 128, TN_COLS = 512;
+static_assert(TN_S + TN_S_STRIDE + TN_ROPE + TN_H <= TN_O && TN_O + TN_O_STRIDE + 3 * 32 + TN_H <= TN_COLS,
+              "tensor-memory columns");
+static_assert(TN_H == 16 && TN_TOK == 32, "four 16-head column groups; a lane per token");
+constexpr uint32_t IDESC_S = tc_idesc_bf16(128, 4 * TN_H, 0, 0);
+constexpr uint32_t IDESC_R = tc_idesc_bf16(128, TN_H, 0, 0);
 constexpr uint32_t IDESC_O = tc_idesc_bf16(128, TN_H, 1, 0);
 constexpr float RESCALE_LOG2 = 8.f;
-constexpr int TN_CTL = 1024;
-constexpr int TN_SMEM = 1024 + TN_QR + TN_NSTAGE * TN_STAGE + 2 * TN_PBUF + TN_CTL;
-constexpr int TN_NITEM = 4;
-static_assert(TN_SMEM <= 227 * 1024, "one CTA per SM");
-static_assert(TN_Q + MLA_DV / 2 <= TN_S && TN_S + 2 * TN_TOK <= TN_O && TN_O + 3 * 32 + TN_H <= TN_COLS,
-              "tensor-memory columns");
-static_assert(TN_QR + TN_STAGE >= 128 * 128, "rows 16-127 of the rotary A operand stay in the stages");
-static_assert(TN_H == 16, "heads are lanes 0-15: warp 0 holds their scores");
 
 struct TnCtl {
     uint64_t kv_full[TN_NSTAGE];                    // the stage's nine pieces landed
     uint64_t kv_empty[TN_NSTAGE];                   // its output update is done
-    uint64_t q_full, o_full, o_free, mma_done;
-    uint64_t s_full[2], s_free[2];                  // the two score buffers
-    uint64_t p_full[2], p_free[2];
+    uint64_t q_full[2], q_free[2];                  // query buffers: landed / scores done
+    uint64_t s_full[2], s_free[2];                  // score buffers
+    uint64_t p_full[2], p_free[2];                  // P^T halves
+    uint64_t o_full[2], o_free[2];                  // output buffers: segment done / written
+    uint64_t ml_full[2];                            // a segment's (max, sum) per head written
     uint64_t item_full[TN_NITEM], item_empty[TN_NITEM];
+    uint64_t mma_done[2], step_done;
     uint32_t tmem_base;
-    int stage_blk[TN_NSTAGE];
     int abort_flag;
-    int flags[2];                                   // per stage (two in turn): 1 rescale the
-                                                    // output, 2 tokens past the cache; >> 2: valid tokens
+    int stage_blk[TN_NSTAGE];
+    uint32_t resc[2];                               // per stage parity, byte w: softmax warp w rescales
     MlaSegment items[TN_NITEM];
     float fac[TN_H];                                // per-head factors of a rescale
-    float lsum[TN_H], mref[TN_H];                   // per-head (sum, max) at a segment's end
-    uint64_t step_done;                             // paged_mla_decode_step: new vectors written
+    float lsum[2][TN_H], mref[2][TN_H];             // per output buffer: (sum, max) per head
 };
 static_assert(sizeof(TnCtl) <= TN_CTL, "control block");
 
-// One score MMA of S[128 x 64] = Q . C^T (rows 0-15 are the heads), slice ks of the 36
-// (16 numbers each): slices 0-31 are the latent numbers, A = the queries in tensor memory
-// (8 columns per slice), slices 32-35 the rotary key, A = the rotary queries in shared
-// memory; B = the matching piece of the stage, K-major, advanced 32 bytes per slice.
-__device__ __forceinline__ void score_mma(uint32_t d, uint32_t tbase, uint64_t st0, uint64_t qr0, int ks)
+// Stages of a segment: two per block, one for a sequence's last block when it holds at
+// most 32 tokens.
+__device__ __forceinline__ int seg_stages(const MlaSegment& it)
 {
-    const uint64_t b = st0 + static_cast<uint64_t>(((ks >> 2) * TN_PIECE + (ks & 3) * 32) >> 4);
-    if (ks < 32)
-        tc_mma_ts(d, tbase + TN_Q + ks * 8, b, IDESC_S, ks > 0);
-    else
-        tc_mma_ss(d, qr0 + static_cast<uint64_t>(((ks & 3) * 32) >> 4), b, IDESC_S, true);
+    const int extra = (it.blk0 + it.n) * TN_BLK - it.ctx;
+    return 2 * it.n - (extra >= TN_TOK ? 1 : 0);
 }
 
-// One output MMA: O^T[128 i .. 128 i + 127, 16 heads] += C^T . P^T over tokens 16 kk ..
-// 16 kk + 15 -- A = pieces 2i and 2i + 1 read MN-major (64-number atoms one piece
-// apart, 8-token groups 1 KB apart), B = P^T, K-major.
-__device__ __forceinline__ void output_mma(uint32_t tbase, uint32_t stage_addr, uint64_t p0, int i, int kk,
-                                           bool first)
+// Score MMAs of one stage into the score buffer at tensor-memory address d: 8 for the
+// latent pieces (two groups of four pieces stacked on M, 16 numbers per MMA) and 4 for
+// the rotary piece (rows 96-127 = piece 8 against the rotary queries, N = 16, at d + 64).
+// st_k, q_k: K-major descriptors of the stage and of the query buffer; every operand is
+// their start moved by a constant (descriptor addresses count 16-byte units), so the
+// issuing thread spends no time building descriptors.
+__device__ __forceinline__ void issue_scores(uint32_t d, uint64_t st_k, uint64_t q_k)
 {
-    const uint64_t a = tc_smem_desc(stage_addr + 2 * i * TN_PIECE, TN_PIECE, 1024) +
-                       static_cast<uint64_t>((kk * 2048) >> 4);
-    tc_mma_ss(tbase + TN_O + 32 * i, a, p0 + static_cast<uint64_t>((kk * 32) >> 4), IDESC_O,
-              !(first && kk == 0));
-}
-
-__device__ __forceinline__ void issue_scores(uint32_t tbase, uint32_t sbuf, uint32_t stage_addr, uint32_t qr_addr)
-{
-    const uint64_t st0 = tc_smem_desc(stage_addr, 16, 1024), qr0 = tc_smem_desc(qr_addr, 16, 1024);
 #pragma unroll
-    for (int ks = 0; ks < TN_NPIECE * 4; ++ks) score_mma(tbase + sbuf, tbase, st0, qr0, ks);
+    for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tc_mma_ss(d, st_k + ((grp * 4 * TN_PIECE + c * 32) >> 4), q_k + ((grp * 4 * TN_QPIECE + c * 32) >> 4),
+                      IDESC_S, (grp | c) != 0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        tc_mma_ss(d + TN_ROPE, st_k + ((5 * TN_PIECE + c * 32) >> 4), q_k + ((8 * TN_QPIECE + c * 32) >> 4), IDESC_R,
+                  c != 0);
 }
 
-__device__ __forceinline__ void issue_output(uint32_t tbase, uint32_t stage_addr, uint32_t p_addr, bool first)
+// Output MMAs of one stage: O^T[128 i .. 128 i + 127, 16 heads] += C^T . P^T over tokens
+// 16 kk .. 16 kk + 15 -- A = pieces 2i and 2i + 1 read MN-major (st_mn: the stage's
+// descriptor with 64-number atoms one piece apart, 8-token groups 1 KB apart), B = the
+// stage's half of P^T, K-major (p_k).
+__device__ __forceinline__ void issue_output(uint32_t obase, uint64_t st_mn, uint64_t p_k, bool first)
 {
-    const uint64_t p0 = tc_smem_desc(p_addr, 16, 1024);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int kk = 0; kk < TN_TOK / 16; ++kk) output_mma(tbase, stage_addr, p0, i, kk, first);
+        for (int kk = 0; kk < TN_TOK / 16; ++kk)
+            tc_mma_ss(obase + 32 * i, st_mn + ((2 * i * TN_PIECE + kk * 2048) >> 4), p_k + ((kk * 32) >> 4), IDESC_O,
+                      !(first && kk == 0));
 }
 
-// The MMA thread: the output update of stage go (segment ko; first / last: its place in
-// the segment) once its probabilities are written -- and, for a segment's first stage,
-// once the previous segment's output has been read.  Frees the stage's slot and the
-// probabilities' buffer; after a segment's last stage, hands the output to the epilogue.
-__device__ __forceinline__ bool mma_output_stage(TnCtl* ctl, uint32_t tbase, uint8_t* stages, uint8_t* pbuf, int go,
-                                                 int ko, bool first, bool last)
+// The MMA thread: the output update of stage gp (segment kp, slot stp; first / last: its
+// place in the segment) once its probabilities are written -- and, for a segment's first
+// stage, once the epilogue has read the output buffer the segment reuses.  Frees the
+// stage's slot and the probabilities' half; after a segment's last stage, hands the
+// output buffer to the epilogue.
+__device__ __forceinline__ bool mma_output_stage(TnCtl* ctl, uint32_t tbase, uint64_t st_mn0, uint64_t p_k0,
+                                                 int gp, int kp, int stp, bool first, bool last)
 {
-    bool ok = mbar_wait_bounded(smem_u32(&ctl->p_full[go & 1]), static_cast<uint32_t>(go >> 1) & 1u);
-    if (ok && first && ko >= 1) ok = mbar_wait_bounded(smem_u32(&ctl->o_free), static_cast<uint32_t>(ko - 1) & 1u);
+    bool ok = mbar_wait_bounded(smem_u32(&ctl->p_full[gp & 1]), static_cast<uint32_t>(gp >> 1) & 1u);
+    if (ok && first && kp >= 2)
+        ok = mbar_wait_bounded(smem_u32(&ctl->o_free[kp & 1]), static_cast<uint32_t>((kp >> 1) - 1) & 1u);
     if (!ok) return false;
     tc_fence_after();
-    issue_output(tbase, smem_u32(stages + (go % TN_NSTAGE) * TN_STAGE), smem_u32(pbuf + (go & 1) * TN_PBUF), first);
-    tc_commit(smem_u32(&ctl->kv_empty[go % TN_NSTAGE]));
-    tc_commit(smem_u32(&ctl->p_free[go & 1]));
-    if (last) tc_commit(smem_u32(&ctl->o_full));
+    issue_output(tbase + TN_O + TN_O_STRIDE * (kp & 1), st_mn0 + static_cast<uint64_t>((stp * TN_STAGE) >> 4),
+                 p_k0 + static_cast<uint64_t>((64 * (gp & 1)) >> 4), first);
+    tc_commit(smem_u32(&ctl->kv_empty[stp]));
+    tc_commit(smem_u32(&ctl->p_free[gp & 1]));
+    if (last) tc_commit(smem_u32(&ctl->o_full[kp & 1]));
     return true;
 }
 
-// Warp 0: the queries of heads ht * 16 + 0..15 of sequence b -- the 512 latent numbers
-// into tensor-memory lanes 0-15, columns [0, 256) (128-byte chunk j of a row -> columns
-// 32 j .. 32 j + 31), the 64 rotary numbers into the shared-memory rows at qr (row h,
-// 16-byte chunk c at (c ^ (h & 7))).  Lane h fetches chunks 0-4 of head h, lane h + 16
-// chunks 5-8 (5-7 passed down by shuffles; lanes 16-31 store into tensor-memory lanes
-// 16-31, which no result is read from), in two rounds of at most three chunks per lane
-// (one round would spill registers).  Rows past q_heads are zero.
-__device__ __forceinline__ void load_queries(const MlaParams& p, int b, int ht, uint32_t lrow, uint32_t qr,
-                                             int lane)
+// Four floats to / from shared memory (shared-space addresses).
+__device__ __forceinline__ void sts_f4(uint32_t addr, const float* v)
 {
-    const int h = lane & 15, hi = lane >> 4;
-    const int head = ht * TN_H + h;
-    const bool valid = head < p.q_heads;
-    const uint4* row = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.q_heads + (valid ? head : 0)) * MLA_DK);
-    // round 0: lanes 0-15 chunks 0-2, lanes 16-31 chunks 5-7; round 1: chunks 3-4 and 8
-#pragma unroll
-    for (int round = 0; round < 2; ++round) {
-        const int nlo = round == 0 ? 3 : 2;         // chunks of lanes 0-15 this round
-        const int nhi = round == 0 ? 3 : 1;         // chunks of lanes 16-31
-        const int c_lo = round == 0 ? 0 : 3, c_hi = round == 0 ? 5 : 8;
-        uint32_t r[3][32];
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                if (valid && j < (hi ? nhi : nlo)) x = __ldg(row + ((hi ? c_hi : c_lo) + j) * 8 + v);
-                r[j][4 * v] = x.x;
-                r[j][4 * v + 1] = x.y;
-                r[j][4 * v + 2] = x.z;
-                r[j][4 * v + 3] = x.w;
-            }
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-            if (j < nlo) tc_st32(lrow + TN_Q + 32 * (c_lo + j), r[j]);
-        if (round == 0) {
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                uint32_t x[32];
-#pragma unroll
-                for (int v = 0; v < 32; ++v) x[v] = __shfl_down_sync(FULL_MASK, r[j][v], 16);
-                tc_st32(lrow + TN_Q + 32 * (c_hi + j), x);
-            }
-        } else if (hi) {
-            // the rotary chunk: lane h + 16 writes row h
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(qr + h * 128 + ((c ^ (h & 7)) << 4)),
-                             "r"(r[0][4 * c]), "r"(r[0][4 * c + 1]), "r"(r[0][4 * c + 2]), "r"(r[0][4 * c + 3])
-                             : "memory");
-        }
-    }
-    fence_proxy_async_smem();
-    tc_wait_st();
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void lds_add_f4(uint32_t addr, float* v)
+{
+    float a, b, c, d;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr) : "memory");
+    v[0] += a;
+    v[1] += b;
+    v[2] += c;
+    v[3] += d;
 }
 
 }  // namespace
 
-// STEP: paged_mla_decode_step (p.kv_new set), whose new vectors a seventh warp writes.
+// STEP: paged_mla_decode_step (p.kv_new set), whose new vectors a twelfth warp writes.
 template <bool STEP>
 __global__ void __launch_bounds__(STEP ? TN_THREADS_STEP : TN_THREADS, 1)
-paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
+paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const __grid_constant__ CUtensorMap tmq,
+                     const MlaParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* stages = smem + TN_QR;
-    uint8_t* pbuf = stages + TN_NSTAGE * TN_STAGE;
-    TnCtl* ctl = reinterpret_cast<TnCtl*>(pbuf + 2 * TN_PBUF);
+    uint8_t* qbufs = smem + TN_OFF_Q;
+    uint8_t* stages = smem + TN_OFF_ST;
+    uint8_t* pbuf = smem + TN_OFF_P;
+    uint8_t* xbuf = smem + TN_OFF_X;
+    TnCtl* ctl = reinterpret_cast<TnCtl*>(smem + TN_OFF_CTL);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     volatile int* abort_flag = &ctl->abort_flag;
+    // query rows per TMA box: 16, or all heads when there are fewer (the other rows of
+    // the buffers are zeroed once here)
+    const int q_rows = min(TN_H, p.q_heads);
 
     if (tid == 0) {
         for (int i = 0; i < TN_NSTAGE; ++i) {
@@ -254,21 +237,29 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         }
         for (int i = 0; i < TN_NITEM; ++i) {
             mbar_init(smem_u32(&ctl->item_full[i]), 1);
-            mbar_init(smem_u32(&ctl->item_empty[i]), 5);   // the MMA thread + warps 0-3
+            mbar_init(smem_u32(&ctl->item_empty[i]), TN_ITEM_READERS);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&ctl->p_full[i]), 1);
-            mbar_init(smem_u32(&ctl->p_free[i]), 1);
+            mbar_init(smem_u32(&ctl->q_full[i]), 1);
+            mbar_init(smem_u32(&ctl->q_free[i]), 1);
             mbar_init(smem_u32(&ctl->s_full[i]), 1);
-            mbar_init(smem_u32(&ctl->s_free[i]), 1);
+            mbar_init(smem_u32(&ctl->s_free[i]), 4);
+            mbar_init(smem_u32(&ctl->p_full[i]), 4);
+            mbar_init(smem_u32(&ctl->p_free[i]), 1);
+            mbar_init(smem_u32(&ctl->o_full[i]), 1);
+            mbar_init(smem_u32(&ctl->o_free[i]), 4);
+            mbar_init(smem_u32(&ctl->ml_full[i]), 4);
         }
-        mbar_init(smem_u32(&ctl->q_full), 1);
-        mbar_init(smem_u32(&ctl->o_full), 1);
-        mbar_init(smem_u32(&ctl->o_free), 4);
-        mbar_init(smem_u32(&ctl->mma_done), 1);
-        mbar_init(smem_u32(&ctl->step_done), 32);   // the lanes of warp 6 (STEP)
+        mbar_init(smem_u32(&ctl->mma_done[0]), 1);
+        mbar_init(smem_u32(&ctl->mma_done[1]), 1);
+        mbar_init(smem_u32(&ctl->step_done), 32);   // the lanes of warp 11 (STEP)
         ctl->abort_flag = 0;
         fence_mbar_init();
+    }
+    if (q_rows < TN_H) {
+        for (int i = tid; i < 2 * TN_QBUF / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(qbufs)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
     }
     if (warp == 5) tc_alloc(smem_u32(&ctl->tmem_base), TN_COLS);
     grid_dependency_wait();                     // inputs of the preceding kernel are ready
@@ -279,22 +270,20 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
 
     if (warp == 4) {
         // ------------------------------------------------------------ segments and loads
-        MlaPartition<TN_TOK, MLA_SEG_PAD_NARROW> part;
+        MlaPartition<TN_BLK, MLA_SEG_PAD_NARROW> part;
         part.init(p, p.head_tiles, lane);
         if (lane == 0) {
             prefetch_tensormap(&tmp);
+            prefetch_tensormap(&tmq);
             int k = 0;                              // segments handed on
+            int nq = 0;                             // segments whose queries were loaded
             int g = 0;                              // stages issued (all segments)
             bool ok = true;
-            bool step_written = false;              // paged_mla_decode_step: waited for lanes 1-31
+            bool step_written = false;              // paged_mla_decode_step: waited for warp 11
+            const uint32_t qbytes = static_cast<uint32_t>(TN_NPIECE * q_rows * 128);
             for (;;) {
                 const MlaSegment it = *abort_flag ? MlaSegment{0, 0, 0, -1, 0, 0, 0} : part.next();
                 const bool last = it.n < 0;
-                if (!last) {
-                    const int nhq = min(TN_H, p.q_heads - it.outer * TN_H);
-                    prefetch_l2_bulk(p.q + (static_cast<size_t>(it.b) * p.q_heads + it.outer * TN_H) * MLA_DK,
-                                     static_cast<uint32_t>(nhq) * MLA_DK * 2);
-                }
                 const int slot = k % TN_NITEM;
                 if (!mbar_wait_bounded(smem_u32(&ctl->item_empty[slot]),
                                        (static_cast<uint32_t>(k / TN_NITEM) & 1u) ^ 1u)) {
@@ -303,26 +292,43 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 }
                 ctl->items[slot] = it;
                 mbar_arrive(smem_u32(&ctl->item_full[slot]));
-                ++k;
                 if (last) break;
+                // the queries into buffer k & 1, once the scores of segment k - 2 are done
+                if (k >= 2 && !mbar_wait_bounded(smem_u32(&ctl->q_free[k & 1]),
+                                                 static_cast<uint32_t>((k >> 1) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    const uint32_t qb = smem_u32(qbufs + (k & 1) * TN_QBUF), fb = smem_u32(&ctl->q_full[k & 1]);
+                    mbar_arrive_expect_tx(fb, qbytes);
+                    for (int j = 0; j < TN_NPIECE; ++j)
+                        tma_load_3d(qb + j * TN_QPIECE, &tmq, 64 * j, it.outer * TN_H, it.b, fb);
+                    nq = k + 1;
+                }
+                ++k;
+                const int ns = seg_stages(it);
                 const int32_t* trow = p.tables + static_cast<size_t>(it.b) * p.max_blocks + it.blk0;
-                int next_blk = __ldg(trow);         // block id read one stage ahead
-                // paged_mla_decode_step: the segment's stage whose block holds the new vector
-                const int step_s = STEP ? mla_step_block(p, it.b, TN_TOK) - it.blk0 : -1;
-                for (int s = 0; s < it.n; ++s, ++g) {
+                int next_bid = __ldg(trow);         // block id read one block ahead
+                int bid = -1;
+                // paged_mla_decode_step: the segment's block that holds the new vector
+                const int step_j = STEP ? mla_step_block(p, it.b, TN_BLK) - it.blk0 : -1;
+                for (int s = 0; s < ns; ++s, ++g) {
                     const int st = g % TN_NSTAGE;
-                    int bid = next_blk;
-                    if (s + 1 < it.n) next_blk = __ldg(trow + s + 1);
-                    if (bid < 0 || bid >= p.num_blocks) {
-                        atomicOr(p.err, KV_DEVERR_BLOCK_ID);
-                        bid = -1;
-                    }
-                    if (STEP && s == step_s && bid >= 0 && !step_written) {   // warp 6 wrote it?
-                        if (!mbar_wait_bounded(smem_u32(&ctl->step_done), 0u)) {
-                            ok = false;
-                            break;
+                    if ((s & 1) == 0) {
+                        bid = next_bid;
+                        if ((s >> 1) + 1 < it.n) next_bid = __ldg(trow + (s >> 1) + 1);
+                        if (bid < 0 || bid >= p.num_blocks) {
+                            atomicOr(p.err, KV_DEVERR_BLOCK_ID);
+                            bid = -1;
                         }
-                        step_written = true;
+                        if (STEP && (s >> 1) == step_j && bid >= 0 && !step_written) {   // warp 11 wrote it?
+                            if (!mbar_wait_bounded(smem_u32(&ctl->step_done), 0u)) {
+                                ok = false;
+                                break;
+                            }
+                            step_written = true;
+                        }
                     }
                     if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty[st]),
                                            (static_cast<uint32_t>(g / TN_NSTAGE) & 1u) ^ 1u) ||
@@ -336,7 +342,7 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         const uint32_t dst = smem_u32(stages + st * TN_STAGE);
                         mbar_arrive_expect_tx(fb, TN_STAGE);
                         for (int j = 0; j < TN_NPIECE; ++j)
-                            tma_load_5d(dst + j * TN_PIECE, &tmp, 0, j, 0, 0, bid, fb);
+                            tma_load_5d(dst + j * TN_PIECE, &tmp, 0, j, 0, TN_TOK * (s & 1), bid, fb);
                     } else {
                         mbar_arrive(fb);
                     }
@@ -352,291 +358,349 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 if (!mbar_wait_bounded(smem_u32(&ctl->kv_full[j % TN_NSTAGE]),
                                        static_cast<uint32_t>(j / TN_NSTAGE) & 1u))
                     break;
+            for (int j = max(0, nq - 2); j < nq; ++j)
+                if (!mbar_wait_bounded(smem_u32(&ctl->q_full[j & 1]), static_cast<uint32_t>(j >> 1) & 1u))
+                    break;
         }
         grid_dependents_launch();
-    } else if (STEP && warp == 6) {
+    } else if (STEP && warp == 11) {
         // ------------------------------------------------------------ the step's new vectors
         // The same partition, walked beside the producer: every block of the range that holds
         // a sequence's new vector gets it before the producer loads that block.
-        MlaPartition<TN_TOK, MLA_SEG_PAD_NARROW> part;
+        MlaPartition<TN_BLK, MLA_SEG_PAD_NARROW> part;
         part.init(p, p.head_tiles, lane, false);
         part.write_step_rows(smem_u32(&ctl->step_done), lane, 32);
-    } else if (warp == 5) {
+    } else if (warp == 5 || warp == 10) {
         // ------------------------------------------------------------ MMA issue
+        // Two issuing threads, so that neither kind of MMA waits behind the other: warp 5
+        // issues the scores of each stage as soon as it has landed (and its score buffer is
+        // free), warp 10 the output update of each stage as soon as its probabilities are
+        // written.  They touch different tensor memory; the update of stage g follows the
+        // scores of stage g through the softmax's barrier.
         if (lane == 0) {
-            // A fixed order: the scores of stage g, then the output update of stage g - 1,
-            // so that the scores of the next block run while the softmax of the last one
-            // does, and each wait blocks (try_wait) rather than polls.  At a segment
-            // boundary the last output update of the old segment comes first.
-            const uint32_t qr = smem_u32(smem);
+            const bool scores = warp == 5;
             bool ok = true;
-            int g = 0;                              // stages scored (all segments)
-            int pk = -1, pfirst = 0, plast = 0;     // the stage whose output update is due, its
-                                                    // segment, first / last in the segment
+            // descriptors of the first stage (K-major; MN-major with atoms a piece apart), of
+            // the query buffers and of P^T; the others are these moved by a constant
+            const uint64_t st_k0 = tc_smem_desc(smem_u32(stages), 16, 1024);
+            const uint64_t st_mn0 = tc_smem_desc(smem_u32(stages), TN_PIECE, 1024);
+            const uint64_t q_k0 = tc_smem_desc(smem_u32(qbufs), 16, 1024);
+            const uint64_t p_k0 = tc_smem_desc(smem_u32(pbuf), 16, 1024);
+            int g = 0;                              // stages (all segments)
             for (int k = 0; ok; ++k) {
                 const int slot = k % TN_NITEM;
                 ok = mbar_wait_bounded(smem_u32(&ctl->item_full[slot]), static_cast<uint32_t>(k / TN_NITEM) & 1u);
                 if (!ok) break;
-                const int n = ctl->items[slot].n;
+                const MlaSegment it = ctl->items[slot];
                 mbar_arrive(smem_u32(&ctl->item_empty[slot]));
-                if (n < 0) break;
-                for (int s = 0; ok && s < n; ++s, ++g) {
+                if (it.n < 0) break;
+                const int ns = seg_stages(it);
+                const uint64_t q_k = q_k0 + static_cast<uint64_t>(((k & 1) * TN_QBUF) >> 4);
+                for (int s = 0; ok && s < ns; ++s, ++g) {
                     const int st = g % TN_NSTAGE;
-                    if (s == 0 && pk >= 0) {
-                        // the previous segment's last output update goes first: it does not
-                        // wait for this segment's queries, and its epilogue can then run
-                        // while they load
-                        ok = mma_output_stage(ctl, tbase, stages, pbuf, g - 1, pk, pfirst, plast);
-                        pk = -1;
-                        if (!ok) break;
+                    if (!scores) {
+                        ok = mma_output_stage(ctl, tbase, st_mn0, p_k0, g, k, st, s == 0, s == ns - 1);
+                        if (ok && *abort_flag) ok = false;
+                        continue;
                     }
                     ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(g / TN_NSTAGE) & 1u);
                     if (ok && g >= 2)
                         ok = mbar_wait_bounded(smem_u32(&ctl->s_free[g & 1]), static_cast<uint32_t>((g - 2) >> 1) & 1u);
-                    if (ok && s == 0) ok = mbar_wait_bounded(smem_u32(&ctl->q_full), static_cast<uint32_t>(k) & 1u);
+                    if (ok && s == 0)
+                        ok = mbar_wait_bounded(smem_u32(&ctl->q_full[k & 1]), static_cast<uint32_t>(k >> 1) & 1u);
                     if (!ok || *abort_flag) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_scores(tbase, TN_S + TN_TOK * (g & 1), smem_u32(stages + st * TN_STAGE), qr);
+                    issue_scores(tbase + TN_S + TN_S_STRIDE * (g & 1), st_k0 + static_cast<uint64_t>((st * TN_STAGE) >> 4), q_k);
                     tc_commit(smem_u32(&ctl->s_full[g & 1]));
-                    if (pk >= 0) ok = mma_output_stage(ctl, tbase, stages, pbuf, g - 1, pk, pfirst, plast);
-                    pk = k;
-                    pfirst = s == 0;
-                    plast = s == n - 1;
+                    if (s == ns - 1) tc_commit(smem_u32(&ctl->q_free[k & 1]));
                 }
             }
-            if (ok && pk >= 0) ok = mma_output_stage(ctl, tbase, stages, pbuf, g - 1, pk, pfirst, plast);
             if (!ok) {
                 atomicOr(p.err, KV_DEVERR_TIMEOUT);
                 ctl->abort_flag = 1;
             }
             // every MMA issued must be complete before the tensor memory is freed
-            tc_commit(smem_u32(&ctl->mma_done));
-            mbar_wait_bounded(smem_u32(&ctl->mma_done), 0);
+            const uint32_t done = smem_u32(&ctl->mma_done[scores ? 0 : 1]);
+            tc_commit(done);
+            mbar_wait_bounded(done, 0);
         }
-    } else {
-        // ------------------------------------------------------------ softmax / epilogue
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax
         const uint32_t lrow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-        const int h = lane & 15;                    // warp 0: the head of this lane
-        const bool soft = warp == 0 && lane < TN_H;
         const float sl2 = p.scale_log2;
         bool failed = false;
         int g = 0;                                  // stages processed (all segments)
-        MlaSegment item{};
-        {
-            const bool ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->item_full[0]), 0));
-            item = ctl->items[0];
-            failed = !ok;
-        }
-        if (warp == 0 && !failed && item.n >= 0) {
-            load_queries(p, item.b, item.outer, lrow, smem_u32(smem), lane);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->q_full));
-        }
-        // every warp of the four reaches this barrier once per segment, failed or not: it is
-        // the one place they leave the loop together
         for (int k = 0;; ++k) {
             const int slot = k % TN_NITEM;
-            if (k > 0 && !failed) {
-                const bool ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->item_full[slot]),
-                                                         static_cast<uint32_t>(k / TN_NITEM) & 1u));
-                item = ctl->items[slot];
-                if (!ok) failed = true;
-            }
-            __syncwarp();
-            if (lane == 0 && !failed) mbar_arrive(smem_u32(&ctl->item_empty[slot]));
-            if (named_barrier_or(1, TN_EPI, failed || item.n < 0 || *abort_flag != 0)) {
-                failed = failed || *abort_flag != 0;
+            // warp 0 alone polls the barriers of the four; the others wait at the named
+            // barrier (every warp reaches it once per segment and once per stage, failed or
+            // not: it is the one place they leave the loop together)
+            bool bad = failed;
+            if (warp == 0 && !bad)
+                bad = !all_ok(mbar_wait_bounded(smem_u32(&ctl->item_full[slot]), static_cast<uint32_t>(k / TN_NITEM) & 1u));
+            if (named_barrier_or(1, TN_SOFT, bad || *abort_flag != 0)) {
+                failed = true;
                 break;
             }
-            const int b = item.b, ht = item.outer, split = item.split, n = item.n, ctx = item.ctx;
-            const int blk0 = item.blk0, nsplit = item.nsplit;
-            const int nh = min(TN_H, p.q_heads - ht * TN_H);
-            const size_t row0 = static_cast<size_t>(b) * p.q_heads + ht * TN_H;
-            float m_ref = -INFINITY, l = 0.f;
-            for (int s = 0; s < n; ++s) {
+            const MlaSegment item = ctl->items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->item_empty[slot]));
+            if (item.n < 0) break;
+            const int ns = seg_stages(item);
+            // warp v: heads 4 v + i, this lane's token of each stage
+            float m_ref[4], l[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                m_ref[i] = -INFINITY;
+                l[i] = 0.f;
+            }
+            for (int s = 0; s < ns; ++s) {
                 const int gs = g + s;
                 const int st = gs % TN_NSTAGE;
-                float sv[64];
-                int nvalid = 0;
-                bool ok = true;
-                if (warp == 0) {
-                    ok = mbar_wait_bounded(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(gs / TN_NSTAGE) & 1u);
-                    if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->s_full[gs & 1]), static_cast<uint32_t>(gs >> 1) & 1u);
-                    ok = all_ok(ok);
-                    const int blk = ok ? ctl->stage_blk[st] : -1;
-                    nvalid = blk < 0 ? 0 : min(TN_TOK, ctx - (blk0 + s) * TN_TOK);
-                    if (ok) {
-                        tc_fence_after();
-                        uint32_t r[32];
-                        tc_ld32(lrow + TN_S + TN_TOK * (gs & 1), r);
+                // each warp checks the stage's barriers itself (the scores are issued well
+                // ahead, so these are normally complete already); a failure is passed on at
+                // the stage's last barrier
+                bool ok = !failed;
+                if (ok) ok = mbar_wait_spin(smem_u32(&ctl->kv_full[st]), static_cast<uint32_t>(gs / TN_NSTAGE) & 1u);
+                if (ok) ok = mbar_wait_spin(smem_u32(&ctl->s_full[gs & 1]), static_cast<uint32_t>(gs >> 1) & 1u);
+                ok = all_ok(ok);
+                if (!ok) failed = true;
+                const int blk = ok ? ctl->stage_blk[st] : -1;
+                const int nvalid = blk < 0 ? 0 : max(0, min(TN_TOK, item.ctx - item.blk0 * TN_BLK - TN_TOK * s));
+                // this warp's K-group partial of token `lane`, 16 heads
+                float sc[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sc[j] = 0.f;
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t sb = lrow + TN_S + TN_S_STRIDE * (gs & 1);
+                    uint32_t r[16];
+                    tc_ld16(sb + 16 * warp, r);
+                    if (warp == 3) {
+                        uint32_t r2[16];
+                        tc_ld16(sb + TN_ROPE, r2);
                         tc_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(r[j]);
-                        tc_ld32(lrow + TN_S + TN_TOK * (gs & 1) + 32, r);
+                        for (int j = 0; j < 16; ++j) sc[j] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
+                    } else {
                         tc_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(r[j]);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[gs & 1]));
+                        for (int j = 0; j < 16; ++j) sc[j] = __uint_as_float(r[j]);
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->s_free[gs & 1]));
                     if (nvalid < TN_TOK) {
-#pragma unroll
-                        for (int j = 0; j < 64; ++j)
-                            if (j >= nvalid) sv[j] = -INFINITY;   // not cached (may be NaN)
+                        // value rows of tokens past the cache (or of a skipped block) are
+                        // zeroed; the scores, which read them too, are complete
+                        uint8_t* sp = stages + st * TN_STAGE;
+                        for (int i = tid; i < (TN_TOK - nvalid) * 64; i += TN_SOFT) {
+                            const int row = nvalid + (i >> 6);
+                            const int pc = (i >> 3) & 7;
+                            const int ch = i & 7;
+                            *reinterpret_cast<uint4*>(sp + pc * TN_PIECE + row * 128 + (ch << 4)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
                     }
-                    float mx = sv[0];
-#pragma unroll
-                    for (int j = 1; j < 64; ++j) mx = fmaxf(mx, sv[j]);
-                    const float m_new = fmaxf(m_ref, mx * sl2);
-                    float f = 1.f;
-                    if (m_ref == -INFINITY) {
-                        m_ref = m_new;              // nothing accumulated yet
-                    } else if (m_new > m_ref + RESCALE_LOG2) {
-                        f = fast_exp2(m_ref - m_new);
-                        l *= f;
-                        m_ref = m_new;
-                    }
-                    const bool any = __any_sync(FULL_MASK, soft && f != 1.f);
-                    if (lane < TN_H) ctl->fac[h] = f;
-                    if (lane == 0)
-                        ctl->flags[gs & 1] = (any ? 1 : 0) | (nvalid < TN_TOK ? 2 : 0) | (max(0, nvalid) << 2);
                 }
-                // warp 0 publishes the stage's flags; a failure anywhere ends the loop here
-                if (named_barrier_or(1, TN_EPI, failed || !ok || *abort_flag != 0)) {
+                // the four partials added in one round through shared memory: warp w hands the
+                // partials of heads 4 v .. 4 v + 3 to warp v (slot 3 v + the rank of w among the
+                // other three), then each warp adds the three it received to its own, in the
+                // order of the sending warps
+                const uint32_t xb = smem_u32(xbuf) + lane * 16;
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (v != warp) sts_f4(xb + (3 * v + (warp < v ? warp : warp - 1)) * 512, sc + 4 * v);
+                named_barrier_sync(1, TN_SOFT);
+                float s4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    s4[i] = warp == 0 ? sc[i] : warp == 1 ? sc[4 + i] : warp == 2 ? sc[8 + i] : sc[12 + i];
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    if (w != warp) lds_add_f4(xb + (3 * warp + (w < warp ? w : w - 1)) * 512, s4);
+                if (lane >= nvalid) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) s4[i] = -INFINITY;   // not cached (may be NaN)
+                }
+                // The stage's maxima are needed only where some score exceeds its head's
+                // reference by more than 2^8 (or no reference is set yet): a vote decides,
+                // the maxima are reduced only then.
+                bool over = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) over = over || s4[i] * sl2 > m_ref[i] + RESCALE_LOG2;
+                bool resc = false;
+                if (__any_sync(FULL_MASK, over)) {
+                    float mx[4], fi[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx[i] = s4[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(FULL_MASK, mx[i], o));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float m_new = fmaxf(m_ref[i], mx[i] * sl2);
+                        fi[i] = 1.f;
+                        if (m_ref[i] == -INFINITY) {
+                            m_ref[i] = m_new;       // nothing accumulated yet
+                        } else if (m_new > m_ref[i] + RESCALE_LOG2) {
+                            fi[i] = fast_exp2(m_ref[i] - m_new);
+                            l[i] *= fi[i];
+                            m_ref[i] = m_new;
+                            resc = true;
+                        }
+                    }
+                    // the factors of this warp's heads (1 where nothing changed), read by all
+                    // four when this warp's flag is set
+                    if (resc && lane < 4)
+                        ctl->fac[4 * warp + lane] = lane == 0 ? fi[0] : lane == 1 ? fi[1] : lane == 2 ? fi[2] : fi[3];
+                }
+                if (lane == 0) reinterpret_cast<volatile uint8_t*>(&ctl->resc[gs & 1])[warp] = resc ? 1 : 0;
+                // a failure anywhere ends the loop here; past it, every warp knows which heads'
+                // output columns are to be rescaled
+                if (named_barrier_or(1, TN_SOFT, failed || *abort_flag != 0)) {
                     failed = true;
                     break;
                 }
-                const int flags = ctl->flags[gs & 1];
-                if (flags & 1) {
-                    // scale the output columns by their heads' factors once the updates of
-                    // the earlier stages are done
+                const uint32_t rw = *reinterpret_cast<volatile uint32_t*>(&ctl->resc[gs & 1]);
+                const int rs = static_cast<int>((rw & 1u) | ((rw >> 7) & 2u) | ((rw >> 14) & 4u) | ((rw >> 21) & 8u));
+                if (rs != 0) {
+                    // scale the output columns of the rescaled heads by their factors once the
+                    // updates of the earlier stages are done (a segment's first stage never
+                    // rescales)
                     const bool w = all_ok(mbar_wait_bounded(smem_u32(&ctl->p_free[(gs - 1) & 1]),
                                                             static_cast<uint32_t>((gs - 1) >> 1) & 1u));
-                    if (!w) failed = true;
-                    if (w) {
-                        tc_fence_after();
-                        float fh[TN_H];
-#pragma unroll
-                        for (int j = 0; j < TN_H; ++j) fh[j] = ctl->fac[j];
-#pragma unroll 1
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t r[32];
-                            tc_ld32(lrow + TN_O + 32 * i, r);
-                            tc_wait_ld();
-                            uint32_t x[16];
-#pragma unroll
-                            for (int j = 0; j < TN_H; ++j) x[j] = __float_as_uint(__uint_as_float(r[j]) * fh[j]);
-                            tc_st16(lrow + TN_O + 32 * i, x);
-                        }
-                        tc_wait_st();
-                        tc_fence_before();
-                    }
-                }
-                if (flags & 2) {
-                    // value rows of tokens past the cache (or of a skipped block) are zeroed
-                    // (the stage's scores, which read them too, are complete)
-                    const int v0 = max(0, flags >> 2);
-                    uint8_t* sp = stages + st * TN_STAGE;
-                    for (int i = tid; i < (TN_TOK - v0) * 64; i += TN_EPI) {
-                        const int row = v0 + (i >> 6);
-                        const int pc = (i >> 3) & 7;
-                        const int ch = i & 7;
-                        *reinterpret_cast<uint4*>(sp + pc * TN_PIECE + row * 128 + (ch << 4)) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                }
-                if (flags != 0 && named_barrier_or(1, TN_EPI, failed)) {
-                    failed = true;
-                    break;
-                }
-                if (warp == 0) {
-                    // probabilities (bf16) of this thread's head: P^T row h, 128-byte swizzle
-                    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                    uint32_t pk[32];
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float p0 = fast_exp2(fmaf(sv[2 * j], sl2, -m_use));
-                        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], sl2, -m_use));
-                        ls[j & 3] += p0 + p1;
-                        pk[j] = pack_bf16x2(p0, p1);
-                    }
-                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    bool w = true;
-                    if (gs >= 2)
-                        w = mbar_wait_bounded(smem_u32(&ctl->p_free[gs & 1]), static_cast<uint32_t>((gs - 2) >> 1) & 1u);
-                    w = all_ok(w);
                     if (!w) {
                         failed = true;
                     } else {
-                        if (lane < TN_H) {
-                            const uint32_t row = smem_u32(pbuf + (gs & 1) * TN_PBUF) + h * 128;
+                        tc_fence_after();
+                        float fh[TN_H];
 #pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ (h & 7)) << 4)),
-                                             "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                             : "memory");
+                        for (int j = 0; j < TN_H; ++j) fh[j] = (rs >> (j >> 2)) & 1 ? ctl->fac[j] : 1.f;
+                        const uint32_t ob = lrow + TN_O + TN_O_STRIDE * (k & 1);
+#pragma unroll 1
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t r[16];
+                            tc_ld16(ob + 32 * i, r);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < TN_H; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * fh[j]);
+                            tc_st16(ob + 32 * i, r);
+                        }
+                        tc_wait_st();
+                    }
+                }
+                if (!failed) {
+                    // probabilities (bf16) of this lane's token: P^T rows 4 warp + i, the
+                    // stage's 64-byte half of each 128-byte swizzled row
+                    const bool w = gs < 2 || all_ok(mbar_wait_spin(smem_u32(&ctl->p_free[gs & 1]),
+                                                                   static_cast<uint32_t>((gs - 2) >> 1) & 1u));
+                    if (!w) {
+                        failed = true;
+                    } else {
+                        const int chunk = 4 * (gs & 1) + (lane >> 3);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float m_use = m_ref[i] == -INFINITY ? 0.f : m_ref[i];
+                            const float pi = fast_exp2(fmaf(s4[i], sl2, -m_use));
+                            l[i] += pi;
+                            const int hd = 4 * warp + i;
+                            asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_u32(pbuf) + hd * 128 + ((chunk ^ (hd & 7)) << 4) +
+                                                                         (lane & 7) * 2),
+                                         "h"(static_cast<unsigned short>(pack_bf16x2(pi, 0.f)))
+                                         : "memory");
                         }
                         fence_proxy_async_smem();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(smem_u32(&ctl->p_full[gs & 1]));
+                if (s == ns - 1 && !failed) {
+                    // the segment's (max, sum) per head, for the epilogue; the buffer's last
+                    // reader was the epilogue of segment k - 2
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) l[i] += __shfl_xor_sync(FULL_MASK, l[i], o);
+                    const bool w = k < 2 || all_ok(mbar_wait_bounded(smem_u32(&ctl->o_free[k & 1]),
+                                                                     static_cast<uint32_t>((k >> 1) - 1) & 1u));
+                    if (!w) {
+                        failed = true;
+                    } else {
+                        if (lane < 4) {
+                            ctl->lsum[k & 1][4 * warp + lane] = lane == 0 ? l[0] : lane == 1 ? l[1] : lane == 2 ? l[2] : l[3];
+                            ctl->mref[k & 1][4 * warp + lane] =
+                                lane == 0 ? m_ref[0] : lane == 1 ? m_ref[1] : lane == 2 ? m_ref[2] : m_ref[3];
+                        }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[gs & 1]));
+                        if (lane == 0) mbar_arrive(smem_u32(&ctl->ml_full[k & 1]));
                     }
                 }
             }
-            if (warp == 0 && lane < TN_H) {
-                ctl->lsum[h] = l;
-                ctl->mref[h] = m_ref;
-            }
-            if (named_barrier_or(1, TN_EPI, failed)) {
+            g += ns;
+        }
+        if (failed && lane == 0) {
+            atomicOr(p.err, KV_DEVERR_TIMEOUT);
+            ctl->abort_flag = 1;
+        }
+        grid_dependents_launch();
+    } else if (warp < 10) {
+        // ------------------------------------------------------------ epilogue
+        // warp 6 + i reads lane quarter (6 + i) & 3: latent rows 128 t + 32 q + lane of the
+        // four tiles, 16 heads each; a whole sequence's output in bf16, a piece of a cut one
+        // as its fp16 partial [piece][head][512] with (max, sum) per head
+        const int q4 = warp & 3;
+        const uint32_t lrow = tbase + (static_cast<uint32_t>(q4 * 32) << 16);
+        bool failed = false;
+        for (int k = 0;; ++k) {
+            const int slot = k % TN_NITEM;
+            // warp 6 alone polls (sleeping between polls: these waits last a segment); warps
+            // 7-9 wait at named barrier 3
+            bool bad = false;
+            if (warp == 6)
+                bad = !all_ok(mbar_wait_sleep(smem_u32(&ctl->item_full[slot]), static_cast<uint32_t>(k / TN_NITEM) & 1u));
+            if (named_barrier_or(3, TN_SOFT, bad)) {
                 failed = true;
                 break;
             }
-            // ---- warp 0 loads the next segment's queries first (its scores may then start
-            // while this segment's output is written); each warp then writes its quarter
-            // of the output.  A failure is passed on at the next segment's barrier.
-            if (warp == 0) {
-                const int nslot = (k + 1) % TN_NITEM;
-                const bool ok = all_ok(mbar_wait_bounded(smem_u32(&ctl->item_full[nslot]),
-                                                         static_cast<uint32_t>((k + 1) / TN_NITEM) & 1u));
-                if (!ok) {
-                    failed = true;
-                } else {
-                    const MlaSegment nx = ctl->items[nslot];
-                    if (nx.n >= 0) {
-                        load_queries(p, nx.b, nx.outer, lrow, smem_u32(smem), lane);
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&ctl->q_full));
-                    }
-                }
+            const MlaSegment item = ctl->items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->item_empty[slot]));
+            if (item.n < 0) break;
+            if (warp == 6) {
+                bool ok = mbar_wait_sleep(smem_u32(&ctl->o_full[k & 1]), static_cast<uint32_t>(k >> 1) & 1u);
+                if (ok) ok = mbar_wait_sleep(smem_u32(&ctl->ml_full[k & 1]), static_cast<uint32_t>(k >> 1) & 1u);
+                bad = !all_ok(ok);
             }
-            if (!failed && !all_ok(mbar_wait_bounded(smem_u32(&ctl->o_full), static_cast<uint32_t>(k) & 1u)))
+            if (named_barrier_or(3, TN_SOFT, bad || *abort_flag != 0)) {
                 failed = true;
-            if (failed) continue;                   // leaves at the next segment's barrier
+                break;
+            }
             tc_fence_after();
-            // ---- epilogue: latent rows 128 i + 32 warp + lane of the four tiles, 16 heads
-            // each; a whole sequence's output in bf16, a piece of a cut one as its fp32
-            // partial [piece][head][512] with (max, sum) per head
-            const bool whole = nsplit == 1;
-            const size_t piece = (static_cast<size_t>(b) * p.head_tiles + ht) * p.max_splits + split;
+            const int b = item.b, ht = item.outer;
+            const int nh = min(TN_H, p.q_heads - ht * TN_H);
+            const bool whole = item.nsplit == 1;
+            const size_t row0 = static_cast<size_t>(b) * p.q_heads + ht * TN_H;
+            const size_t piece = (static_cast<size_t>(b) * p.head_tiles + ht) * p.max_splits + item.split;
             float inv[TN_H];
 #pragma unroll
             for (int j = 0; j < TN_H; ++j) {
-                const float lj = ctl->lsum[j];
+                const float lj = ctl->lsum[k & 1][j];
                 inv[j] = lj > 0.f ? 1.f / lj : 0.f;
             }
+            const uint32_t ob = lrow + TN_O + TN_O_STRIDE * (k & 1);
 #pragma unroll 1
             for (int i = 0; i < 4; ++i) {
-                uint32_t r[32];
-                tc_ld32(lrow + TN_O + 32 * i, r);
+                uint32_t r[16];
+                tc_ld16(ob + 32 * i, r);
                 tc_wait_ld();
-                const int d = 128 * i + 32 * warp + lane;
+                const int d = 128 * i + 32 * q4 + lane;
                 if (whole) {
                     uint16_t* dst = p.out + row0 * MLA_DV + d;
 #pragma unroll
@@ -651,18 +715,22 @@ paged_mla_decode_tcn(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                         dst[j * MLA_DV] = static_cast<uint16_t>(pack_f16x2(__uint_as_float(r[j]) * inv[j], 0.f));
                 }
             }
+            float mj = 0.f, lj = 0.f;
+            if (warp == 6 && lane < TN_H) {
+                mj = ctl->mref[k & 1][lane];
+                lj = ctl->lsum[k & 1][lane];
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->o_free));
-            if (warp == 0 && lane < TN_H) {
-                const float mj = ctl->mref[h], lj = ctl->lsum[h];
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->o_free[k & 1]));
+            if (warp == 6 && lane < TN_H) {
                 if (!whole)
-                    reinterpret_cast<float2*>(p.part_ml)[piece * TN_H + h] = make_float2(mj, lj);
-                else if (p.lse != nullptr && h < nh)
-                    p.lse[row0 + h] = lse_from(mj, lj);
+                    reinterpret_cast<float2*>(p.part_ml)[piece * TN_H + lane] = make_float2(mj, lj);
+                else if (p.lse != nullptr && lane < nh)
+                    p.lse[row0 + lane] = lse_from(mj, lj);
             }
-            if (tid == 0 && p.tickets != nullptr) p.tickets[static_cast<size_t>(b) * p.head_tiles + ht] = nsplit;
-            g += n;
+            if (warp == 6 && lane == 0 && p.tickets != nullptr)
+                p.tickets[static_cast<size_t>(b) * p.head_tiles + ht] = item.nsplit;
         }
         if (failed && lane == 0) {
             atomicOr(p.err, KV_DEVERR_TIMEOUT);
@@ -751,12 +819,14 @@ cudaError_t prepare_mla_decode_tcn()
                                 TN_SMEM);
 }
 
-cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
-                                  cudaStream_t s)
+cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const CUtensorMap& tq,
+                                  const MlaParams& p, cudaStream_t s)
 {
     cudaError_t e = p.kv_new != nullptr
-                        ? launch_dependent(paged_mla_decode_tcn<true>, grid, dim3(TN_THREADS_STEP), TN_SMEM, s, tm, p)
-                        : launch_dependent(paged_mla_decode_tcn<false>, grid, dim3(TN_THREADS), TN_SMEM, s, tm, p);
+                        ? launch_dependent(paged_mla_decode_tcn<true>, grid, dim3(TN_THREADS_STEP), TN_SMEM, s,
+                                           tm, tq, p)
+                        : launch_dependent(paged_mla_decode_tcn<false>, grid, dim3(TN_THREADS), TN_SMEM, s, tm,
+                                           tq, p);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     return launch_dependent(paged_mla_merge_tcn, dim3(p.batch, p.head_tiles, MLA_DV / 128), dim3(256), 0, s, p);
 }

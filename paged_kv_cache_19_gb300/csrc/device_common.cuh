@@ -80,6 +80,49 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Non-blocking probe of the phase (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// As mbar_wait_bounded, for the waits on a pipeline's critical path: the thread polls
+// with test_wait, so it sees the completion within a few cycles instead of whenever a
+// suspended try_wait resumes.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
+                                               unsigned long long limit_ns = WAIT_LIMIT_NS)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// The same for waits expected to be long (a whole segment of work): the thread sleeps
+// `ns` between polls, so that its polls of the barrier's shared-memory word do not take
+// bandwidth from the other roles.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, unsigned ns = 128,
+                                                unsigned long long limit_ns = WAIT_LIMIT_NS)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ----------------------------------------------------------------- TMA
 // 5-D tiled bulk tensor load global -> shared, completion counted in bytes on
 // the mbarrier.  The destination CTA is the issuing one (a cluster of one).
@@ -91,6 +134,17 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
         "r"(bar)
+        : "memory");
+}
+
+// 3-D tiled bulk tensor load global -> shared (same completion as tma_load_5d).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 

@@ -183,15 +183,19 @@ constexpr int MLA_TC_BLOCK = 64;
 cudaError_t prepare_mla_decode_tc();
 cudaError_t launch_mla_decode_tc(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
                                  cudaStream_t s);
-// The narrow tcgen05 form: tiles of 16 heads (rows of an M = 64 score MMA), blocks of 64
-// tokens, one CTA per SM taking an equal contiguous range of the (head tile, sequence,
-// block) units; cut sequences are merged by a second kernel when max_splits > 1.
+// The narrow tcgen05 form: tiles of 16 heads (columns of the score MMAs, whose rows are
+// tokens), blocks of 64 tokens streamed as 32-token stages, one CTA per SM taking an equal
+// contiguous range of the (head tile, sequence, block) units; cut sequences are merged by
+// a second kernel when max_splits > 1.  tm: the latent pool's map with a box of one
+// 64-number piece of 32 slots; tq: the queries' map, dims (MLA_DK, q_heads, batch), a box
+// of one 64-number piece of min(16, q_heads) heads.
 // Partials: part_o [piece][16 heads][MLA_DV], part_ml [piece][16 heads] (max, sum),
 // piece = (sequence, head tile, split); tickets [batch, head_tiles] piece counts.
 constexpr int MLA_TCN_HEADS = 16;
+constexpr int MLA_TCN_STAGE_TOKENS = 32;
 cudaError_t prepare_mla_decode_tcn();
-cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const MlaParams& p,
-                                  cudaStream_t s);
+cudaError_t launch_mla_decode_tcn(dim3 grid, const CUtensorMap& tm, const CUtensorMap& tq,
+                                  const MlaParams& p, cudaStream_t s);
 cudaError_t launch_copy_blocks(const struct kv_block_copy* copies, int n, uint8_t* k_pool,
                                uint8_t* v_pool, size_t block_bytes, int num_blocks, uint32_t* err,
                                cudaStream_t s);

@@ -205,6 +205,25 @@ def test_tcgen05_batches_over_256_sequences(heads):
     st.destroy()
 
 
+@pytest.mark.parametrize("heads", [16, 128])
+def test_frequent_output_rescales(heads):
+    """A softmax scale of 1 spreads the scores so widely (standard deviation ~24) that a
+    head's running maximum keeps growing by more than 2^8 from one stage to the next:
+    the tensor-core forms' lazy output rescale then runs in many stages, each time for
+    some heads only, each head with its own factor."""
+    w = workloads.make(workloads.custom("mla_scale_1", batch=4, q_heads=heads, kv_heads=1,
+                                        head_dim=576, block_size=64, seed=219,
+                                        ctx=[70, 700, 2000, 3000], latent_dim=512,
+                                        qk_head_dim=1, split_tokens=1024))
+    assert w.scale == 1.0
+    st = Staged(w)
+    out, lse = st.mla()
+    torch.cuda.synchronize()
+    assert st.pool.device_errors() == 0
+    check(out, lse, w)
+    st.destroy()
+
+
 def test_copy_blocks_on_a_latent_pool():
     pool = kp.kv_mla_pool_create(6, 16)
     k, _ = pool.raw_bytes()
