@@ -35,6 +35,22 @@ struct MlaSegment {
     int outer, b, blk0, n, ctx, split, nsplit;
 };
 
+// Quotient and remainder of non-negative 64-bit values, by a 32-bit division when both
+// fit in 32 bits (the usual case: a 64-bit division is a long software sequence).
+__device__ __forceinline__ long long udiv_ll(long long a, long long b)
+{
+    if ((static_cast<unsigned long long>(a) | static_cast<unsigned long long>(b)) >> 32 == 0)
+        return static_cast<long long>(static_cast<unsigned>(a) / static_cast<unsigned>(b));
+    return a / b;
+}
+
+__device__ __forceinline__ long long umod_ll(long long a, long long b)
+{
+    if ((static_cast<unsigned long long>(a) | static_cast<unsigned long long>(b)) >> 32 == 0)
+        return static_cast<long long>(static_cast<unsigned>(a) % static_cast<unsigned>(b));
+    return a % b;
+}
+
 template <int TOK, int PAD>
 struct MlaPartition {
     const MlaParams* p;
@@ -52,7 +68,7 @@ struct MlaPartition {
     }
 
     // the CTA whose range holds unit x
-    __device__ __forceinline__ int cta_of(long long x) const { return static_cast<int>(((x + 1) * gact - 1) / T); }
+    __device__ __forceinline__ int cta_of(long long x) const { return static_cast<int>(udiv_ll((x + 1) * gact - 1, T)); }
 
     // Warp-wide (all 32 lanes): block count of the batch, the range of this CTA and the
     // sequences at its ends.  Out-of-range context lengths are flagged and clamped; an
@@ -66,7 +82,7 @@ struct MlaPartition {
         p = &params;
         cap = p->max_blocks * TOK;
         S = 0;
-        int ctxv[8], nbv[8], incl[8];
+        int ctxv[8], nbv[8], incl[8], tot[8];
         for (int b0 = 0; b0 < p->batch; b0 += 256) {
             int raw[8];                             // eight lengths per lane in flight
 #pragma unroll
@@ -83,62 +99,96 @@ struct MlaPartition {
                     x = x < 0 ? 0 : cap;
                 }
                 const int nb = (x + TOK - 1) / TOK;
-                const int wv = nb > 0 ? nb + PAD : 0;   // positions of the sequence
-                if (outputs && bb < p->batch && nb == 0 &&
-                    bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
-                    uint4* dst = reinterpret_cast<uint4*>(p->out + static_cast<size_t>(bb) * p->q_heads * MLA_DV);
-                    for (int v = 0; v < p->q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
-                    if (p->lse != nullptr)
-                        for (int hh = 0; hh < p->q_heads; ++hh) p->lse[static_cast<size_t>(bb) * p->q_heads + hh] = -INFINITY;
-                }
-                int in = wv;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(FULL_MASK, in, o);
-                    if (lane >= o) in += y;
-                }
                 ctxv[i] = x;
-                nbv[i] = wv;
-                incl[i] = in;
-                S += __shfl_sync(FULL_MASK, in, 31);
+                nbv[i] = nb > 0 ? nb + PAD : 0;     // positions of the sequence
+                incl[i] = nbv[i];
+            }
+            // inclusive prefix sums over the lanes, the eight slots' shuffle chains interleaved
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int y = __shfl_up_sync(FULL_MASK, incl[i], o);
+                    if (lane >= o) incl[i] += y;
+                }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                tot[i] = __shfl_sync(FULL_MASK, incl[i], 31);
+                S += tot[i];
+            }
+            if (outputs) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int bb = b0 + i * 32 + lane;
+                    if (bb < p->batch && nbv[i] == 0 &&
+                        bb % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+                        uint4* dst = reinterpret_cast<uint4*>(p->out + static_cast<size_t>(bb) * p->q_heads * MLA_DV);
+                        for (int v = 0; v < p->q_heads * (MLA_DV / 8); ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+                        if (p->lse != nullptr)
+                            for (int hh = 0; hh < p->q_heads; ++hh) p->lse[static_cast<size_t>(bb) * p->q_heads + hh] = -INFINITY;
+                    }
+                }
             }
         }
         T = S * nouter;
-        gact = T / p->split_blocks;
+        gact = udiv_ll(T, p->split_blocks);
         if (gact < 1) gact = 1;
         if (gact > gridDim.x) gact = gridDim.x;
         c = blockIdx.x;
-        u0 = c < gact ? c * T / gact : T;
-        u1 = c < gact ? (c + 1) * T / gact : T;
+        u0 = c < gact ? udiv_ll(c * T, gact) : T;
+        u1 = c < gact ? udiv_ll((c + 1) * T, gact) : T;
         int b_first = 0;
         long long pre_first = 0, pre_last = 0;
         b_last = 0;
         ctx_l = 0;
         if (u0 < u1) {
             if (p->batch <= 256) {
-                // both ends at once from the registers
-                const long long v0 = u0 % S, v1 = (u1 - 1) % S;
+                // both ends at once from the registers: the slots' offsets, then sixteen
+                // independent ballots, then the first slot past each end
+                const long long v0 = umod_ll(u0, S), v1 = umod_ll(u1 - 1, S);
+                long long off[8];
                 long long acc = 0;
-                bool f0 = false, f1 = false;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const unsigned p0 = __ballot_sync(FULL_MASK, acc + incl[i] > v0);
-                    const unsigned p1 = __ballot_sync(FULL_MASK, acc + incl[i] > v1);
-                    if (!f0 && p0 != 0u) {
-                        const int fl = __ffs(p0) - 1;
-                        b_first = i * 32 + fl;
-                        pre_first = acc + __shfl_sync(FULL_MASK, incl[i] - nbv[i], fl);
-                        f0 = true;
-                    }
-                    if (!f1 && p1 != 0u) {
-                        const int fl = __ffs(p1) - 1;
-                        b_last = i * 32 + fl;
-                        pre_last = acc + __shfl_sync(FULL_MASK, incl[i] - nbv[i], fl);
-                        ctx_l = __shfl_sync(FULL_MASK, ctxv[i], fl);
-                        f1 = true;
-                    }
-                    acc += __shfl_sync(FULL_MASK, incl[i], 31);
+                    off[i] = acc;
+                    acc += tot[i];
                 }
+                unsigned p0[8], p1[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p0[i] = __ballot_sync(FULL_MASK, off[i] + incl[i] > v0);
+                    p1[i] = __ballot_sync(FULL_MASK, off[i] + incl[i] > v1);
+                }
+                int i0 = 7, i1 = 7;
+#pragma unroll
+                for (int i = 7; i >= 0; --i) {
+                    if (p0[i] != 0u) i0 = i;
+                    if (p1[i] != 0u) i1 = i;
+                }
+                // the slot's values of the first lane past each end, picked without indexing
+                unsigned q0 = 0u, q1 = 0u;
+                long long o0 = 0, o1 = 0;
+                int e0 = 0, e1 = 0, c1 = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i == i0) {
+                        q0 = p0[i];
+                        o0 = off[i];
+                        e0 = incl[i] - nbv[i];
+                    }
+                    if (i == i1) {
+                        q1 = p1[i];
+                        o1 = off[i];
+                        e1 = incl[i] - nbv[i];
+                        c1 = ctxv[i];
+                    }
+                }
+                const int fl0 = __ffs(q0) - 1, fl1 = __ffs(q1) - 1;
+                b_first = i0 * 32 + fl0;
+                pre_first = o0 + __shfl_sync(FULL_MASK, e0, fl0);
+                b_last = i1 * 32 + fl1;
+                pre_last = o1 + __shfl_sync(FULL_MASK, e1, fl1);
+                ctx_l = __shfl_sync(FULL_MASK, c1, fl1);
             } else {
                 locate(u0, b_first, pre_first, lane);
                 locate(u1 - 1, b_last, pre_last, lane);
@@ -150,24 +200,24 @@ struct MlaPartition {
         outer_l = nb_l = 0;
         ub_l = 0;
         if (u0 < u1) {
-            outer_l = static_cast<int>((u1 - 1) / S);
+            outer_l = static_cast<int>(udiv_ll(u1 - 1, S));
             ub_l = static_cast<long long>(outer_l) * S + pre_last;
             ls = ub_l > u0 ? ub_l : u0;
             nb_l = (ctx_l + TOK - 1) / TOK;
         }
         last_done = !(u0 < u1);
         u = u0;
-        outer = u0 < u1 ? static_cast<int>(u0 / S) : 0;
+        outer = u0 < u1 ? static_cast<int>(udiv_ll(u0, S)) : 0;
         b = b_first;
         pre = pre_first;
-        blk = u0 < u1 ? static_cast<int>(u0 % S - pre_first) : 0;
+        blk = u0 < u1 ? static_cast<int>(umod_ll(u0, S) - pre_first) : 0;
     }
 
     // Warp-wide: the sequence holding position x < T, and the number of positions before
     // it (prefix sums, 32 sequences at a time).
     __device__ void locate(long long x, int& b_at, long long& pre_at, int lane) const
     {
-        const long long v = x % S;
+        const long long v = umod_ll(x, S);
         long long acc = 0;
         b_at = 0;
         pre_at = 0;
