@@ -11,7 +11,7 @@
 // Persistent: one CTA per SM holds its tensor memory for the whole launch and takes
 // one equal contiguous range of the units (latent half, head tile, sequence, block)
 // (mla_partition.cuh); a sequence cut by a range boundary leaves fp32 partials,
-// merged by paged_mla_merge_tc.  320 threads:
+// merged by paged_mla_merge_tc.  352 threads:
 //   * warp 8 walks the range's segments (item = a run of blocks of one sequence,
 //     head tile and half), passes each to the other roles through a 4-slot ring in
 //     shared memory, and streams its 64-token blocks, one per stage, with nine
@@ -21,17 +21,18 @@
 //     the rotary key) and the four pieces of this CTA's output half have
 //     barriers of their own: the first five are reloaded as soon as the scores
 //     of their stage are done, the other four once its output update is.
-//   * warp 9 (one thread) issues the MMAs.  Scores S[128 heads x 64 tokens] =
+//   * warp 9 (one thread) issues the score MMAs.  Scores S[128 heads x 64 tokens] =
 //     Q . C^T in 36 MMAs of K = 16: the 20 over the score-only pieces take A =
 //     the queries' matching 320 numbers held in tensor memory, the 16 over the
 //     output pieces (whose loads land last) take A = the other 256 numbers held
-//     in shared memory.  Then O[128 heads x 256 latent] += P . C[:, half]: A =
-//     the probabilities in tensor memory, B = the four output pieces read
-//     MN-major (the latent numbers of a token are contiguous), 4 MMAs of N =
-//     256.  Completion is signalled by tcgen05.commit on mbarriers.  A fixed
-//     order with blocking waits: the score-only MMAs of stage i+1 run while the
-//     softmax of stage i does, then the other score MMAs of stage i+1 with the
-//     output update of stage i spread among them.
+//     in shared memory.  Warp 10 (one thread) issues the output update
+//     O[128 heads x 256 latent] += P . C[:, half]: A = the probabilities in tensor
+//     memory, B = the four output pieces read MN-major (the latent numbers of a
+//     token are contiguous), 4 MMAs of N = 256.  Completion is signalled by
+//     tcgen05.commit on mbarriers.  With two issuing threads the scores of stage
+//     i+1 start as soon as the softmax has read those of stage i, and the update of
+//     stage i as soon as its probabilities are written; one thread issuing both in a
+//     fixed order made each wait for the other.
 //   * warps 0-7: head h (tensor-memory lane h) belongs to two threads, one in
 //     warp h / 32 (tokens 0-31 of a stage, output columns 0-127) and one in warp
 //     h / 32 + 4 (tokens 32-63, columns 128-255) -- a warp can only reach its
@@ -74,7 +75,7 @@ constexpr int TC_DQ = 256;                      // latent numbers per CTA
 constexpr int TC_M = 128;                       // heads per CTA
 constexpr int TC_QPIECE = TC_M * 128;           // one 64-number piece of 128 heads
 constexpr int TC_QS = TC_NLATE * TC_QPIECE;     // queries kept in shared memory
-constexpr int TC_THREADS = 320;                 // warps 0-7 softmax, 8 loads, 9 MMA
+constexpr int TC_THREADS = 352;                 // warps 0-7 softmax, 8 loads, 9 score MMAs, 10 output MMAs
 constexpr uint32_t TM_Q = 0, TM_S = 160, TM_P = 224, TM_O = 256, TM_COLS = 512;
 constexpr uint32_t IDESC_S = tc_idesc_bf16(TC_M, TC_TOK, 0, 0);
 constexpr uint32_t IDESC_O = tc_idesc_bf16(TC_M, TC_DQ, 0, 1);
@@ -106,7 +107,7 @@ struct TcCtl {
     uint64_t kv_full_l[TC_NSTAGE];                  // output pieces landed
     uint64_t kv_empty_e[TC_NSTAGE];                 // scores of the stage done
     uint64_t kv_empty_l[TC_NSTAGE];                 // output update of the stage done
-    uint64_t s_full, s_free, p_full, p_free, q_ready, mma_done;
+    uint64_t s_full, s_free, p_full, p_free, q_ready, mma_done[2];
     uint64_t item_full[TC_NITEM];
     uint64_t item_empty[TC_NITEM];
     uint32_t tmem_base;
@@ -146,27 +147,6 @@ __device__ __forceinline__ void issue_score_late(uint32_t tbase, uint32_t stage_
                   b0 + static_cast<uint64_t>(((ks >> 2) * TC_PIECE + (ks & 3) * 32) >> 4), IDESC_S, true);
 }
 
-// The scores over the output pieces with the previous stage's output update spread
-// among them: an N = 256 MMA issued between N = 64 ones costs the pipe far less than
-// the same MMA issued alone (measured on GB300).
-__device__ __forceinline__ void issue_score_late_and_output(uint32_t tbase, uint32_t stage_addr, uint32_t q_addr,
-                                                            uint32_t o_stage_addr, bool first)
-{
-    const uint64_t b0 = tc_smem_desc(stage_addr + TC_NEARLY * TC_PIECE, 16, 1024);
-    const uint64_t a0 = tc_smem_desc(q_addr, 16, 1024);
-    const uint64_t o0 = tc_smem_desc(o_stage_addr + TC_NEARLY * TC_PIECE, TC_PIECE, 1024);
-#pragma unroll
-    for (int ks = 0; ks < TC_NLATE * 4; ++ks) {
-        tc_mma_ss(tbase + TM_S, a0 + static_cast<uint64_t>(((ks >> 2) * TC_QPIECE + (ks & 3) * 32) >> 4),
-                  b0 + static_cast<uint64_t>(((ks >> 2) * TC_PIECE + (ks & 3) * 32) >> 4), IDESC_S, true);
-        if ((ks & 3) == 3) {
-            const int kk = ks >> 2;
-            tc_mma_ts(tbase + TM_O, tbase + TM_P + kk * 8, o0 + static_cast<uint64_t>((kk * 2048) >> 4), IDESC_O,
-                      !(first && kk == 0));
-        }
-    }
-}
-
 // The output update of a stage: O += P . C[:, half] over its 64 tokens; the four
 // output pieces are the N = 256 operand read MN-major (64-number atoms one piece
 // apart, 8-token groups 1 KB apart).
@@ -204,14 +184,15 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
         }
         for (int i = 0; i < TC_NITEM; ++i) {
             mbar_init(smem_u32(&ctl->item_full[i]), 1);
-            mbar_init(smem_u32(&ctl->item_empty[i]), 9);   // the MMA thread + 8 softmax warps
+            mbar_init(smem_u32(&ctl->item_empty[i]), 10);  // the two MMA threads + 8 softmax warps
         }
         mbar_init(smem_u32(&ctl->s_full), 1);
         mbar_init(smem_u32(&ctl->s_free), 8);
         mbar_init(smem_u32(&ctl->p_full), 8);
         mbar_init(smem_u32(&ctl->p_free), 1);
         mbar_init(smem_u32(&ctl->q_ready), 8);
-        mbar_init(smem_u32(&ctl->mma_done), 1);
+        mbar_init(smem_u32(&ctl->mma_done[0]), 1);
+        mbar_init(smem_u32(&ctl->mma_done[1]), 1);
         mbar_init(smem_u32(&ctl->step_done), 31);   // lanes 1-31 of the producer warp
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -349,9 +330,17 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
             if (p.kv_new != nullptr) part.write_step_rows(smem_u32(&ctl->step_done), lane - 1, 31);
         }
         grid_dependents_launch();
-    } else if (warp == 9) {
+    } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------------------ MMA issue
+        // Two issuing threads: warp 9 the scores of each stage, as soon as it has landed
+        // and the softmax has read the scores before (one score buffer); warp 10 the output
+        // update of each stage, as soon as its probabilities are written.  The update of a
+        // stage reads the probabilities and this half's pieces, the scores the queries and
+        // all nine pieces: the two touch different tensor memory, and an item's first
+        // update waits for its queries, which the softmax threads load only after their
+        // epilogue has read the output of the item before.
         if (lane == 0) {
+            const bool scores = warp == 9;
             const uint32_t q_addr = smem_u32(qsm);
             bool ok = true;
             int g = 0;                              // stages processed (all items)
@@ -369,6 +358,18 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     const int st = gs % TC_NSTAGE;
                     const uint32_t ph = static_cast<uint32_t>(gs / TC_NSTAGE) & 1u;
                     const uint32_t stage_addr = smem_u32(smem + st * TC_STAGE);
+                    if (!scores) {
+                        ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs) & 1u);
+                        if (!ok || *abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_output_mma(tbase, stage_addr, s == 0);
+                        tc_commit(smem_u32(&ctl->p_free));
+                        tc_commit(smem_u32(&ctl->kv_empty_l[st]));
+                        continue;
+                    }
                     ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_e[st]), ph);
                     // the score buffer is free once the softmax has read the stage before
                     if (ok && gs >= 1) ok = mbar_wait_bounded(smem_u32(&ctl->s_free), static_cast<uint32_t>(gs - 1) & 1u);
@@ -378,38 +379,14 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     }
                     tc_fence_after();
                     issue_score_early(tbase, stage_addr);
-                    // then the scores over the output pieces (their loads, issued once the
-                    // previous update had finished with the slot two stages back) with the
-                    // previous stage's output update spread among them; both waits block
-                    // (try_wait) rather than poll
-                    if (s >= 1)
-                        ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs - 1) & 1u);
-                    if (ok) ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_l[st]), ph);
+                    // then the scores over this half's pieces (their loads, issued once the
+                    // update of the stage two back had finished with the slot)
+                    ok = mbar_wait_bounded(smem_u32(&ctl->kv_full_l[st]), ph);
                     if (!ok) break;
                     tc_fence_after();
-                    if (s >= 1) {
-                        issue_score_late_and_output(tbase, stage_addr, q_addr,
-                                                    smem_u32(smem + ((gs - 1) % TC_NSTAGE) * TC_STAGE), s == 1);
-                        tc_commit(smem_u32(&ctl->s_full));
-                        tc_commit(smem_u32(&ctl->kv_empty_e[st]));
-                        tc_commit(smem_u32(&ctl->p_free));
-                        tc_commit(smem_u32(&ctl->kv_empty_l[(gs - 1) % TC_NSTAGE]));
-                    } else {
-                        issue_score_late(tbase, stage_addr, q_addr);
-                        tc_commit(smem_u32(&ctl->s_full));
-                        tc_commit(smem_u32(&ctl->kv_empty_e[st]));
-                    }
-                }
-                if (ok && n >= 1) {
-                    // the item's last output update, before the next item's queries
-                    const int gl = g + n - 1;
-                    ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gl) & 1u);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_output_mma(tbase, smem_u32(smem + (gl % TC_NSTAGE) * TC_STAGE), n == 1);
-                        tc_commit(smem_u32(&ctl->p_free));
-                        tc_commit(smem_u32(&ctl->kv_empty_l[gl % TC_NSTAGE]));
-                    }
+                    issue_score_late(tbase, stage_addr, q_addr);
+                    tc_commit(smem_u32(&ctl->s_full));
+                    tc_commit(smem_u32(&ctl->kv_empty_e[st]));
                 }
                 g += n;
             }
@@ -418,8 +395,9 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                 ctl->abort_flag = 1;
             }
             // every MMA issued must be complete before the tensor memory is freed
-            tc_commit(smem_u32(&ctl->mma_done));
-            mbar_wait_bounded(smem_u32(&ctl->mma_done), 0);
+            const uint32_t done = smem_u32(&ctl->mma_done[scores ? 0 : 1]);
+            tc_commit(done);
+            mbar_wait_bounded(done, 0);
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
