@@ -292,7 +292,7 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     ge = g + 1;
                     // output pieces: free once that stage's output update is done (its
                     // softmax, which reads stage_blk, is then over too)
-                    if (!mbar_wait_bounded(smem_u32(&ctl->kv_empty_l[st]), ph) || *abort_flag) {
+                    if (!mbar_wait_spin(smem_u32(&ctl->kv_empty_l[st]), ph) || *abort_flag) {
                         ok = false;
                         break;
                     }
@@ -359,7 +359,9 @@ paged_mla_decode_tc(const __grid_constant__ CUtensorMap tmp, const MlaParams p)
                     const uint32_t ph = static_cast<uint32_t>(gs / TC_NSTAGE) & 1u;
                     const uint32_t stage_addr = smem_u32(smem + st * TC_STAGE);
                     if (!scores) {
-                        ok = mbar_wait_bounded(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs) & 1u);
+                        // polled without suspending: this update frees the slot of this half's
+                        // pieces, whose reload the scores two stages on wait for
+                        ok = mbar_wait_spin(smem_u32(&ctl->p_full), static_cast<uint32_t>(gs) & 1u);
                         if (!ok || *abort_flag) {
                             ok = false;
                             break;
